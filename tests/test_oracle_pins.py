@@ -1,0 +1,399 @@
+"""Pins for the CPU oracle: each test checks it against something other than
+itself -- numbers the ZeRO pages print, closed forms, IEEE-defined
+rounding vectors, brute force on tiny inputs and a high-precision
+re-evaluation of Adam -- so that a dropped term, a wrong sign or index, or
+a transposed operand in the oracle fails at least one of them."""
+
+import json
+import math
+import os
+from decimal import Decimal, getcontext
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "page_tables.json")
+
+
+def _tables():
+    with open(GOLDEN) as f:
+        return json.load(f)
+
+
+def _close_to_printed(value: Fraction, printed: str) -> bool:
+    d = Decimal(printed)
+    decimals = max(0, -d.as_tuple().exponent)
+    half = Fraction(1, 2 * 10 ** decimals)
+    return abs(value - Fraction(printed)) <= half
+
+
+# ---------------------------------------------------------------- partition
+@pytest.mark.parametrize("align", [1, 2, 8])
+@pytest.mark.parametrize("n", [1, 2, 3, 4])
+def test_partition_brute_force(n, align):
+    for psi in range(0, 65):
+        p = O.partition(psi, n, align)
+        unit = n * align
+        # smallest multiple of N*align that is >= psi, found by search
+        want = 0
+        while want < psi:
+            want += unit
+        assert p.psi_pad == want
+        assert p.shard * n == p.psi_pad
+        owner = [-1] * p.psi_pad
+        for r, (off, real) in enumerate(zip(p.offsets, p.real)):
+            assert off == r * p.shard
+            for i in range(off, off + p.shard):
+                assert owner[i] == -1
+                owner[i] = r
+            assert real == sum(1 for i in range(off, off + p.shard) if i < psi)
+        assert all(o >= 0 for o in owner)
+        assert sum(p.real) == psi
+
+
+def test_partition_toy_numbers():
+    p = O.partition(637824, 32, 8)
+    assert (p.psi_pad, p.shard) == (637952, 19936)
+    assert p.real[-1] == 637824 - 31 * 19936 == 19808
+
+
+# ---------------------------------------------------------------- accounting
+def test_model_state_tables_printed_on_pages():
+    for row in _tables()["model_state"]:
+        psi = row["psi"]
+        if row.get("padded"):
+            psi = O.partition(psi, row["n"], row["align"]).psi_pad
+        b = O.model_state_bytes(psi, row["n"], row["stage"])
+        assert _close_to_printed(Fraction(b, row["unit_bytes"]), row["printed"]), row
+
+
+def test_unpadded_toy_would_not_print_156():
+    # The padding reading: without it ZeRO-2 at N = 32 would print 1.55 MB.
+    b = O.model_state_bytes(637824, 32, 2)
+    assert not _close_to_printed(Fraction(b, 10 ** 6), "1.56")
+
+
+def test_bytes_per_param_at_32():
+    for row in _tables()["bytes_per_param_at_n32"]:
+        b = O.model_state_bytes(32 * 1000, 32, row["stage"])
+        assert _close_to_printed(Fraction(b, 32 * 1000), row["printed"]), row
+
+
+def test_table1_model_sizes_fit_32gb():
+    for row in _tables()["fits_32gb_table1"]:
+        assert O.model_state_bytes(row["psi"], row["n"], row["stage"]) <= row["capacity_bytes"]
+
+
+def test_exact_formulas_on_integers():
+    for n in (1, 2, 4, 8, 64):
+        psi = n * 1000
+        assert O.model_state_bytes(psi, n, 0) == 16 * psi
+        assert O.model_state_bytes(psi, n, 1) * n == 4 * psi * n + 12 * psi
+        assert O.model_state_bytes(psi, n, 2) * n == 2 * psi * n + 14 * psi
+        assert O.model_state_bytes(psi, n, 3) * n == 16 * psi
+    # at N = 1 every stage holds everything
+    assert len({O.model_state_bytes(800, 1, s) for s in range(4)}) == 1
+
+
+def test_comm_ring_printed():
+    for row in _tables()["comm_ring_per_psi"]:
+        n, psi = row["n"], row["n"] * 10 ** 6
+        if row["model"] == "ring":
+            e = O.comm_elems_ring(psi, n, row["stage"])
+        else:
+            e = O.comm_elems_ring_allreduce_zero1(psi, n)
+        assert _close_to_printed(Fraction(e, psi), row["printed"]), row
+
+
+def test_comm_paper_printed():
+    for row in _tables()["comm_paper_bytes"]:
+        e = O.comm_elems_paper(row["psi"], row["stage"])
+        gb = Fraction(2 * e, 10 ** 9)
+        assert _close_to_printed(gb, row["printed_gb"])
+        assert _close_to_printed(gb / 50, row["printed_s_at_50gbs"])
+    # 1.5x for stage 3 against the DP baseline (ZeRO summary Sec. 7)
+    assert Fraction(O.comm_elems_paper(10, 3), O.comm_elems_paper(10, 0)) == Fraction(3, 2)
+
+
+def test_ring_stage3_cell_is_the_documented_gap():
+    row = _tables()["not_reproduced"][0]
+    e = O.comm_elems_ring(32 * 10 ** 6, 32, 3)
+    assert not _close_to_printed(Fraction(e, 32 * 10 ** 6), "2.89"), row
+    assert Fraction(e, 32 * 10 ** 6) == Fraction(93, 32)
+
+
+# ---------------------------------------------------------------- 16-bit rounding
+FP16_VECTORS = [
+    # (fp32 value, expected binary16 bits), from the IEEE 754 binary16 layout
+    (1.0, 0x3C00), (-2.0, 0xC000), (0.0, 0x0000), (-0.0, 0x8000),
+    (65504.0, 0x7BFF), (65519.99609375, 0x7BFF), (65520.0, 0x7C00),
+    (1e10, 0x7C00), (-1e10, 0xFC00),
+    (2.0 ** -24, 0x0001), (2.0 ** -25, 0x0000),            # tie -> even (zero)
+    (3 * 2.0 ** -25, 0x0002),                              # tie -> even (2 ulp)
+    (1 + 2.0 ** -11, 0x3C00), (1 + 3 * 2.0 ** -11, 0x3C02),  # ties
+    (1 + 2.0 ** -11 + 2.0 ** -20, 0x3C01),                 # above the tie
+    (2.0 ** -14, 0x0400), (2.0 ** -14 - 2.0 ** -24, 0x03FF),
+]
+BF16_VECTORS = [
+    (1.0, 0x3F80), (-1.0, 0xBF80), (0.0, 0x0000), (-0.0, 0x8000),
+    (1 + 2.0 ** -8, 0x3F80), (1 + 3 * 2.0 ** -8, 0x3F82), (1 + 2.0 ** -8 + 2.0 ** -20, 0x3F81),
+    (3.4028234663852886e38, 0x7F80),                       # above bf16 max -> inf
+    ((2 - 2.0 ** -7) * 2.0 ** 127, 0x7F7F),
+    (2.0 ** -149, 0x0000), (2.0 ** -133, 0x0001),
+    (float("inf"), 0x7F80), (float("-inf"), 0xFF80),
+]
+
+
+def test_rne16_fp16_vectors():
+    x = np.array([v for v, _ in FP16_VECTORS], np.float32)
+    got = O.rne16(x, O.FP16)
+    assert [int(b) for b in got] == [b for _, b in FP16_VECTORS]
+
+
+def test_rne16_bf16_vectors():
+    x = np.array([v for v, _ in BF16_VECTORS], np.float32)
+    got = O.rne16(x, O.BF16)
+    assert [int(b) for b in got] == [b for _, b in BF16_VECTORS]
+    nan = O.rne16(np.array([np.nan], np.float32), O.BF16)[0]
+    assert (int(nan) & 0x7F80) == 0x7F80 and (int(nan) & 0x007F) != 0
+
+
+def test_widen16_exact_roundtrip():
+    bits = np.arange(0, 1 << 16, dtype=np.uint32).astype(np.uint16)
+    for dt in (O.FP16, O.BF16):
+        w = O.widen16(bits, dt)
+        finite = np.isfinite(w)
+        back = O.rne16(w[finite], dt)
+        assert np.array_equal(back, bits[finite])
+    # spot values from the formats' definitions
+    assert O.widen16(np.array([0x3C00], np.uint16), O.FP16)[0] == 1.0
+    assert O.widen16(np.array([0x0001], np.uint16), O.FP16)[0] == 2.0 ** -24
+    assert O.widen16(np.array([0x3F80], np.uint16), O.BF16)[0] == 1.0
+
+
+# ---------------------------------------------------------------- hand-worked tiny case
+def _bits(vals, dt):
+    return O.rne16(np.array(vals, np.float32), dt)
+
+
+def _tiny_grads(dt):
+    g0 = [1, 2, -1, 0.5, 4, 0, 0, 0]
+    g1 = [3, 2, -3, -2.5, 0, 0, 0, 0]
+    return np.stack([_bits(g0, dt), _bits(g1, dt)])
+
+
+@pytest.mark.parametrize("dt", [O.FP16, O.BF16])
+@pytest.mark.parametrize("stage", [0, 1, 2, 3])
+def test_tiny_case_by_hand(stage, dt):
+    # psi = 5, N = 2, align = 2: psi_pad = 8, shard 4, offsets [0, 4], real [4, 1].
+    # sums [4, 4, -4, -2, 4] -> g_hat = sums / 2 = [2, 2, -2, -1, 2]; |g_hat|^2 = 17.
+    # Adam t = 1, lr = 2^-6, b1 = 0.5, b2 = 0.75, eps = 0: every update is
+    # lr * sign(g_hat), all exact in fp32 and in both 16-bit formats.
+    part = O.partition(5, 2, 2)
+    assert (part.psi_pad, part.shard, part.offsets, part.real) == (8, 4, (0, 4), (4, 1))
+    h = O.Hyper(lr=2.0 ** -6, beta1=0.5, beta2=0.75, eps=0.0)
+    p0 = [0.5, 0.25, 0.0, -0.5, 1.0]
+    st = O.init_state(stage, dt, part, np.array(p0, np.float32))
+    buckets = [(0, 3), (3, 8)] if stage == 3 else None
+    new, res = O.step(st, _tiny_grads(dt), h, buckets)
+    want = np.array([0.484375, 0.234375, 0.015625, -0.484375, 0.984375], np.float32)
+    assert res.applied and not res.overflow
+    assert res.norm == math.sqrt(17.0)
+    master = new.master[0] if stage == 0 else new.master
+    assert np.array_equal(master[:5], want)
+    assert np.all(master[5:] == 0)
+    qs = new.params if stage == 3 else new.params[0]
+    assert np.array_equal(O.widen16(qs[:5], dt), want)
+    if stage != 3:
+        assert np.array_equal(new.params[0], new.params[1])
+    else:
+        # the gathers hand every rank the owners' 16-bit values of the bucket
+        before = O.rne16(np.array(p0 + [0, 0, 0], np.float32), dt)
+        assert np.array_equal(res.gathered_fwd[0][1], before[0:3])
+        assert np.array_equal(res.gathered_bwd[1][0], before[3:8])
+
+
+# ---------------------------------------------------------------- equivalence
+def _random_case(seed, psi, n, dt, scale=1.0, sigma=1e-2):
+    rng = np.random.default_rng(seed)
+    part = O.partition(psi, n, 8)
+    master = rng.normal(0, 0.02, psi).astype(np.float32)
+    m = rng.normal(0, 1e-4, psi).astype(np.float32)
+    v = np.abs(rng.normal(0, 1e-6, psi)).astype(np.float32)
+    grads = []
+    for _ in range(3):
+        g = np.zeros((n, part.psi_pad), np.float32)
+        g[:, :psi] = rng.normal(0, sigma, (n, psi)) * scale
+        grads.append(O.rne16(g, dt))
+    return part, master, m, v, grads
+
+
+@pytest.mark.parametrize("dt", [O.FP16, O.BF16])
+def test_all_stages_identical(dt):
+    # "zero-stages-simulation" README: every stage produced identical trained weights.
+    n, psi = 4, 1001
+    part, master, m, v, grads = _random_case(1, psi, n, dt)
+    h = O.Hyper(lr=1e-3, weight_decay=0.1, max_norm=0.05)
+    finals = []
+    for stage in range(4):
+        st = O.init_state(stage, dt, part, master, m, v)
+        for k in range(3):
+            buckets = [(0, 96), (96, 640), (640, part.psi_pad)] if stage == 3 else None
+            st, res = O.step(st, grads[k], h, buckets)
+            assert res.applied
+        finals.append(st)
+    ref = finals[1]
+    for st in finals:
+        mm = st.master[0] if st.stage == 0 else st.master
+        assert np.array_equal(mm.view(np.uint32), ref.master.view(np.uint32))
+        q = st.params if st.stage == 3 else st.params[0]
+        assert np.array_equal(q, ref.params[0])
+    s0 = finals[0]
+    for r in range(n):
+        assert np.array_equal(s0.master[r], s0.master[0])
+        assert np.array_equal(s0.m[r], s0.m[0])
+        assert np.array_equal(s0.params[r], s0.params[0])
+
+
+def test_all_reduce_is_reduce_scatter_then_all_gather():
+    # CMU 11-868 notes, exercise 3: all-reduce == reduce-scatter + all-gather.
+    rng = np.random.default_rng(7)
+    part = O.partition(77, 4, 2)
+    g = [rng.normal(0, 1, part.psi_pad).astype(np.float32) for _ in range(4)]
+    ar = O.all_reduce_mean(g, 4, 8.0)
+    ag = O.all_gather(O.reduce_scatter_mean(g, part, 8.0))
+    for r in range(4):
+        assert np.array_equal(ar[r], ag)
+
+
+def test_replicas_equal_cast_of_master():
+    part, master, m, v, grads = _random_case(3, 333, 3, O.BF16)
+    st = O.init_state(2, O.BF16, part, master, m, v)
+    for k in range(3):
+        st, _ = O.step(st, grads[k], O.Hyper())
+        for r in range(3):
+            assert np.array_equal(st.params[r], O.rne16(st.master, O.BF16))
+
+
+# ---------------------------------------------------------------- Adam closed forms
+def test_adam_step1_is_lr_times_sign():
+    # Step 1 of Adam with eps = 0 moves every weight by lr * sign(g) (Kingma & Ba).
+    # Dyadic inputs keep every fp32 operation exact; b1 != 1 - b1 and b2 != 1 - b2
+    # so a swapped coefficient would show.
+    rng = np.random.default_rng(11)
+    k = 4096
+    g = (rng.integers(1, 64, k) * rng.choice([-1, 1], k)).astype(np.float32) * np.float32(2.0 ** -10)
+    p0 = (rng.integers(-512, 512, k)).astype(np.float32) * np.float32(2.0 ** -9)
+    for b1, b2 in ((0.75, 0.9375), (0.5, 0.75), (0.875, 0.984375)):
+        sc = O.step_scalars(O.Hyper(lr=2.0 ** -7, beta1=b1, beta2=b2, eps=0.0), 1)
+        p1, m1, v1 = O.adam_update(p0, np.zeros(k, np.float32), np.zeros(k, np.float32), g, sc)
+        assert np.array_equal(p1, p0 - np.float32(2.0 ** -7) * np.sign(g))
+        assert np.array_equal(m1, np.float32(1 - b1) * g)
+        assert np.array_equal(v1, np.float32(1 - b2) * g * g)
+
+
+def test_zero_gradient_only_decays():
+    sc = O.step_scalars(O.Hyper(lr=1e-2, weight_decay=0.5, eps=1e-8), 3)
+    p0 = np.linspace(-1, 1, 101).astype(np.float32)
+    z = np.zeros_like(p0)
+    p1, m1, v1 = O.adam_update(p0, z, z, z, sc)
+    assert np.array_equal(p1, p0 * np.float32(1 - 1e-2 * np.float32(0.5)))
+    assert not np.any(m1) and not np.any(v1)
+
+
+def _hp_adam(p, m, v, g, h, t):
+    """Kingma & Ba AdamW in 60-digit decimal arithmetic, textbook form:
+    p <- p(1 - lr wd); m <- b1 m + (1-b1) g; v <- b2 v + (1-b2) g^2;
+    p <- p - lr * (m / (1-b1^t)) / (sqrt(v / (1-b2^t)) + eps)."""
+    getcontext().prec = 60
+    D = lambda x: Decimal(float(np.float32(x)))
+    lr, b1, b2, eps, wd = D(h.lr), D(h.beta1), D(h.beta2), D(h.eps), D(h.weight_decay)
+    p, m, v, g = Decimal(float(p)), Decimal(float(m)), Decimal(float(v)), Decimal(float(g))
+    p = p * (1 - lr * wd)
+    m = b1 * m + (1 - b1) * g
+    v = b2 * v + (1 - b2) * g * g
+    mhat = m / (1 - b1 ** t)
+    vhat = v / (1 - b2 ** t)
+    upd = lr * mhat / (vhat.sqrt() + eps)
+    return p - upd, m, v, upd
+
+
+def test_adam_against_high_precision():
+    rng = np.random.default_rng(5)
+    u = 2.0 ** -24
+    for t in (1, 2, 7, 1000):
+        h = O.Hyper(lr=3e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.05)
+        sc = O.step_scalars(h, t)
+        k = 300
+        p = rng.normal(0, 0.02, k).astype(np.float32)
+        m = rng.normal(0, 1e-3, k).astype(np.float32)
+        v = np.abs(rng.normal(0, 1e-5, k)).astype(np.float32)
+        g = rng.normal(0, 1e-2, k).astype(np.float32)
+        p1, m1, v1 = O.adam_update(p, m, v, g, sc)
+        for i in range(k):
+            pe, me, ve, upd = _hp_adam(p[i], m[i], v[i], g[i], h, t)
+            ulp_p = float(np.spacing(np.abs(np.float32(pe))))
+            assert abs(Decimal(float(p1[i])) - pe) <= Decimal(2 * ulp_p) + abs(upd) * Decimal(16 * u)
+            mag_m = abs(Decimal(float(np.float32(h.beta1))) * Decimal(float(m[i]))) + abs(Decimal(float(g[i])) / 10)
+            assert abs(Decimal(float(m1[i])) - me) <= mag_m * Decimal(4 * u)
+            assert abs(Decimal(float(v1[i])) - ve) <= abs(ve) * Decimal(4 * u) + Decimal(float(g[i]) ** 2) * Decimal(4 * u)
+
+
+# ---------------------------------------------------------------- overflow / norm / clip
+@pytest.mark.parametrize("bad", [np.inf, -np.inf, np.nan])
+@pytest.mark.parametrize("stage", [0, 1, 2, 3])
+def test_overflow_skips_step_and_halves_scale(stage, bad):
+    part, master, m, v, grads = _random_case(9, 200, 4, O.FP16, scale=1024.0)
+    st = O.init_state(stage, O.FP16, part, master, m, v, loss_scale=1024.0)
+    st.t = 5
+    g = grads[0].copy()
+    g[2, 123] = O.rne16(np.array([bad], np.float32), O.FP16)[0]
+    new, res = O.step(st, g, O.Hyper())
+    assert res.overflow and not res.applied
+    assert new.loss_scale == 512.0 and new.t == 5
+    for a, b in ((new.master, st.master), (new.m, st.m), (new.v, st.v), (new.params, st.params)):
+        assert a.tobytes() == b.tobytes()
+
+
+def test_overflow_in_padding_is_ignored_and_scale_floor():
+    part = O.partition(10, 2, 8)
+    st = O.init_state(1, O.FP16, part, np.ones(10, np.float32), loss_scale=1.0)
+    g = np.zeros((2, part.psi_pad), np.uint16)
+    g[1, 12] = 0x7C00  # +inf in padding: ignored
+    new, res = O.step(st, g, O.Hyper(eps=1e-8))
+    assert res.applied
+    g[1, 3] = 0x7C00
+    new2, res2 = O.step(new, g, O.Hyper())
+    assert res2.overflow and new2.loss_scale == 1.0
+
+
+def test_norm_of_constant_gradient():
+    # all-equal averaged gradient c over psi = 64 elements: norm = |c| * 8
+    part = O.partition(64, 4, 8)
+    g = np.full((4, part.psi_pad), O.rne16(np.array([-0.375], np.float32), O.FP16)[0], np.uint16)
+    st = O.init_state(2, O.FP16, part, np.zeros(64, np.float32))
+    _, res = O.step(st, g, O.Hyper(eps=1e-8))
+    assert res.norm == 0.375 * 8
+
+
+def test_clip_scales_gradient_to_max_norm():
+    part, master, m, v, grads = _random_case(13, 500, 2, O.FP16)
+    h_free = O.Hyper(beta1=0.75, eps=1e-8)
+    st = O.init_state(2, O.FP16, part, master)
+    _, res = O.step(st, grads[0], h_free)
+    norm = res.norm
+    assert res.clip is None
+    h_clip = O.Hyper(beta1=0.75, eps=1e-8, max_norm=norm / 4)
+    new, res2 = O.step(st, grads[0], h_clip)
+    assert res2.clip is not None
+    c = float(np.float32(norm / 4)) / (norm + 1e-6)   # max_norm / (norm + 1e-6)
+    assert abs(float(res2.clip) - c) <= 2.0 ** -24 * c
+    # m after step 1 from m = 0 is (1 - b1) * c * g_hat: its norm is 0.25 * c * norm
+    m_norm = float(np.sqrt(np.sum(new.m.astype(np.float64) ** 2)))
+    assert abs(m_norm - 0.25 * c * norm) <= 1e-6 * m_norm
+    # max_norm above the norm: no clipping
+    _, res3 = O.step(st, grads[0], O.Hyper(beta1=0.75, eps=1e-8, max_norm=norm * 2))
+    assert res3.clip is None
