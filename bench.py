@@ -1,0 +1,364 @@
+#!/usr/bin/env python3
+"""Throughput of the fused partitioned mixed-precision ZeRO step on GB300.
+
+Default workload: flat psi = 1.5e9 parameters, N = 8 simulated ranks, stage 1
+(P_os), fp16 gradients N(0, 1e-3^2) x loss scale 2^16, warm m/v, four grad
+sets cycled (the third carries one +inf in rank 5, so every fourth step is
+the overflow-skip path).  One bench step = one zero_step call over one set:
+reduce-scatter + unscale + overflow flag + global norm + AdamW + cast +
+all-gather into 8 replicas, all inputs resident in HBM (84 GB per step, far
+larger than L2).
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
+a bounded slab of the same workload instead (it needs no GPU).
+Other workloads (``--workload toy|gpt2|llama7b|sweep``) print lines of the
+same form for the tables in the docs.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "params/sec of fused ZeRO step at N ranks; achieved HBM GB/s vs GB300 peak"
+RESULT_BYTES = 56   # sizeof(zero_result_t)
+
+
+# ---------------------------------------------------------------- environment
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("zero_kernels.cu", "zero_internal.h"):
+        with open(os.path.join(ROOT, "zero_partitioned_mixed_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(summary: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on this kernel source."""
+    path = os.path.join(ROOT, "profiles", summary)
+    try:
+        txt = open(path).read()
+    except OSError:
+        return None
+    src = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", txt)
+    val = re.search(r"dram_bytes_per_launch_full_size:\s*([0-9.eE+]+)", txt)
+    if not src or not val or src.group(1) != kernel_source_hash():
+        return None
+    return float(val.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.dev = device_index
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.dev)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.samples = []
+        if self.proc is None:
+            return False
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append(parts)
+        return False
+
+    def summary(self):
+        if not getattr(self, "samples", None):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        sm = [float(p[1]) for p in self.samples if p[1].replace(".", "").isdigit()]
+        mx = [float(p[2]) for p in self.samples if p[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in self.samples for i in range(4) if p[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.samples)}
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+def oracle_timing(psi_sample: int, n: int, stage: int, dtype: str, steps: int, warmup: int,
+                  budget_s: float = None):
+    """Time the oracle's step on a slab of psi_sample elements (numpy, one core)."""
+    import numpy as np
+    import oracle as O
+    rng = np.random.default_rng(0)
+    part = O.partition(psi_sample, n, 8)
+    master = rng.normal(0, 0.02, psi_sample).astype(np.float32)
+    m = rng.normal(0, 1e-4, psi_sample).astype(np.float32)
+    v = np.abs(rng.normal(0, 1e-6, psi_sample)).astype(np.float32)
+    st = O.init_state(stage, dtype, part, master, m, v, loss_scale=65536.0)
+    g = np.zeros((n, part.psi_pad), np.float32)
+    g[:, :psi_sample] = rng.normal(0, 1e-3, (n, psi_sample)) * 65536.0
+    gb = O.rne16(g, dtype)
+    h = O.Hyper()
+    for _ in range(warmup):
+        st, _ = O.step(st, gb, h)
+    times = []
+    t_start = time.perf_counter()
+    for i in range(steps):
+        t0 = time.perf_counter()
+        st, _ = O.step(st, gb, h)
+        times.append(time.perf_counter() - t0)
+        if budget_s is not None and time.perf_counter() - t_start > budget_s and i >= 2:
+            break
+    total = sum(times)
+    return {"value": psi_sample * len(times) / total, "steps": len(times), "seconds": total,
+            "ms_per_step": 1e3 * total / len(times)}
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return 0
+    psi_s = 1 << 20
+    r = oracle_timing(psi_s, 8, 1, "fp16", args.steps, args.warmup)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": r["value"], "unit": "params/s",
+        "n_gpus": ws, "steps": r["steps"], "warmup": args.warmup, "ms_per_step": r["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": "flat_psi1.5e9_n8_stage1_fp16_ls65536", "n_ranks": 8, "stage": 1,
+                   "parallelism": "replicas only"},
+        "cpu_baseline": {"value": r["value"], "unit": "params/s", "cores": 1, "kind": "oracle",
+                         "sample": f"oracle stage-1 step on a slab of {psi_s} parameters x 8 ranks "
+                                   "(numpy, one thread), same distributions as the workload"},
+        "e2e": {"value": r["value"], "unit": "params/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- GPU workloads
+def setup_flat15b(Z, S, torch):
+    """Buffers and four resident gradient sets of the 1.5B stage-1 workload."""
+    from zero_partitioned_mixed_gb300.buffers import RankBuffers
+    w = S.FLAT15B
+    buf = RankBuffers(w.psi, w.n_ranks, w.stage, w.dtype, double_buffer=True, alloc_grads=False)
+    P = buf.psi_pad
+    mv, mm, vv = buf.state(0)
+    S.draw_master(w, mv, w.psi)
+    S.draw_moments(w, mm, vv, w.psi)
+    buf.params[:, :P].copy_(mv.to(S.torch_dtype(w.dtype)).unsqueeze(0).expand(w.n_ranks, P))
+    td = S.torch_dtype(w.dtype)
+    sets = torch.empty((w.steps, w.n_ranks, buf.stride), dtype=td, device="cuda")
+    scale = w.loss_scale
+    for k in range(w.steps):
+        for r in range(w.n_ranks):
+            S.draw_grads(w, sets[k, r], w.psi, k + 1, r, scale)
+        if k + 1 == w.inject_step:
+            S.inject_inf(w, sets[k, w.inject_rank], w.psi)
+            scale = max(scale / 2, 1.0)   # the step after the skip is drawn at the halved scale
+    buf.set_scaler(w.loss_scale, 0, 0)
+    torch.cuda.synchronize()
+    return w, buf, sets
+
+
+def run_ours(args, ws, rank, local):
+    import torch
+    import zero_partitioned_mixed_gb300 as Z
+    from zero_partitioned_mixed_gb300 import synth as S
+    from zero_partitioned_mixed_gb300.build import build_library
+
+    torch.cuda.set_device(local)
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    if rank == 0 or ws > 1:
+        build_library()
+    if ws > 1:
+        dist.barrier()
+
+    w, buf, sets = setup_flat15b(Z, S, torch)
+    N, P = w.n_ranks, buf.psi_pad
+    hyp = Z.hyper(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay, w.max_norm, Z.ZERO_MODE_AUTO)
+    stream = torch.cuda.current_stream()
+    nsets = sets.shape[0]
+
+    def rows(k):
+        return [sets[k, r] for r in range(N)]
+
+    for i in range(args.warmup):
+        buf.step(hyp, rows(i % nsets))
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    kinds = []
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(K):
+            k = (args.warmup + i) % nsets
+            kinds.append(k)
+            ev[i][0].record(stream)
+            buf.step(hyp, rows(k))
+            ev[i][1].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    total_ms = t0.elapsed_time(t1)
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    if ws > 1:
+        tt = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    status = buf.status()
+
+    inject_set = w.inject_step - 1
+    applied_ms = [t for t, k in zip(step_ms, kinds) if k != inject_set]
+    skipped_ms = [t for t, k in zip(step_ms, kinds) if k == inject_set]
+    alg_bytes = (4 * N + 24) * P                 # per applied step: 2N + 12 read, 12 + 2N write
+    kernel_ms = statistics.mean(applied_ms) if applied_ms else statistics.mean(step_ms)
+    peaks, peak_src = measured_peaks()
+    peak = float(peaks.get("hbm_gbs", 6800.0))
+    achieved = alg_bytes / (kernel_ms * 1e-3) / 1e9
+    traffic = ncu_traffic("step_spec_flat1.5b_n8.md")
+
+    value = w.psi * K * ws / (total_ms * 1e-3)
+    line = {
+        "metric": METRIC, "value": value, "unit": "params/s", "n_gpus": ws, "steps": K,
+        "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "storage_dtype": w.dtype,
+        "data": "synthetic",
+        "config": {"workload": w.name, "psi": w.psi, "n_ranks": N, "stage": w.stage, "mode": "speculative",
+                   "grad_sets": nsets, "overflow_every": f"set {inject_set + 1} of {nsets} (+inf in rank 5)",
+                   "l2": "inputs larger than L2: 84 GB per step, no flush needed",
+                   "parallelism": "replicas only" if ws > 1 else "1 GPU"},
+        "hbm_gbs_applied_step": achieved,
+        "ms_per_applied_step": kernel_ms,
+        "ms_per_skipped_step": statistics.mean(skipped_ms) if skipped_ms else None,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "k_step_spec (fp16, 8-wide)",
+                     "algorithmic_bytes_per_launch": alg_bytes,
+                     "peak_source": f"{peak_src} hbm_gbs (copy)"},
+        "gpu_launches": 2 * K,
+        "status_after": {k: status[k] for k in ("steps_applied", "steps_skipped", "loss_scale")},
+    }
+    c = clocks.summary()
+    line["clocks"] = c
+
+    if not args.no_e2e:
+        line["e2e"] = e2e_flat(args, w, buf, sets, hyp, stream, torch, ws, dist)
+    del sets
+    torch.cuda.empty_cache()
+    if rank == 0 and not args.no_cpu_baseline and ws >= 1:
+        r = oracle_timing(1 << 21, 8, 1, "fp16", 200, 1, budget_s=12.0)
+        line["cpu_baseline"] = {"value": r["value"], "unit": "params/s", "cores": 1, "kind": "oracle",
+                                "sample": f"{r['steps']} oracle stage-1 steps on a slab of 2^21 parameters "
+                                          "x 8 ranks (numpy, one thread)"}
+    buf.close()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def e2e_flat(args, w, buf, sets, hyp, stream, torch, ws, dist):
+    """Same step through the public API with the gradients coming from pinned host memory."""
+    N, P = w.n_ranks, buf.psi_pad
+    try:
+        host = torch.empty((N, buf.stride), dtype=sets.dtype, pin_memory=True)
+    except Exception as e:  # not enough pinnable host memory
+        return {"value": None, "unit": "params/s", "error": f"pinned host buffer: {e}"[:200]}
+    host.copy_(sets[0])
+    dev = sets[0]
+    K = max(3, min(args.steps, 10))
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(K):
+        dev.copy_(host, non_blocking=True)
+        buf.step(hyp, [dev[r] for r in range(N)])
+        buf.status(stream)          # device->host read of the step's result, synchronises
+    t = time.perf_counter() - t0
+    if ws > 1:
+        tt = torch.tensor([t], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t = float(tt.item())
+    del host
+    return {"value": w.psi * K * ws / t, "unit": "params/s", "h2d_bytes_per_step": N * buf.stride * 2,
+            "d2h_bytes_per_step": RESULT_BYTES, "steps": K}
+
+
+def run_other(args, ws, rank, local):
+    raise SystemExit(f"workload {args.workload}: not wired yet")
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=4)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=["flat1.5b", "toy", "gpt2", "llama7b", "sweep"], default="flat1.5b")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    ws, rank, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, ws, rank)
+    if args.workload != "flat1.5b":
+        return run_other(args, ws, rank, local)
+    return run_ours(args, ws, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,241 @@
+/*
+ * zero_gb300.h -- C ABI of the partitioned mixed-precision ZeRO step on one
+ * GB300 (sm_103a).  N data-parallel ranks are simulated inside one GPU's
+ * HBM: every rank's 16-bit gradient buffer and parameter replica are
+ * separate device buffers, and the owner shards of the fp32 optimizer state
+ * are laid out back to back in one flat buffer.  The collectives of the
+ * method (reduce-scatter, all-gather, per-bucket broadcast, the scalar
+ * all-reduce of norm and overflow flag) are HBM streams fused into the
+ * update kernels.
+ *
+ * Sources (web pages on ZeRO, cited by title and section):
+ *  - "ZeRO: Memory Optimizations Toward Training Trillion Parameter Models"
+ *    (summary), Sec. 3.1 mixed-precision Adam state (2+2+12 bytes/param),
+ *    Sec. 5 stages P_os / P_os+g / P_os+g+p, Sec. 7 communication volume,
+ *    residual states (gradient norm over the flattened buffer).
+ *  - "zero-stages-simulation" README: flat contiguous partition, rank r owns
+ *    chunk r; per-stage schedule table; byte-accurate accounting.
+ *  - "CMU 11-868 L18: How ZeRO Cuts Data-Parallel Memory": ZeRO-1 call
+ *    sequence (reduce-scatter into an FP32 shard, update, copy to 16-bit,
+ *    all-gather); ZeRO-3 broadcast from owner before forward and backward.
+ *
+ * General conventions
+ *  - Every call returns a zero_status_t.  Nothing aborts, throws or traps;
+ *    on error the call launches nothing and zero_last_error() says why.
+ *  - All tensor arguments are caller-owned DEVICE pointers (the caller
+ *    allocates them, e.g. with PyTorch) unless a comment says "host".  The
+ *    library owns only its small workspace (status word, per-block norm
+ *    partials, and for some modes an fp32 gradient buffer of psi_pad floats).
+ *  - Device pointers must be 16-byte aligned.  The 128-bit vector path runs
+ *    when psi_pad (or a bucket's bounds) are multiples of 8; otherwise an
+ *    element-wise path runs with the same arithmetic.
+ *  - Calls are asynchronous on the given CUDA stream (a cudaStream_t passed
+ *    as void*, NULL = legacy default stream).  One host thread per handle.
+ *  - Elements [psi, psi_pad) are padding: gradients there are ignored, and
+ *    master/m/v/params there are written as 0.
+ *  - The loss scale, the count t of applied Adam steps and the live slot of
+ *    double-buffered state are DEVICE-side handle state, so a step never
+ *    waits for the host: an overflowing step halves the scale (floor 1.0)
+ *    and leaves t unchanged without a host round trip.
+ */
+#ifndef ZERO_GB300_H
+#define ZERO_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define ZERO_API __attribute__((visibility("default")))
+#else
+#define ZERO_API
+#endif
+
+typedef enum {
+    ZERO_OK = 0,
+    ZERO_EINVAL = 1,    /* bad argument: null/misaligned pointer, range, stage/mode mismatch */
+    ZERO_ENOMEM = 2,    /* workspace allocation failed */
+    ZERO_ECUDA = 3,     /* a CUDA runtime call or kernel launch failed */
+    ZERO_ETIMEOUT = 4,  /* reserved: no call waits on the device */
+    ZERO_ESTATE = 5     /* call sequence wrong (e.g. stage-3 step before every bucket was reduced) */
+} zero_status_t;
+
+typedef enum { ZERO_FP16 = 0, ZERO_BF16 = 1 } zero_dtype_t;
+
+typedef enum {
+    ZERO_MODE_AUTO = 0,            /* SPECULATIVE if possible, else TWO_PASS_WS for N > 4, else REREAD */
+    ZERO_MODE_TWO_PASS_WS = 1,     /* pass 1 writes fp32 g_hat to workspace; pass 2 reads it */
+    ZERO_MODE_TWO_PASS_REREAD = 2, /* pass 2 reduces the N gradient buffers again */
+    ZERO_MODE_SPECULATIVE = 3      /* one pass writing the shadow state slot; commit or roll back */
+} zero_mode_t;
+
+/* zero_init_partition flags */
+#define ZERO_F_DOUBLE_BUFFER 1u    /* master/m/v hold two slots of psi_pad floats (stages 1-3) */
+
+#define ZERO_MAX_RANKS 64
+
+typedef struct zero_handle* zero_handle_t;   /* opaque, library-owned */
+
+typedef struct {
+    float lr, beta1, beta2, eps, weight_decay;
+    float max_norm;   /* global-norm clip threshold; <= 0 disables clipping */
+    int32_t mode;     /* zero_mode_t */
+} zero_hyper_t;
+
+typedef struct {
+    int32_t overflow;       /* last step saw a non-finite averaged gradient (step skipped) */
+    int32_t applied;        /* last step updated the state */
+    int32_t state_slot;     /* live slot (0/1) of double-buffered master/m/v; 0 otherwise */
+    int32_t error;          /* device-side error word, 0 = none */
+    double grad_norm;       /* L2 norm of the averaged unscaled gradient of the last step */
+    double clip_coef;       /* fp32 factor applied to the gradient (1.0 when not clipping) */
+    float loss_scale;       /* current loss scale, after any halving */
+    float reserved;
+    int64_t steps_applied;  /* t: Adam steps applied so far */
+    int64_t steps_skipped;  /* steps skipped on overflow so far */
+} zero_result_t;
+
+typedef struct {
+    uint64_t psi, psi_pad, shard, n_ranks, stage;
+    uint64_t model_state_bytes_per_rank;  /* 16/4+12/N/2+14/N/16/N bytes x psi_pad, exact */
+    uint64_t comm_elems_paper;            /* 2 psi_pad (stages 0-2), 3 psi_pad (stage 3) */
+    uint64_t comm_elems_ring;             /* 2(N-1)/N psi_pad, 3(N-1)/N psi_pad for stage 3 */
+    uint64_t hbm_read_bytes, hbm_write_bytes;   /* algorithmic HBM bytes of the last call */
+    uint64_t hbm_read_total, hbm_write_total;   /* cumulative since init */
+} zero_bytes_t;
+
+/*
+ * zero_init_partition -- a1: partition a flat buffer of psi parameters over
+ * n_ranks simulated ranks and allocate the handle's workspace.
+ *   ("zero-stages-simulation" README, flat partitioning: N near-equal
+ *    contiguous chunks, rank r owns chunk r; ZeRO summary Sec. 5, P_os: N_d
+ *    equal partitions.)
+ * psi_pad = smallest multiple of n_ranks*align >= psi; shard = psi_pad/N;
+ * offset_r = r*shard; real_r = clamp(psi - offset_r, 0, shard).
+ *   psi      >= 0 (0 gives an empty step)
+ *   n_ranks  1..ZERO_MAX_RANKS
+ *   stage    0..3 (ZeRO-0 plain DP, P_os, P_os+g, P_os+g+p)
+ *   dtype    zero_dtype_t of gradients and parameters
+ *   align    >= 1 elements (8 keeps every shard 16-byte aligned)
+ *   flags    ZERO_F_DOUBLE_BUFFER or 0 (stage 0 rejects it)
+ *   out      host pointer receiving the handle
+ * Uses the current CUDA device.  Errors: EINVAL, ENOMEM, ECUDA.
+ */
+ZERO_API int zero_init_partition(uint64_t psi, int n_ranks, int stage, int dtype, int align,
+                        unsigned flags, zero_handle_t* out);
+
+/*
+ * zero_partition_info -- the partition (host values, exact).  offsets and
+ * real are host arrays of n_ranks entries, or NULL.  Any output may be NULL.
+ */
+ZERO_API int zero_partition_info(zero_handle_t h, uint64_t* psi_pad, uint64_t* shard,
+                        uint64_t* offsets, uint64_t* real);
+
+/*
+ * zero_set_scaler -- set the device-side loss scale, applied-step count t
+ * and live state slot (0/1; must be 0 without ZERO_F_DOUBLE_BUFFER).  Used
+ * before the first step and to resume from a checkpoint.  Stream-ordered.
+ * The loss scale must be finite and > 0.  Errors: EINVAL, ECUDA.
+ */
+ZERO_API int zero_set_scaler(zero_handle_t h, float loss_scale, int64_t steps_applied,
+                    int32_t state_slot, void* stream);
+
+/*
+ * zero_step -- one mixed-precision ZeRO step (a2..a8, a11).
+ *   Stages 0-2: reduce the N ranks' 16-bit gradients in fixed order 0..N-1
+ *   in fp32, divide by N*loss_scale (CMU notes, ZeRO-1 step 3: sum and
+ *   average into an FP32 shard), test for inf/nan, form the global L2 norm
+ *   (ZeRO summary, residual states: norm over the flattened gradient), clip
+ *   if max_norm > 0, run AdamW on the owners' fp32 master/m/v (ZeRO summary
+ *   Sec. 3.1 and Sec. 5), round to 16 bits and write every rank's replica
+ *   (the all-gather; CMU notes steps 5-6).  Stage 0 all-reduces and updates
+ *   N full replicas of the state (ZeRO summary Sec. 7, baseline DP).
+ *   Stage 3: grads must be NULL; the N gradients were already consumed by
+ *   zero_reduce_scatter_bucket calls covering [0, psi_pad) exactly once
+ *   since the last step.  This call finishes the norm/overflow/clip and
+ *   (two-pass modes) applies Adam and writes the 16-bit shard.
+ * On overflow nothing of master/m/v/params changes, the scale halves and t
+ * is not advanced.
+ *   grads   host array of N device pointers, psi_pad 16-bit elements each
+ *           (stages 0-2); NULL for stage 3
+ *   params  host array of N device pointers to psi_pad 16-bit replicas
+ *           (stages 0-2), or of 1 pointer to the psi_pad 16-bit
+ *           concatenation of the owner shards (stage 3).  Replicas must
+ *           equal the RNE cast of the live master on entry.
+ *   master, m, v  fp32 device buffers.  Stages 1-3: psi_pad floats (the N
+ *           owner shards back to back), or 2*psi_pad with
+ *           ZERO_F_DOUBLE_BUFFER (slot s at offset s*psi_pad).  Stage 0:
+ *           N*psi_pad floats, replica r at offset r*psi_pad.
+ *   hyper   host pointer, read during the call only
+ * Errors: EINVAL, ESTATE, ECUDA, ENOMEM (first two-pass call allocates the
+ * fp32 workspace; make it before any stream capture).
+ */
+ZERO_API int zero_step(zero_handle_t h, const void* const* grads, void* const* params,
+              float* master, float* m, float* v, const zero_hyper_t* hyper, void* stream);
+
+/*
+ * zero_gather_bucket -- a9: ZeRO-3 parameter gather of bucket [a, b): every
+ * rank receives the owners' 16-bit values, out[r][j] = shard16[a + j].
+ *   (ZeRO summary Sec. 5, P_os+g+p: the owner broadcasts a layer's
+ *    parameters before its forward and again before its backward; CMU
+ *    notes, ZeRO-3: ncclBroadcast from the owning GPU.)
+ *   0 <= a <= b <= psi_pad.  shard16: device, psi_pad 16-bit elements.
+ *   out: host array of N device pointers, b - a elements each.
+ * Stage 3 only.  Errors: EINVAL, ECUDA.
+ */
+ZERO_API int zero_gather_bucket(zero_handle_t h, uint64_t a, uint64_t b, const void* shard16,
+                       void* const* out, void* stream);
+
+/*
+ * zero_reduce_scatter_bucket -- a10: ZeRO-3 gradient reduce-scatter of
+ * bucket [a, b) into the owners' shards: the a2..a5 steps restricted to the
+ * bucket.  (ZeRO summary Sec. 5, P_os+g / P_os+g+p: reduce-scatter as the
+ * gradients of each layer appear in backward; CMU notes, ZeRO-2/3: each
+ * segment's gradients are reduced to its owner.)
+ * With ZERO_F_DOUBLE_BUFFER and no clipping (mode AUTO or SPECULATIVE) the
+ * bucket's AdamW update is fused here: new master/m/v go to the shadow slot
+ * and the new 16-bit values straight into shard16[a, b); zero_step then
+ * commits, or on overflow restores shard16 from the old master.  Otherwise
+ * the averaged gradient is written to the fp32 workspace and zero_step
+ * applies Adam.
+ *   grads: host array of N device pointers, b - a 16-bit elements each.
+ *   master, m, v, shard16: as for zero_step of stage 3 (may be NULL in
+ *   two-pass modes).  Every call of one step must pass the same hyper.
+ *   Buckets of one step must not overlap.  At most 4096 per step.
+ * Stage 3 only.  Errors: EINVAL, ESTATE, ECUDA, ENOMEM.
+ */
+ZERO_API int zero_reduce_scatter_bucket(zero_handle_t h, uint64_t a, uint64_t b,
+                               const void* const* grads, float* master, float* m, float* v,
+                               void* shard16, const zero_hyper_t* hyper, void* stream);
+
+/*
+ * zero_get_status -- a11: copy the device status of the last step to the
+ * host struct *out (host pointer).  Synchronises the given stream.
+ * Errors: EINVAL, ECUDA.
+ */
+ZERO_API int zero_get_status(zero_handle_t h, void* stream, zero_result_t* out);
+
+/*
+ * zero_bytes_moved -- D4/D5 accounting and algorithmic HBM bytes.
+ *   (ZeRO summary Sec. 5 memory equations and Sec. 7 communication volume;
+ *    "zero-stages-simulation" README: byte-accurate memory tracker and a
+ *    counting interconnect.)  Host-only, exact integers.  The HBM counters
+ *   count the bytes the method must move for the calls made, assuming
+ *   each step applied (an overflow's rollback pass is not counted).
+ */
+ZERO_API int zero_bytes_moved(zero_handle_t h, zero_bytes_t* out);
+
+/* Last error message of this handle (or of the last failed init when h is
+ * NULL).  The string is owned by the library and valid until the next call. */
+ZERO_API const char* zero_last_error(zero_handle_t h);
+
+/* Free the handle and its workspace.  Synchronises the device first.  NULL is a no-op. */
+ZERO_API void zero_destroy(zero_handle_t h);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZERO_GB300_H */

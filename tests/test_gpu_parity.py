@@ -1,0 +1,204 @@
+"""CUDA path vs the oracle, element by element, through the C ABI.
+
+Sizes span several 8-element groups per thread, several blocks and a
+ragged tail; every stage, mode and dtype; overflow, clipping, padding,
+non-power-of-two scales, N up to 64, empty inputs and unaligned buckets.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from _parity import run_case
+
+pytestmark = pytest.mark.gpu
+
+INF, NINF, NAN = float("inf"), float("-inf"), float("nan")
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("stage", [1, 2])
+@pytest.mark.parametrize("mode", [0, 1, 2, 3])
+def test_stage12_modes(stage, mode, dtype):
+    st = run_case(300_007, 8, stage, dtype, steps=3, mode=mode, double_buffer=(mode in (0, 3)),
+                  hyper_kw=dict(weight_decay=0.1))
+    st.check()
+    assert st.mismatches == 0, st
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_stage0_toy_shape(dtype):
+    # the README's toy buffer: psi = 637,824 over 32 simulated ranks
+    st = run_case(637_824, 32, 0, dtype, steps=2, double_buffer=False)
+    st.check()
+    assert st.mismatches == 0, st
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("double_buffer", [True, False])
+def test_stage3_layer_buckets(dtype, double_buffer):
+    psi, n = 200_003, 4
+    pp = (psi + 31) // 32 * 32
+    buckets = [(0, 40_000), (40_000, 40_008), (40_008, 123_456), (123_456, 123_457), (123_457, pp)]
+    st = run_case(psi, n, 3, dtype, steps=3, buckets=buckets, double_buffer=double_buffer)
+    st.check()
+    assert st.mismatches == 0, st
+
+
+@pytest.mark.parametrize("stage", [1, 2, 3])
+def test_overflow_skip_and_scale_halving(stage):
+    n, psi = 8, 100_000
+    inject = [(1, 5, 4_321, INF), (2, 0, 99_999, NAN), (3, 7, 0, NINF)]
+    st = run_case(psi, n, stage, "fp16", steps=5, loss_scale=65536.0, sigma=1e-3, inject=inject,
+                  buckets=[(0, 50_000), (50_000, 100_032)] if stage == 3 else None)
+    st.check()
+    assert st.mismatches == 0, st
+
+
+def test_overflow_in_padding_is_ignored():
+    # psi = 1001, N = 4, align 8 -> psi_pad 1024; an inf at index 1010 is padding
+    st = run_case(1001, 4, 2, "fp16", steps=2, inject=[(0, 2, 1010, INF)])
+    st.check()
+    assert st.mismatches == 0
+
+
+def test_two_pass_stage0_overflow():
+    st = run_case(5000, 3, 0, "bf16", steps=3, double_buffer=False, inject=[(1, 1, 17, INF)])
+    st.check()
+    assert st.mismatches == 0
+
+
+@pytest.mark.parametrize("stage,mode", [(1, 1), (2, 2), (0, 0), (3, 0)])
+def test_clipping_active(stage, mode):
+    # max_norm well below the norm: every gradient scaled by max_norm / (norm + 1e-6)
+    st = run_case(250_000, 4, stage, "bf16", steps=3, mode=mode, double_buffer=(stage == 3),
+                  hyper_kw=dict(max_norm=0.05, weight_decay=0.01))
+    st.check()
+
+
+def test_clip_inactive_when_norm_small():
+    st = run_case(250_000, 4, 2, "bf16", steps=2, mode=1, double_buffer=False,
+                  hyper_kw=dict(max_norm=1e6))
+    st.check()
+    assert st.mismatches == 0
+
+
+@pytest.mark.parametrize("n", [1, 3, 5, 13, 64])
+def test_rank_counts_and_nonpow2_scale(n):
+    # N * scale not a power of two -> the kernels divide; ragged psi
+    st = run_case(20_011, n, 2, "fp16", steps=2, loss_scale=1000.0, sigma=1e-3, mode=3)
+    st.check()
+    assert st.mismatches == 0
+
+
+@pytest.mark.parametrize("align", [1, 2])
+def test_elementwise_path_when_not_multiple_of_8(align):
+    # psi_pad % 8 != 0 takes the element-wise kernels
+    st = run_case(1001, 3, 1, "bf16", steps=2, align=align, mode=1, double_buffer=False)
+    st.check()
+    assert st.mismatches == 0
+
+
+def test_tiny_hand_case_through_the_abi():
+    # psi = 5, N = 2, align = 2: the hand-worked case, lr 2^-6, b = (0.5, 0.75), eps 0
+    import oracle as O
+    from zero_partitioned_mixed_gb300 import _binding as B
+    from zero_partitioned_mixed_gb300.buffers import RankBuffers
+    buf = RankBuffers(5, 2, 1, "fp16", align=2, double_buffer=False)
+    assert (buf.psi_pad, buf.shard, buf.offsets, buf.real) == (8, 4, [0, 4], [4, 1])
+    p0 = torch.tensor([0.5, 0.25, 0.0, -0.5, 1.0, 0, 0, 0], device="cuda")
+    mv, _, _ = buf.state(0)
+    mv.copy_(p0)
+    buf.params[:, :8].copy_(p0.to(torch.float16))
+    buf.grads[0, :8].copy_(torch.tensor([1, 2, -1, 0.5, 4, 0, 0, 0], device="cuda"))
+    buf.grads[1, :8].copy_(torch.tensor([3, 2, -3, -2.5, 0, 0, 0, 0], device="cuda"))
+    buf.step(B.hyper(lr=2.0 ** -6, beta1=0.5, beta2=0.75, eps=0.0, mode=1))
+    s = buf.status()
+    assert s["grad_norm"] == 17 ** 0.5 and s["applied"] == 1
+    want = [0.484375, 0.234375, 0.015625, -0.484375, 0.984375, 0, 0, 0]
+    assert mv.cpu().tolist() == want
+    assert buf.params[0, :8].float().cpu().tolist() == want
+    assert buf.params[1, :8].float().cpu().tolist() == want
+    buf.close()
+
+
+def test_empty_psi():
+    from zero_partitioned_mixed_gb300 import _binding as B
+    from zero_partitioned_mixed_gb300.buffers import RankBuffers
+    for stage in (0, 1, 2, 3):
+        buf = RankBuffers(0, 4, stage, "bf16")
+        assert buf.psi_pad == 0
+        buf.step(B.hyper())
+        s = buf.status()
+        assert s["applied"] == 1 and s["overflow"] == 0 and s["grad_norm"] == 0.0
+        buf.close()
+
+
+def test_errors_are_returned_not_raised_on_device():
+    from zero_partitioned_mixed_gb300 import _binding as B
+    from zero_partitioned_mixed_gb300.buffers import RankBuffers
+    buf = RankBuffers(1024, 2, 2, "bf16")
+    bad = buf.grads.view(-1)[1:]            # 2-byte offset: misaligned
+    with pytest.raises(B.ZeroError) as e:
+        B.zero_step(buf.h, [bad, buf.grads[1]], buf.param_rows(), buf.master, buf.m, buf.v, B.hyper())
+    assert e.value.code == 1 and "aligned" in str(e.value)
+    with pytest.raises(B.ZeroError) as e:
+        B.zero_step(buf.h, buf.grad_rows(), buf.param_rows(), buf.master, buf.m, buf.v,
+                    B.hyper(max_norm=1.0, mode=3))
+    assert e.value.code == 1
+    with pytest.raises(B.ZeroError):
+        B.zero_gather_bucket(buf.h, 0, 8, buf.params, buf.param_rows())   # not stage 3
+    buf.close()
+    b3 = RankBuffers(1024, 2, 3, "bf16")
+    with pytest.raises(B.ZeroError) as e:
+        b3.step(B.hyper())                  # no bucket reduced yet
+    assert e.value.code == 5
+    g = [torch.zeros(512, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    b3.reduce_scatter(0, 512, g, B.hyper())
+    with pytest.raises(B.ZeroError) as e:
+        b3.reduce_scatter(256, 768, g, B.hyper())   # overlaps
+    assert e.value.code == 5
+    b3.close()
+
+
+def test_byte_counters_exact():
+    from zero_partitioned_mixed_gb300 import _binding as B
+    from zero_partitioned_mixed_gb300.buffers import RankBuffers
+    import oracle as O
+    buf = RankBuffers(637_824, 32, 1, "fp16")
+    b = buf.bytes_moved()
+    assert b["psi_pad"] == 637_952 and b["shard"] == 19_936
+    assert b["model_state_bytes_per_rank"] == O.model_state_bytes(637_952, 32, 1) == 2_791_040
+    assert b["comm_elems_paper"] == O.comm_elems_paper(637_952, 1)
+    assert b["comm_elems_ring"] == O.comm_elems_ring(637_952, 32, 1)
+    buf.step(B.hyper())
+    b = buf.bytes_moved()
+    P, N = 637_952, 32
+    assert (b["hbm_read_bytes"], b["hbm_write_bytes"]) == (2 * N * P + 12 * P, 12 * P + 2 * N * P)
+    buf.close()
+
+
+def test_state_slot_and_resume():
+    # resume from (scale, t, slot) gives the same result as running on
+    from zero_partitioned_mixed_gb300 import _binding as B
+    from zero_partitioned_mixed_gb300.buffers import RankBuffers
+    torch.manual_seed(0)
+    a = RankBuffers(4096, 4, 1, "bf16")
+    a.master[:4096].normal_(0, 0.02)
+    a.params[:, :4096].copy_(a.master[:4096].to(torch.bfloat16))
+    a.grads.normal_(0, 1e-2)
+    h = B.hyper()
+    a.step(h)
+    a.step(h)
+    s = a.status()
+    assert s["state_slot"] == 0 and s["steps_applied"] == 2
+    b = RankBuffers(4096, 4, 1, "bf16")
+    b.master.copy_(a.master); b.m.copy_(a.m); b.v.copy_(a.v); b.params.copy_(a.params)
+    b.grads.copy_(a.grads)
+    b.set_scaler(s["loss_scale"], s["steps_applied"], s["state_slot"])
+    a.step(h)
+    b.step(h)
+    sa, sb = a.status(), b.status()
+    assert sa["state_slot"] == sb["state_slot"] == 1
+    assert torch.equal(a.master, b.master) and torch.equal(a.params, b.params)
+    a.close(); b.close()

@@ -1,0 +1,503 @@
+// Host side of the C ABI declared in include/zero_gb300.h: argument
+// validation, the flat partition, exact accounting, workspace ownership and
+// the order of kernel launches for each stage and mode.  Nothing here waits
+// on the device except zero_get_status and zero_destroy.
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <new>
+#include <string>
+#include <utility>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "zero_gb300.h"
+#include "zero_internal.h"
+
+namespace {
+
+thread_local std::string g_init_error;
+
+}  // namespace
+
+struct zero_handle {
+    uint64_t psi = 0, psi_pad = 0, shard = 0;
+    int n = 0, stage = 0, dtype = 0, align = 0;
+    unsigned flags = 0;
+    int device = 0;
+    std::vector<uint64_t> offsets, real;
+    zg::Workspace ws{};
+    void* ws_block = nullptr;
+    // ZeRO-3 step bookkeeping (host side)
+    std::vector<std::pair<uint64_t, uint64_t>> covered;
+    int rs_calls = 0;
+    int rs_mode = -1;
+    zero_hyper_t rs_hyper{};
+    // accounting
+    uint64_t last_r = 0, last_w = 0, tot_r = 0, tot_w = 0;
+    std::string err;
+};
+
+namespace {
+
+int fail(zero_handle* h, int code, const std::string& msg) {
+    if (h) h->err = msg;
+    else g_init_error = msg;
+    return code;
+}
+
+int cuda_fail(zero_handle* h, cudaError_t e, const char* what) {
+    return fail(h, ZERO_ECUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool double_buffered(const zero_handle* h) { return (h->flags & ZERO_F_DOUBLE_BUFFER) != 0; }
+
+void count(zero_handle* h, uint64_t r, uint64_t w) {
+    h->last_r = r;
+    h->last_w = w;
+    h->tot_r += r;
+    h->tot_w += w;
+}
+
+// Resolve AUTO and check that the requested mode fits the handle.
+int resolve_mode(zero_handle* h, const zero_hyper_t* hy, int* mode) {
+    const bool clip = hy->max_norm > 0.0f;
+    const bool db = double_buffered(h);
+    switch (hy->mode) {
+        case ZERO_MODE_AUTO:
+            if (h->stage != 0 && db && !clip) *mode = ZERO_MODE_SPECULATIVE;
+            else if (h->stage == 0 || h->stage == 3) *mode = ZERO_MODE_TWO_PASS_WS;
+            else *mode = h->n > 4 ? ZERO_MODE_TWO_PASS_WS : ZERO_MODE_TWO_PASS_REREAD;
+            return ZERO_OK;
+        case ZERO_MODE_SPECULATIVE:
+            if (h->stage == 0) return fail(h, ZERO_EINVAL, "speculative mode is not available for stage 0");
+            if (!db) return fail(h, ZERO_EINVAL, "speculative mode needs ZERO_F_DOUBLE_BUFFER state");
+            if (clip) return fail(h, ZERO_EINVAL, "clipping needs the global norm before the update: use a two-pass mode");
+            *mode = ZERO_MODE_SPECULATIVE;
+            return ZERO_OK;
+        case ZERO_MODE_TWO_PASS_WS:
+            *mode = ZERO_MODE_TWO_PASS_WS;
+            return ZERO_OK;
+        case ZERO_MODE_TWO_PASS_REREAD:
+            if (h->stage == 0 || h->stage == 3)
+                return fail(h, ZERO_EINVAL, "stages 0 and 3 keep g_hat in the workspace: use TWO_PASS_WS or AUTO");
+            *mode = ZERO_MODE_TWO_PASS_REREAD;
+            return ZERO_OK;
+        default:
+            return fail(h, ZERO_EINVAL, "unknown mode");
+    }
+}
+
+int ensure_ghat(zero_handle* h) {
+    if (h->ws.ghat || h->psi_pad == 0) return ZERO_OK;
+    void* p = nullptr;
+    cudaError_t e = cudaMalloc(&p, h->psi_pad * sizeof(float));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(h, ZERO_ENOMEM, "cannot allocate the fp32 gradient workspace (" +
+                                        std::to_string(h->psi_pad * 4) + " bytes)");
+    }
+    h->ws.ghat = static_cast<float*>(p);
+    return ZERO_OK;
+}
+
+zg::Args base_args(const zero_handle* h, const zero_hyper_t* hy) {
+    zg::Args a;
+    std::memset(&a, 0, sizeof(a));
+    a.n_ranks = h->n;
+    a.stage = h->stage;
+    a.psi = h->psi;
+    a.psi_pad = h->psi_pad;
+    a.ws = h->ws;
+    if (hy) {
+        a.hyper.lr = hy->lr;
+        a.hyper.beta1 = hy->beta1;
+        a.hyper.beta2 = hy->beta2;
+        a.hyper.eps = hy->eps;
+        a.hyper.weight_decay = hy->weight_decay;
+        a.hyper.max_norm = hy->max_norm;
+    }
+    return a;
+}
+
+int launch(zero_handle* h, zg::Kind kind, bool vec8, const zg::Args& a, cudaStream_t s, const char* what) {
+    cudaError_t e = zg::launch(kind, h->dtype, vec8, a, s, nullptr);
+    if (e != cudaSuccess) return cuda_fail(h, e, what);
+    return ZERO_OK;
+}
+
+int check_ptr(zero_handle* h, const void* p, const char* name) {
+    if (!p) return fail(h, ZERO_EINVAL, std::string(name) + " is NULL");
+    if (!aligned16(p)) return fail(h, ZERO_EINVAL, std::string(name) + " is not 16-byte aligned");
+    return ZERO_OK;
+}
+
+int check_hyper(zero_handle* h, const zero_hyper_t* hy) {
+    if (!hy) return fail(h, ZERO_EINVAL, "hyper is NULL");
+    const float vals[] = {hy->lr, hy->beta1, hy->beta2, hy->eps, hy->weight_decay, hy->max_norm};
+    for (float x : vals)
+        if (!std::isfinite(x)) return fail(h, ZERO_EINVAL, "hyper-parameters must be finite");
+    if (!(hy->beta1 >= 0.0f && hy->beta1 < 1.0f && hy->beta2 >= 0.0f && hy->beta2 < 1.0f))
+        return fail(h, ZERO_EINVAL, "beta1 and beta2 must lie in [0, 1)");
+    return ZERO_OK;
+}
+
+bool same_hyper(const zero_hyper_t& x, const zero_hyper_t& y) {
+    return std::memcmp(&x, &y, sizeof(zero_hyper_t)) == 0;
+}
+
+}  // namespace
+
+extern "C" {
+
+int zero_init_partition(uint64_t psi, int n_ranks, int stage, int dtype, int align, unsigned flags,
+                        zero_handle_t* out) {
+    if (!out) return fail(nullptr, ZERO_EINVAL, "out is NULL");
+    *out = nullptr;
+    if (n_ranks < 1 || n_ranks > ZERO_MAX_RANKS)
+        return fail(nullptr, ZERO_EINVAL, "n_ranks must be in 1..64");
+    if (stage < 0 || stage > 3) return fail(nullptr, ZERO_EINVAL, "stage must be 0..3");
+    if (dtype != ZERO_FP16 && dtype != ZERO_BF16) return fail(nullptr, ZERO_EINVAL, "dtype must be fp16 or bf16");
+    if (align < 1) return fail(nullptr, ZERO_EINVAL, "align must be >= 1");
+    if (flags & ~ZERO_F_DOUBLE_BUFFER) return fail(nullptr, ZERO_EINVAL, "unknown flag");
+    if (stage == 0 && (flags & ZERO_F_DOUBLE_BUFFER))
+        return fail(nullptr, ZERO_EINVAL, "stage 0 keeps its state in place (no double buffer)");
+    const uint64_t unit = static_cast<uint64_t>(n_ranks) * static_cast<uint64_t>(align);
+    if (psi > (UINT64_MAX / 64) - unit) return fail(nullptr, ZERO_EINVAL, "psi too large");
+
+    zero_handle* h = new (std::nothrow) zero_handle();
+    if (!h) return fail(nullptr, ZERO_ENOMEM, "host allocation failed");
+    h->psi = psi;
+    h->n = n_ranks;
+    h->stage = stage;
+    h->dtype = dtype;
+    h->align = align;
+    h->flags = flags;
+    h->psi_pad = (psi + unit - 1) / unit * unit;
+    h->shard = h->psi_pad / static_cast<uint64_t>(n_ranks);
+    for (int r = 0; r < n_ranks; ++r) {
+        const uint64_t off = static_cast<uint64_t>(r) * h->shard;
+        h->offsets.push_back(off);
+        h->real.push_back(psi > off ? std::min(psi - off, h->shard) : 0);
+    }
+    cudaError_t e = cudaGetDevice(&h->device);
+    if (e != cudaSuccess) {
+        delete h;
+        return cuda_fail(nullptr, e, "cudaGetDevice");
+    }
+    // one block: status | partials | flags | bucket partials | bucket flags
+    const size_t st_bytes = (sizeof(zg::DevStatus) + 255) / 256 * 256;
+    const size_t bytes = st_bytes + zg::kMaxBlocks * (sizeof(double) + sizeof(int32_t)) +
+                         zg::kMaxBuckets * (sizeof(double) + sizeof(int32_t));
+    e = cudaMalloc(&h->ws_block, bytes);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        delete h;
+        return fail(nullptr, ZERO_ENOMEM, "cannot allocate the workspace");
+    }
+    char* base = static_cast<char*>(h->ws_block);
+    h->ws.status = reinterpret_cast<zg::DevStatus*>(base);
+    h->ws.partials = reinterpret_cast<double*>(base + st_bytes);
+    h->ws.bucket_norm = h->ws.partials + zg::kMaxBlocks;
+    h->ws.flags = reinterpret_cast<int32_t*>(h->ws.bucket_norm + zg::kMaxBuckets);
+    h->ws.bucket_flag = h->ws.flags + zg::kMaxBlocks;
+    h->ws.ghat = nullptr;
+    e = cudaMemset(h->ws_block, 0, bytes);
+    if (e == cudaSuccess) e = zg::launch_set_scaler(h->ws.status, 1.0f, 0, 0, nullptr);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        cudaFree(h->ws_block);
+        delete h;
+        return cuda_fail(nullptr, e, "workspace initialisation");
+    }
+    *out = h;
+    return ZERO_OK;
+}
+
+int zero_partition_info(zero_handle_t h, uint64_t* psi_pad, uint64_t* shard, uint64_t* offsets,
+                        uint64_t* real) {
+    if (!h) return fail(nullptr, ZERO_EINVAL, "handle is NULL");
+    if (psi_pad) *psi_pad = h->psi_pad;
+    if (shard) *shard = h->shard;
+    for (int r = 0; r < h->n; ++r) {
+        if (offsets) offsets[r] = h->offsets[r];
+        if (real) real[r] = h->real[r];
+    }
+    return ZERO_OK;
+}
+
+int zero_set_scaler(zero_handle_t h, float loss_scale, int64_t steps_applied, int32_t state_slot,
+                    void* stream) {
+    if (!h) return fail(nullptr, ZERO_EINVAL, "handle is NULL");
+    if (!std::isfinite(loss_scale) || loss_scale <= 0.0f)
+        return fail(h, ZERO_EINVAL, "loss_scale must be finite and > 0");
+    if (steps_applied < 0) return fail(h, ZERO_EINVAL, "steps_applied must be >= 0");
+    if (state_slot != 0 && !(double_buffered(h) && state_slot == 1))
+        return fail(h, ZERO_EINVAL, "state_slot must be 0 (or 1 with a double buffer)");
+    h->covered.clear();
+    h->rs_calls = 0;
+    h->rs_mode = -1;
+    cudaError_t e = zg::launch_set_scaler(h->ws.status, loss_scale, steps_applied, state_slot,
+                                          static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(h, e, "set_scaler");
+    return ZERO_OK;
+}
+
+int zero_step(zero_handle_t h, const void* const* grads, void* const* params, float* master, float* m,
+              float* v, const zero_hyper_t* hyper, void* stream) {
+    if (!h) return fail(nullptr, ZERO_EINVAL, "handle is NULL");
+    int rc = check_hyper(h, hyper);
+    if (rc) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const uint64_t P = h->psi_pad, N = static_cast<uint64_t>(h->n);
+    const bool vec8 = (P % 8) == 0;
+    const bool any = P > 0;
+    zg::Args a = base_args(h, hyper);
+    a.base = 0;
+    a.count = P;
+    a.slot_stride = double_buffered(h) ? P : 0;
+
+    if (h->stage == 3) {
+        if (grads) return fail(h, ZERO_EINVAL, "stage 3: grads must be NULL (use zero_reduce_scatter_bucket)");
+        if (!params) return fail(h, ZERO_EINVAL, "params is NULL");
+        uint64_t covered = 0;
+        for (auto& iv : h->covered) covered += iv.second - iv.first;
+        if (covered != P)
+            return fail(h, ZERO_ESTATE, "stage 3: reduce-scatter buckets cover " + std::to_string(covered) +
+                                            " of " + std::to_string(P) + " elements this step");
+        int mode = h->rs_mode;
+        if (P == 0) {
+            rc = resolve_mode(h, hyper, &mode);
+            if (rc) return rc;
+        } else if (!same_hyper(*hyper, h->rs_hyper)) {
+            return fail(h, ZERO_EINVAL, "stage 3: zero_step hyper differs from the reduce-scatter calls'");
+        }
+        if (any) {
+            if ((rc = check_ptr(h, params[0], "params[0]")) || (rc = check_ptr(h, master, "master")) ||
+                (rc = check_ptr(h, m, "m")) || (rc = check_ptr(h, v, "v")))
+                return rc;
+        }
+        a.params[0] = any ? params[0] : nullptr;
+        a.master = master;
+        a.m = m;
+        a.v = v;
+        a.bucket_index = h->rs_calls;
+        const bool spec = mode == ZERO_MODE_SPECULATIVE;
+        cudaError_t e = zg::launch_finalize3(spec, a, s);
+        if (e != cudaSuccess) return cuda_fail(h, e, "finalize");
+        if (any) {
+            rc = launch(h, spec ? zg::Kind::kRollbackShard : zg::Kind::kApplyWsShard, vec8, a, s,
+                        spec ? "rollback" : "apply");
+            if (rc) return rc;
+        }
+        h->covered.clear();
+        h->rs_calls = 0;
+        h->rs_mode = -1;
+        if (spec) count(h, 0, 0);
+        else count(h, 16 * P, 14 * P);
+        return ZERO_OK;
+    }
+
+    int mode = 0;
+    rc = resolve_mode(h, hyper, &mode);
+    if (rc) return rc;
+    if (any) {
+        if (!grads) return fail(h, ZERO_EINVAL, "grads is NULL");
+        if (!params) return fail(h, ZERO_EINVAL, "params is NULL");
+        for (int r = 0; r < h->n; ++r) {
+            if ((rc = check_ptr(h, grads[r], "grads[r]"))) return rc;
+            if ((rc = check_ptr(h, params[r], "params[r]"))) return rc;
+            a.grads[r] = grads[r];
+            a.params[r] = params[r];
+        }
+        if ((rc = check_ptr(h, master, "master")) || (rc = check_ptr(h, m, "m")) || (rc = check_ptr(h, v, "v")))
+            return rc;
+    }
+    a.master = master;
+    a.m = m;
+    a.v = v;
+
+    if (mode == ZERO_MODE_SPECULATIVE) {
+        if ((rc = launch(h, zg::Kind::kStepSpec, vec8, a, s, "step"))) return rc;
+        if ((rc = launch(h, zg::Kind::kRollbackReplicas, vec8, a, s, "rollback"))) return rc;
+        count(h, 2 * N * P + 12 * P, 12 * P + 2 * N * P);
+        return ZERO_OK;
+    }
+    if (mode == ZERO_MODE_TWO_PASS_WS) {
+        if ((rc = ensure_ghat(h))) return rc;
+        a.ws = h->ws;
+        if ((rc = launch(h, zg::Kind::kReduceWs, vec8, a, s, "reduce"))) return rc;
+        if (h->stage == 0) {
+            if ((rc = launch(h, zg::Kind::kApplyStage0, vec8, a, s, "apply"))) return rc;
+            count(h, 2 * N * P + 4 * P + 12 * N * P, 4 * P + 12 * N * P + 2 * N * P);
+        } else {
+            if ((rc = launch(h, zg::Kind::kApplyWs, vec8, a, s, "apply"))) return rc;
+            count(h, 2 * N * P + 4 * P + 12 * P, 4 * P + 12 * P + 2 * N * P);
+        }
+        return ZERO_OK;
+    }
+    // TWO_PASS_REREAD
+    if ((rc = launch(h, zg::Kind::kReduceNoWs, vec8, a, s, "reduce"))) return rc;
+    if ((rc = launch(h, zg::Kind::kApplyReread, vec8, a, s, "apply"))) return rc;
+    count(h, 4 * N * P + 12 * P, 12 * P + 2 * N * P);
+    return ZERO_OK;
+}
+
+int zero_gather_bucket(zero_handle_t h, uint64_t a0, uint64_t b0, const void* shard16, void* const* out,
+                       void* stream) {
+    if (!h) return fail(nullptr, ZERO_EINVAL, "handle is NULL");
+    if (h->stage != 3) return fail(h, ZERO_EINVAL, "zero_gather_bucket is for stage 3");
+    if (a0 > b0 || b0 > h->psi_pad) return fail(h, ZERO_EINVAL, "bucket must satisfy 0 <= a <= b <= psi_pad");
+    const uint64_t L = b0 - a0, N = static_cast<uint64_t>(h->n);
+    if (L == 0) {
+        count(h, 0, 0);
+        return ZERO_OK;
+    }
+    int rc = check_ptr(h, shard16, "shard16");
+    if (rc) return rc;
+    if (!out) return fail(h, ZERO_EINVAL, "out is NULL");
+    zg::Args a = base_args(h, nullptr);
+    a.grads[0] = shard16;
+    for (int r = 0; r < h->n; ++r) {
+        if ((rc = check_ptr(h, out[r], "out[r]"))) return rc;
+        a.params[r] = out[r];
+    }
+    a.base = a0;
+    a.count = L;
+    const bool vec8 = (a0 % 8) == 0 && (L % 8) == 0;
+    if ((rc = launch(h, zg::Kind::kGather, vec8, a, static_cast<cudaStream_t>(stream), "gather"))) return rc;
+    count(h, 2 * L, 2 * N * L);
+    return ZERO_OK;
+}
+
+int zero_reduce_scatter_bucket(zero_handle_t h, uint64_t a0, uint64_t b0, const void* const* grads,
+                               float* master, float* m, float* v, void* shard16, const zero_hyper_t* hyper,
+                               void* stream) {
+    if (!h) return fail(nullptr, ZERO_EINVAL, "handle is NULL");
+    if (h->stage != 3) return fail(h, ZERO_EINVAL, "zero_reduce_scatter_bucket is for stage 3");
+    int rc = check_hyper(h, hyper);
+    if (rc) return rc;
+    if (a0 > b0 || b0 > h->psi_pad) return fail(h, ZERO_EINVAL, "bucket must satisfy 0 <= a <= b <= psi_pad");
+    const uint64_t L = b0 - a0, N = static_cast<uint64_t>(h->n);
+    for (auto& iv : h->covered)
+        if (a0 < iv.second && iv.first < b0)
+            return fail(h, ZERO_ESTATE, "bucket overlaps one already reduced this step");
+    if (h->rs_calls >= zg::kMaxBuckets) return fail(h, ZERO_ESTATE, "more than 4096 buckets in one step");
+    int mode = 0;
+    if (h->rs_calls == 0) {
+        if ((rc = resolve_mode(h, hyper, &mode))) return rc;
+    } else {
+        if (!same_hyper(*hyper, h->rs_hyper))
+            return fail(h, ZERO_EINVAL, "every reduce-scatter of one step must pass the same hyper");
+        mode = h->rs_mode;
+    }
+    if (L == 0) {
+        count(h, 0, 0);
+        return ZERO_OK;
+    }
+    if (!grads) return fail(h, ZERO_EINVAL, "grads is NULL");
+    zg::Args a = base_args(h, hyper);
+    for (int r = 0; r < h->n; ++r) {
+        if ((rc = check_ptr(h, grads[r], "grads[r]"))) return rc;
+        a.grads[r] = grads[r];
+    }
+    const bool spec = mode == ZERO_MODE_SPECULATIVE;
+    if (spec) {
+        if ((rc = check_ptr(h, master, "master")) || (rc = check_ptr(h, m, "m")) || (rc = check_ptr(h, v, "v")) ||
+            (rc = check_ptr(h, shard16, "shard16")))
+            return rc;
+    } else {
+        if ((rc = ensure_ghat(h))) return rc;
+    }
+    a.master = master;
+    a.m = m;
+    a.v = v;
+    a.params[0] = shard16;
+    a.ws = h->ws;
+    a.slot_stride = double_buffered(h) ? h->psi_pad : 0;
+    a.base = a0;
+    a.count = L;
+    a.bucket_index = h->rs_calls;
+    const bool vec8 = (a0 % 8) == 0 && (L % 8) == 0;
+    if ((rc = launch(h, spec ? zg::Kind::kRsSpec : zg::Kind::kRsWs, vec8, a, static_cast<cudaStream_t>(stream),
+                     "reduce-scatter")))
+        return rc;
+    if (h->rs_calls == 0) {
+        h->rs_mode = mode;
+        h->rs_hyper = *hyper;
+    }
+    h->rs_calls += 1;
+    h->covered.emplace_back(a0, b0);
+    if (spec) count(h, 2 * N * L + 12 * L, 12 * L + 2 * L);
+    else count(h, 2 * N * L, 4 * L);
+    return ZERO_OK;
+}
+
+int zero_get_status(zero_handle_t h, void* stream, zero_result_t* out) {
+    if (!h) return fail(nullptr, ZERO_EINVAL, "handle is NULL");
+    if (!out) return fail(h, ZERO_EINVAL, "out is NULL");
+    zg::DevStatus st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(&st, h->ws.status, sizeof(st), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "status read");
+    out->overflow = st.overflow;
+    out->applied = st.applied;
+    out->state_slot = st.live_slot;
+    out->error = st.error;
+    out->grad_norm = st.norm;
+    out->clip_coef = st.clip_coef;
+    out->loss_scale = st.loss_scale;
+    out->reserved = 0.0f;
+    out->steps_applied = st.t;
+    out->steps_skipped = st.skipped;
+    return ZERO_OK;
+}
+
+int zero_bytes_moved(zero_handle_t h, zero_bytes_t* out) {
+    if (!h) return fail(nullptr, ZERO_EINVAL, "handle is NULL");
+    if (!out) return fail(h, ZERO_EINVAL, "out is NULL");
+    const uint64_t P = h->psi_pad, N = static_cast<uint64_t>(h->n);
+    out->psi = h->psi;
+    out->psi_pad = P;
+    out->shard = h->shard;
+    out->n_ranks = N;
+    out->stage = static_cast<uint64_t>(h->stage);
+    switch (h->stage) {
+        case 0: out->model_state_bytes_per_rank = 16 * P; break;
+        case 1: out->model_state_bytes_per_rank = 4 * P + 12 * P / N; break;
+        case 2: out->model_state_bytes_per_rank = 2 * P + 14 * P / N; break;
+        default: out->model_state_bytes_per_rank = 16 * P / N; break;
+    }
+    out->comm_elems_paper = (h->stage == 3 ? 3 : 2) * P;
+    out->comm_elems_ring = (h->stage == 3 ? 3 : 2) * (P / N) * (N - 1);
+    out->hbm_read_bytes = h->last_r;
+    out->hbm_write_bytes = h->last_w;
+    out->hbm_read_total = h->tot_r;
+    out->hbm_write_total = h->tot_w;
+    return ZERO_OK;
+}
+
+const char* zero_last_error(zero_handle_t h) {
+    if (!h) return g_init_error.c_str();
+    return h->err.c_str();
+}
+
+void zero_destroy(zero_handle_t h) {
+    if (!h) return;
+    int prev = 0;
+    cudaGetDevice(&prev);
+    cudaSetDevice(h->device);
+    cudaDeviceSynchronize();
+    if (h->ws.ghat) cudaFree(h->ws.ghat);
+    if (h->ws_block) cudaFree(h->ws_block);
+    cudaSetDevice(prev);
+    delete h;
+}
+
+}  // extern "C"

@@ -1,0 +1,98 @@
+// Internal types shared by the host C ABI (zero_api.cpp) and the kernels
+// (zero_kernels.cu).  Not part of the public interface.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace zg {
+
+constexpr int kMaxRanks = 64;
+constexpr int kMaxBlocks = 4096;    // per-block norm partials of one launch
+constexpr int kMaxBuckets = 4096;   // reduce-scatter calls of one ZeRO-3 step
+constexpr int kThreads = 256;
+
+enum Dtype : int { kFp16 = 0, kBf16 = 1 };
+
+// Adam coefficients of one step, each rounded once to fp32 from double.
+struct StepScalars {
+    float b1, b2, a1, a2, eps, dfac, step_size, bc2s;
+};
+
+struct HyperDev {
+    float lr, beta1, beta2, eps, weight_decay, max_norm;
+};
+
+// Device-resident state of a handle.  Written only by the last block of a
+// step's reducing kernel (or by the one-block finaliser), read by the next
+// kernels on the stream.
+struct DevStatus {
+    float loss_scale;
+    int32_t live_slot;
+    int64_t t;          // applied steps
+    int64_t skipped;
+    int32_t overflow;
+    int32_t applied;
+    double norm;
+    double clip_coef;   // fp32 factor applied, as double (1.0 when none)
+    float clip_f;
+    int32_t use_clip;
+    int32_t error;
+    int32_t pad0;
+    StepScalars sc;     // coefficients of the step being applied (two-pass)
+    uint32_t ticket;    // last-block counter; returns to 0 after every launch
+    uint32_t pad1;
+};
+
+struct Workspace {
+    DevStatus* status;
+    double* partials;      // [kMaxBlocks]
+    int32_t* flags;        // [kMaxBlocks]
+    double* bucket_norm;   // [kMaxBuckets]
+    int32_t* bucket_flag;  // [kMaxBuckets]
+    float* ghat;           // [psi_pad] fp32 averaged gradient, or null
+};
+
+// Everything a launch needs, passed by value as a __grid_constant__ param.
+struct Args {
+    const void* grads[kMaxRanks];  // N rank buffers (16-bit)
+    void* params[kMaxRanks];       // N replicas, or [0] = 16-bit shard
+    int n_ranks;
+    int stage;
+    uint64_t psi;        // real elements; global indices >= psi are padding
+    uint64_t psi_pad;
+    uint64_t base;       // global index of the launch's first element
+    uint64_t count;      // elements processed by the launch
+    float* master;       // slot 0 (or replica 0 for stage 0)
+    float* m;
+    float* v;
+    uint64_t slot_stride;  // floats between state slots (double buffer), else 0
+    HyperDev hyper;
+    Workspace ws;
+    int bucket_index;
+    int use_div;         // 1: N*scale is not a power of two -> IEEE divide
+};
+
+enum class Kind : int {
+    kStepSpec,        // stages 1/2: one pass, shadow slot
+    kReduceWs,        // two-pass pass 1, writes g_hat to workspace
+    kReduceNoWs,      // two-pass pass 1, norm/flag only
+    kApplyWs,         // two-pass pass 2 from workspace -> replicas
+    kApplyReread,     // two-pass pass 2 re-reducing grads -> replicas
+    kApplyWsShard,    // stage 3 two-pass pass 2 -> 16-bit shard
+    kApplyStage0,     // stage 0 pass 2: N state replicas
+    kRollbackReplicas,
+    kRollbackShard,
+    kGather,
+    kRsSpec,          // stage 3 bucket reduce-scatter + fused speculative Adam
+    kRsWs,            // stage 3 bucket reduce-scatter into the workspace
+};
+
+// Launchers (zero_kernels.cu).  Return the cudaError_t of the launch.
+cudaError_t launch(Kind kind, int dtype, bool vec8, const Args& a, cudaStream_t s, int* grid_out);
+cudaError_t launch_finalize3(bool spec, const Args& a, cudaStream_t s);
+cudaError_t launch_set_scaler(DevStatus* st, float loss_scale, int64_t t, int32_t slot, cudaStream_t s);
+
+}  // namespace zg

@@ -1,0 +1,681 @@
+// Kernels of the partitioned mixed-precision ZeRO step, written for sm_103a.
+//
+// The N simulated ranks of the method live in one GPU's HBM, so each
+// collective becomes an HBM stream fused into an update kernel:
+//   reduce-scatter  -> every thread reads the N ranks' 16-bit gradients of
+//                      its 8 elements and sums them in rank order in fp32;
+//   scalar all-reduce of the norm and overflow flag -> per-block partials
+//                      that the last block to finish reduces in a fixed
+//                      order (a ticket counter, no spinning);
+//   all-gather / broadcast -> the thread writes the RNE-cast 16-bit result
+//                      to all N replicas.
+// Every kernel is an HBM-bound stream: 128-bit loads and stores of
+// contiguous 8-element groups, grid-stride over a persistent grid sized
+// from the SM count and the kernel's occupancy.  There is no contraction,
+// so no tensor-core path.
+//
+// Arithmetic follows the method exactly as the CPU oracle states it: fp32
+// operations each rounded once (explicit _rn intrinsics, built with
+// -fmad=false), ranks summed from +0 in order 0..N-1, IEEE divide and
+// square root, round-to-nearest-even casts.  Sources, by page and section:
+// "ZeRO: Memory Optimizations Toward Training Trillion Parameter Models"
+// (summary) Sec. 3.1, Sec. 5, Sec. 7 and the residual-state discussion of
+// the flattened gradient-norm buffer; "CMU 11-868 L18" ZeRO-1/2/3 call
+// sequences; "zero-stages-simulation" README partition and schedule.
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "zero_internal.h"
+
+namespace zg {
+namespace {
+
+// ------------------------------------------------------------------ 16-bit
+template <int DT>
+__device__ __forceinline__ float widen(uint32_t bits16);
+template <>
+__device__ __forceinline__ float widen<kFp16>(uint32_t b) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(b)));
+}
+template <>
+__device__ __forceinline__ float widen<kBf16>(uint32_t b) {
+    return __uint_as_float(b << 16);
+}
+
+template <int DT>
+__device__ __forceinline__ uint32_t narrow(float x);
+template <>
+__device__ __forceinline__ uint32_t narrow<kFp16>(float x) {
+    return __half_as_ushort(__float2half_rn(x));
+}
+template <>
+__device__ __forceinline__ uint32_t narrow<kBf16>(float x) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+
+// W consecutive 16-bit values at element index i of buffer p.
+template <int W>
+struct Io;
+
+template <>
+struct Io<8> {
+    __device__ static __forceinline__ void ld16(const void* p, uint64_t i, uint32_t (&out)[8]) {
+        const uint4 x = __ldcs(reinterpret_cast<const uint4*>(p) + (i >> 3));
+        out[0] = x.x & 0xFFFFu; out[1] = x.x >> 16;
+        out[2] = x.y & 0xFFFFu; out[3] = x.y >> 16;
+        out[4] = x.z & 0xFFFFu; out[5] = x.z >> 16;
+        out[6] = x.w & 0xFFFFu; out[7] = x.w >> 16;
+    }
+    __device__ static __forceinline__ void st16(void* p, uint64_t i, const uint32_t (&q)[8]) {
+        uint4 x;
+        x.x = q[0] | (q[1] << 16); x.y = q[2] | (q[3] << 16);
+        x.z = q[4] | (q[5] << 16); x.w = q[6] | (q[7] << 16);
+        __stcs(reinterpret_cast<uint4*>(p) + (i >> 3), x);
+    }
+    __device__ static __forceinline__ void ldf(const float* p, uint64_t i, float (&out)[8]) {
+        const float4 a = __ldcs(reinterpret_cast<const float4*>(p + i));
+        const float4 b = __ldcs(reinterpret_cast<const float4*>(p + i) + 1);
+        out[0] = a.x; out[1] = a.y; out[2] = a.z; out[3] = a.w;
+        out[4] = b.x; out[5] = b.y; out[6] = b.z; out[7] = b.w;
+    }
+    __device__ static __forceinline__ void stf(float* p, uint64_t i, const float (&x)[8]) {
+        __stcs(reinterpret_cast<float4*>(p + i), make_float4(x[0], x[1], x[2], x[3]));
+        __stcs(reinterpret_cast<float4*>(p + i) + 1, make_float4(x[4], x[5], x[6], x[7]));
+    }
+};
+
+template <>
+struct Io<1> {
+    __device__ static __forceinline__ void ld16(const void* p, uint64_t i, uint32_t (&out)[1]) {
+        out[0] = __ldcs(reinterpret_cast<const unsigned short*>(p) + i);
+    }
+    __device__ static __forceinline__ void st16(void* p, uint64_t i, const uint32_t (&q)[1]) {
+        __stcs(reinterpret_cast<unsigned short*>(p) + i, static_cast<unsigned short>(q[0]));
+    }
+    __device__ static __forceinline__ void ldf(const float* p, uint64_t i, float (&out)[1]) {
+        out[0] = __ldcs(p + i);
+    }
+    __device__ static __forceinline__ void stf(float* p, uint64_t i, const float (&x)[1]) {
+        __stcs(p + i, x[0]);
+    }
+};
+
+// ------------------------------------------------------------------ scalars
+// Adam coefficients of step t, formed in double and rounded once to fp32.
+__device__ StepScalars make_scalars(const HyperDev& h, int64_t t) {
+    const double lr = h.lr, b1 = h.beta1, b2 = h.beta2, wd = h.weight_decay;
+    const double bc1 = __dsub_rn(1.0, pow(b1, static_cast<double>(t)));
+    const double bc2 = __dsub_rn(1.0, pow(b2, static_cast<double>(t)));
+    StepScalars s;
+    s.b1 = h.beta1;
+    s.b2 = h.beta2;
+    s.a1 = __double2float_rn(__dsub_rn(1.0, b1));
+    s.a2 = __double2float_rn(__dsub_rn(1.0, b2));
+    s.eps = h.eps;
+    s.dfac = __double2float_rn(__dsub_rn(1.0, __dmul_rn(lr, wd)));
+    s.step_size = __double2float_rn(__ddiv_rn(lr, bc1));
+    s.bc2s = __double2float_rn(__dsqrt_rn(bc2));
+    return s;
+}
+
+// One AdamW update, each operation rounded once, in the oracle's order.
+__device__ __forceinline__ void adam1(float g, float& p, float& m, float& v, const StepScalars& c) {
+    p = __fmul_rn(p, c.dfac);
+    m = __fadd_rn(__fmul_rn(c.b1, m), __fmul_rn(c.a1, g));
+    v = __fadd_rn(__fmul_rn(c.b2, v), __fmul_rn(c.a2, __fmul_rn(g, g)));
+    const float den = __fadd_rn(__fdiv_rn(__fsqrt_rn(v), c.bc2s), c.eps);
+    p = __fsub_rn(p, __fmul_rn(c.step_size, __fdiv_rn(m, den)));
+}
+
+__device__ __forceinline__ bool nonfinite(float x) {
+    return (__float_as_uint(x) & 0x7F800000u) == 0x7F800000u;
+}
+
+// Per-block view of the device status, read once by thread 0.
+struct Pro {
+    StepScalars sc;
+    float den, inv, clip_f;
+    int use_div, live, use_clip, overflow;
+};
+
+// Prologue of kernels that reduce gradients: unscale denominator N*scale
+// (fp32 product, as the oracle forms it) and, for the one-pass kernels,
+// the Adam coefficients of step t+1.
+__device__ __forceinline__ void prologue_reduce(const Args& a, Pro& pro, bool with_scalars) {
+    if (threadIdx.x == 0) {
+        const DevStatus* st = a.ws.status;
+        const float den = __fmul_rn(static_cast<float>(a.n_ranks), st->loss_scale);
+        const uint32_t bits = __float_as_uint(den);
+        const uint32_t ex = (bits >> 23) & 0xFFu;
+        // a power of two whose reciprocal is a normal number: s*inv == s/den exactly
+        const bool pow2 = (bits & 0x7FFFFFu) == 0u && ex >= 1u && ex <= 253u;
+        pro.den = den;
+        pro.use_div = pow2 ? 0 : 1;
+        pro.inv = pow2 ? __fdiv_rn(1.0f, den) : 0.0f;
+        pro.live = st->live_slot;
+        pro.clip_f = st->clip_f;
+        pro.use_clip = st->use_clip;
+        pro.overflow = st->overflow;
+        if (with_scalars) pro.sc = make_scalars(a.hyper, st->t + 1);
+        else pro.sc = st->sc;
+    }
+    __syncthreads();
+}
+
+// Sum of the N ranks' values of W elements at local index j, then unscale.
+template <int DT, int W>
+__device__ __forceinline__ void reduce_group(const Args& a, uint64_t j, const Pro& pro, float (&g)[W]) {
+    float s[W];
+#pragma unroll
+    for (int k = 0; k < W; ++k) s[k] = 0.0f;
+    const int n = a.n_ranks;
+    int r = 0;
+    for (; r + 8 <= n; r += 8) {
+        uint32_t raw[8][W];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) Io<W>::ld16(a.grads[r + q], j, raw[q]);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+#pragma unroll
+            for (int k = 0; k < W; ++k) s[k] = __fadd_rn(s[k], widen<DT>(raw[q][k]));
+    }
+    for (; r < n; ++r) {
+        uint32_t raw[W];
+        Io<W>::ld16(a.grads[r], j, raw);
+#pragma unroll
+        for (int k = 0; k < W; ++k) s[k] = __fadd_rn(s[k], widen<DT>(raw[k]));
+    }
+#pragma unroll
+    for (int k = 0; k < W; ++k) g[k] = pro.use_div ? __fdiv_rn(s[k], pro.den) : __fmul_rn(s[k], pro.inv);
+}
+
+// Squares of the real elements into the thread's fp64 accumulator: an
+// exact product (FMA error term) and a compensated fp32 sum per group, then
+// one fp64 add, so the result carries ~1e-14 relative error.
+template <int W>
+__device__ __forceinline__ void norm_group(const float (&g)[W], int valid, double& acc, int& bad) {
+    float hi = 0.0f, lo = 0.0f;
+#pragma unroll
+    for (int k = 0; k < W; ++k) {
+        if (k < valid) {
+            const float x = g[k];
+            bad |= nonfinite(x) ? 1 : 0;
+            const float p = __fmul_rn(x, x);
+            const float e = __fmaf_rn(x, x, -p);
+            const float s = __fadd_rn(hi, p);
+            const float bp = __fsub_rn(s, hi);
+            const float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bp)), __fsub_rn(p, bp));
+            hi = s;
+            lo = __fadd_rn(lo, __fadd_rn(err, e));
+        }
+    }
+    acc = __dadd_rn(acc, __dadd_rn(static_cast<double>(hi), static_cast<double>(lo)));
+}
+
+__device__ __forceinline__ int valid_count(uint64_t gi, int W, uint64_t psi) {
+    if (gi + W <= psi) return W;
+    if (gi >= psi) return 0;
+    return static_cast<int>(psi - gi);
+}
+
+// Deterministic block sum (fixed shuffle tree, then warp sums in order).
+__device__ double block_sum(double x) {
+    __shared__ double sm[kThreads / 32];
+    __syncthreads();
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) x = __dadd_rn(x, __shfl_down_sync(0xFFFFFFFFu, x, off));
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) sm[warp] = x;
+    __syncthreads();
+    double t = 0.0;
+    if (threadIdx.x == 0) {
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t = __dadd_rn(t, sm[w]);
+    }
+    return t;  // valid in thread 0
+}
+
+// Publish the block's partial; true in every thread of the last block.
+__device__ bool publish(const Args& a, double blk, int flag, double* slot_norm, int32_t* slot_flag) {
+    __shared__ int s_last;
+    if (threadIdx.x == 0) {
+        slot_norm[blockIdx.x] = blk;
+        slot_flag[blockIdx.x] = flag;
+        __threadfence();
+        const unsigned prev = atomicAdd(&a.ws.status->ticket, 1u);
+        s_last = (prev == gridDim.x - 1) ? 1 : 0;
+    }
+    __syncthreads();
+    return s_last != 0;
+}
+
+// In the last block: fixed-order sum of all blocks' partials.
+__device__ void gather_partials(const double* slot_norm, const int32_t* slot_flag, int count,
+                                double& q, int& flag) {
+    __threadfence();
+    double s = 0.0;
+    int f = 0;
+    for (int b = threadIdx.x; b < count; b += blockDim.x) {
+        s = __dadd_rn(s, *reinterpret_cast<const volatile double*>(slot_norm + b));
+        f |= *reinterpret_cast<const volatile int32_t*>(slot_flag + b);
+    }
+    q = block_sum(s);
+    flag = __syncthreads_or(f);
+}
+
+// Overflow: skip.  The scale halves (floor 1.0); t and the state stay.
+__device__ void status_skip(DevStatus* st, double q) {
+    st->overflow = 1;
+    st->applied = 0;
+    st->norm = __dsqrt_rn(q);
+    st->clip_coef = 1.0;
+    st->clip_f = 1.0f;
+    st->use_clip = 0;
+    st->loss_scale = fmaxf(__fmul_rn(st->loss_scale, 0.5f), 1.0f);
+    st->skipped += 1;
+}
+
+// Speculative pass done without overflow: the shadow slot becomes live.
+__device__ void status_commit_spec(DevStatus* st, double q) {
+    st->overflow = 0;
+    st->applied = 1;
+    st->norm = __dsqrt_rn(q);
+    st->clip_coef = 1.0;
+    st->clip_f = 1.0f;
+    st->use_clip = 0;
+    st->live_slot ^= 1;
+    st->t += 1;
+}
+
+// Two-pass decision before the apply pass: clip factor and step t+1 scalars.
+__device__ void status_decide_two_pass(DevStatus* st, double q, const HyperDev& h) {
+    const double norm = __dsqrt_rn(q);
+    st->overflow = 0;
+    st->applied = 1;
+    st->norm = norm;
+    st->use_clip = 0;
+    st->clip_f = 1.0f;
+    if (h.max_norm > 0.0f) {
+        const double c = __ddiv_rn(static_cast<double>(h.max_norm), __dadd_rn(norm, 1e-6));
+        if (c < 1.0) {
+            st->use_clip = 1;
+            st->clip_f = __double2float_rn(c);
+        }
+    }
+    st->clip_coef = static_cast<double>(st->clip_f);
+    st->t += 1;
+    st->sc = make_scalars(h, st->t);
+}
+
+__device__ __forceinline__ uint64_t grid_threads() {
+    return static_cast<uint64_t>(gridDim.x) * blockDim.x;
+}
+__device__ __forceinline__ uint64_t thread_id() {
+    return static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+}
+
+// ------------------------------------------------------------------ kernels
+// Stages 1/2, one pass: reduce-scatter + unscale + flag + norm partial +
+// AdamW from the live slot into the shadow slot + cast + all-gather.  The
+// last block commits the shadow slot, or records the overflow (the
+// rollback kernel then restores the replicas).
+template <int DT, int W>
+__global__ void __launch_bounds__(kThreads) k_step_spec(const __grid_constant__ Args a) {
+    __shared__ Pro pro;
+    prologue_reduce(a, pro, true);
+    const uint64_t src = static_cast<uint64_t>(pro.live) * a.slot_stride;
+    const uint64_t dst = static_cast<uint64_t>(pro.live ^ 1) * a.slot_stride;
+    const uint64_t nvec = a.count / W;
+    double acc = 0.0;
+    int bad = 0;
+    for (uint64_t vi = thread_id(); vi < nvec; vi += grid_threads()) {
+        const uint64_t gi = vi * W;
+        float g[W], p[W], m[W], v[W];
+        reduce_group<DT, W>(a, gi, pro, g);
+        Io<W>::ldf(a.master + src, gi, p);
+        Io<W>::ldf(a.m + src, gi, m);
+        Io<W>::ldf(a.v + src, gi, v);
+        const int valid = valid_count(gi, W, a.psi);
+        norm_group<W>(g, valid, acc, bad);
+        uint32_t q[W];
+#pragma unroll
+        for (int k = 0; k < W; ++k) {
+            if (k < valid) {
+                adam1(g[k], p[k], m[k], v[k], pro.sc);
+            } else {
+                p[k] = 0.0f; m[k] = 0.0f; v[k] = 0.0f;
+            }
+            q[k] = narrow<DT>(p[k]);
+        }
+        Io<W>::stf(a.master + dst, gi, p);
+        Io<W>::stf(a.m + dst, gi, m);
+        Io<W>::stf(a.v + dst, gi, v);
+        for (int r = 0; r < a.n_ranks; ++r) Io<W>::st16(a.params[r], gi, q);
+    }
+    const double blk = block_sum(acc);
+    const int flag = __syncthreads_or(bad);
+    if (publish(a, blk, flag, a.ws.partials, a.ws.flags)) {
+        double qsum;
+        int f;
+        gather_partials(a.ws.partials, a.ws.flags, gridDim.x, qsum, f);
+        if (threadIdx.x == 0) {
+            DevStatus* st = a.ws.status;
+            if (f) status_skip(st, qsum);
+            else status_commit_spec(st, qsum);
+            st->ticket = 0u;
+        }
+    }
+}
+
+// Two-pass, pass 1: reduce + unscale + flag + norm partial (+ fp32 g_hat to
+// the workspace).  The last block decides: skip, or clip factor and step
+// scalars for pass 2.
+template <int DT, int W, bool WS>
+__global__ void __launch_bounds__(kThreads) k_reduce(const __grid_constant__ Args a) {
+    __shared__ Pro pro;
+    prologue_reduce(a, pro, false);
+    const uint64_t nvec = a.count / W;
+    double acc = 0.0;
+    int bad = 0;
+    for (uint64_t vi = thread_id(); vi < nvec; vi += grid_threads()) {
+        const uint64_t gi = vi * W;
+        float g[W];
+        reduce_group<DT, W>(a, gi, pro, g);
+        const int valid = valid_count(gi, W, a.psi);
+        norm_group<W>(g, valid, acc, bad);
+        if (WS) {
+#pragma unroll
+            for (int k = 0; k < W; ++k)
+                if (k >= valid) g[k] = 0.0f;
+            Io<W>::stf(a.ws.ghat, gi, g);
+        }
+    }
+    const double blk = block_sum(acc);
+    const int flag = __syncthreads_or(bad);
+    if (publish(a, blk, flag, a.ws.partials, a.ws.flags)) {
+        double qsum;
+        int f;
+        gather_partials(a.ws.partials, a.ws.flags, gridDim.x, qsum, f);
+        if (threadIdx.x == 0) {
+            DevStatus* st = a.ws.status;
+            if (f) status_skip(st, qsum);
+            else status_decide_two_pass(st, qsum, a.hyper);
+            st->ticket = 0u;
+        }
+    }
+}
+
+// Two-pass, pass 2 (stages 1/2/3): skip on overflow; else AdamW in place on
+// the live slot with g_hat from the workspace (SRC_WS) or re-reduced from
+// the N gradients, clipped if decided, then the 16-bit result to the N
+// replicas (stages 1/2) or to the shard (stage 3, TO_SHARD).
+template <int DT, int W, bool SRC_WS, bool TO_SHARD>
+__global__ void __launch_bounds__(kThreads) k_apply(const __grid_constant__ Args a) {
+    __shared__ Pro pro;
+    prologue_reduce(a, pro, false);
+    if (pro.overflow) return;
+    const uint64_t off = static_cast<uint64_t>(pro.live) * a.slot_stride;
+    const uint64_t nvec = a.count / W;
+    for (uint64_t vi = thread_id(); vi < nvec; vi += grid_threads()) {
+        const uint64_t gi = vi * W;
+        float g[W], p[W], m[W], v[W];
+        if (SRC_WS) Io<W>::ldf(a.ws.ghat, gi, g);
+        else reduce_group<DT, W>(a, gi, pro, g);
+        Io<W>::ldf(a.master + off, gi, p);
+        Io<W>::ldf(a.m + off, gi, m);
+        Io<W>::ldf(a.v + off, gi, v);
+        const int valid = valid_count(gi, W, a.psi);
+        uint32_t q[W];
+#pragma unroll
+        for (int k = 0; k < W; ++k) {
+            if (k < valid) {
+                const float gk = pro.use_clip ? __fmul_rn(g[k], pro.clip_f) : g[k];
+                adam1(gk, p[k], m[k], v[k], pro.sc);
+            } else {
+                p[k] = 0.0f; m[k] = 0.0f; v[k] = 0.0f;
+            }
+            q[k] = narrow<DT>(p[k]);
+        }
+        Io<W>::stf(a.master + off, gi, p);
+        Io<W>::stf(a.m + off, gi, m);
+        Io<W>::stf(a.v + off, gi, v);
+        if (TO_SHARD) {
+            Io<W>::st16(a.params[0], gi, q);
+        } else {
+            for (int r = 0; r < a.n_ranks; ++r) Io<W>::st16(a.params[r], gi, q);
+        }
+    }
+}
+
+// Stage 0, pass 2: every rank holds the full averaged gradient and its own
+// full replica of master/m/v (rank r at r*psi_pad) and updates all of it.
+template <int DT, int W>
+__global__ void __launch_bounds__(kThreads) k_apply_stage0(const __grid_constant__ Args a) {
+    __shared__ Pro pro;
+    prologue_reduce(a, pro, false);
+    if (pro.overflow) return;
+    const uint64_t nvec = a.count / W;
+    for (uint64_t vi = thread_id(); vi < nvec; vi += grid_threads()) {
+        const uint64_t gi = vi * W;
+        float g[W];
+        Io<W>::ldf(a.ws.ghat, gi, g);
+        const int valid = valid_count(gi, W, a.psi);
+#pragma unroll
+        for (int k = 0; k < W; ++k)
+            if (k < valid && pro.use_clip) g[k] = __fmul_rn(g[k], pro.clip_f);
+        for (int r = 0; r < a.n_ranks; ++r) {
+            const uint64_t ri = static_cast<uint64_t>(r) * a.psi_pad + gi;
+            float p[W], m[W], v[W];
+            Io<W>::ldf(a.master, ri, p);
+            Io<W>::ldf(a.m, ri, m);
+            Io<W>::ldf(a.v, ri, v);
+            uint32_t q[W];
+#pragma unroll
+            for (int k = 0; k < W; ++k) {
+                if (k < valid) {
+                    adam1(g[k], p[k], m[k], v[k], pro.sc);
+                } else {
+                    p[k] = 0.0f; m[k] = 0.0f; v[k] = 0.0f;
+                }
+                q[k] = narrow<DT>(p[k]);
+            }
+            Io<W>::stf(a.master, ri, p);
+            Io<W>::stf(a.m, ri, m);
+            Io<W>::stf(a.v, ri, v);
+            Io<W>::st16(a.params[r], gi, q);
+        }
+    }
+}
+
+// After a speculative pass: when the step overflowed, rewrite the 16-bit
+// copies from the live (old) master; otherwise exit at once.
+template <int DT, int W, bool TO_SHARD>
+__global__ void __launch_bounds__(kThreads) k_rollback(const __grid_constant__ Args a) {
+    const DevStatus* st = a.ws.status;
+    if (!st->overflow) return;
+    const uint64_t off = static_cast<uint64_t>(st->live_slot) * a.slot_stride;
+    const uint64_t nvec = a.count / W;
+    for (uint64_t vi = thread_id(); vi < nvec; vi += grid_threads()) {
+        const uint64_t gi = a.base + vi * W;
+        float p[W];
+        Io<W>::ldf(a.master + off, gi, p);
+        uint32_t q[W];
+#pragma unroll
+        for (int k = 0; k < W; ++k) q[k] = narrow<DT>(p[k]);
+        if (TO_SHARD) {
+            Io<W>::st16(a.params[0], gi, q);
+        } else {
+            for (int r = 0; r < a.n_ranks; ++r) Io<W>::st16(a.params[r], gi, q);
+        }
+    }
+}
+
+// ZeRO-3 gather of [base, base+count): out[r][j] = shard[base + j].
+template <int W>
+__global__ void __launch_bounds__(kThreads) k_gather(const __grid_constant__ Args a) {
+    const uint64_t nvec = a.count / W;
+    for (uint64_t vi = thread_id(); vi < nvec; vi += grid_threads()) {
+        const uint64_t j = vi * W;
+        uint32_t x[W];
+        Io<W>::ld16(a.grads[0], a.base + j, x);
+        for (int r = 0; r < a.n_ranks; ++r) Io<W>::st16(a.params[r], j, x);
+    }
+}
+
+// ZeRO-3 reduce-scatter of bucket [base, base+count).  SPEC: the bucket's
+// AdamW update runs here into the shadow slot and the 16-bit shard; else
+// g_hat goes to the workspace.  The last block stores the bucket's norm
+// partial and flag for the step's finaliser.
+template <int DT, int W, bool SPEC>
+__global__ void __launch_bounds__(kThreads) k_rs(const __grid_constant__ Args a) {
+    __shared__ Pro pro;
+    prologue_reduce(a, pro, SPEC);
+    const uint64_t src = static_cast<uint64_t>(pro.live) * a.slot_stride;
+    const uint64_t dst = static_cast<uint64_t>(pro.live ^ 1) * a.slot_stride;
+    const uint64_t nvec = a.count / W;
+    double acc = 0.0;
+    int bad = 0;
+    for (uint64_t vi = thread_id(); vi < nvec; vi += grid_threads()) {
+        const uint64_t j = vi * W;
+        const uint64_t gi = a.base + j;
+        float g[W];
+        reduce_group<DT, W>(a, j, pro, g);
+        const int valid = valid_count(gi, W, a.psi);
+        if (SPEC) {
+            float p[W], m[W], v[W];
+            Io<W>::ldf(a.master + src, gi, p);
+            Io<W>::ldf(a.m + src, gi, m);
+            Io<W>::ldf(a.v + src, gi, v);
+            norm_group<W>(g, valid, acc, bad);
+            uint32_t q[W];
+#pragma unroll
+            for (int k = 0; k < W; ++k) {
+                if (k < valid) {
+                    adam1(g[k], p[k], m[k], v[k], pro.sc);
+                } else {
+                    p[k] = 0.0f; m[k] = 0.0f; v[k] = 0.0f;
+                }
+                q[k] = narrow<DT>(p[k]);
+            }
+            Io<W>::stf(a.master + dst, gi, p);
+            Io<W>::stf(a.m + dst, gi, m);
+            Io<W>::stf(a.v + dst, gi, v);
+            Io<W>::st16(a.params[0], gi, q);
+        } else {
+            norm_group<W>(g, valid, acc, bad);
+#pragma unroll
+            for (int k = 0; k < W; ++k)
+                if (k >= valid) g[k] = 0.0f;
+            Io<W>::stf(a.ws.ghat, gi, g);
+        }
+    }
+    const double blk = block_sum(acc);
+    const int flag = __syncthreads_or(bad);
+    if (publish(a, blk, flag, a.ws.partials, a.ws.flags)) {
+        double qsum;
+        int f;
+        gather_partials(a.ws.partials, a.ws.flags, gridDim.x, qsum, f);
+        if (threadIdx.x == 0) {
+            a.ws.bucket_norm[a.bucket_index] = qsum;
+            a.ws.bucket_flag[a.bucket_index] = f;
+            a.ws.status->ticket = 0u;
+        }
+    }
+}
+
+// ZeRO-3 step finaliser (one block): combine the buckets' partials in call
+// order, then commit / skip (SPEC) or decide clip and scalars (two-pass).
+template <bool SPEC>
+__global__ void __launch_bounds__(kThreads) k_finalize3(const __grid_constant__ Args a) {
+    double q;
+    int f;
+    gather_partials(a.ws.bucket_norm, a.ws.bucket_flag, a.bucket_index, q, f);
+    if (threadIdx.x == 0) {
+        DevStatus* st = a.ws.status;
+        if (f) status_skip(st, q);
+        else if (SPEC) status_commit_spec(st, q);
+        else status_decide_two_pass(st, q, a.hyper);
+    }
+}
+
+__global__ void k_set_scaler(DevStatus* st, float loss_scale, int64_t t, int32_t slot) {
+    st->loss_scale = loss_scale;
+    st->t = t;
+    st->live_slot = slot;
+    st->skipped = 0;
+    st->overflow = 0;
+    st->applied = 0;
+    st->norm = 0.0;
+    st->clip_coef = 1.0;
+    st->clip_f = 1.0f;
+    st->use_clip = 0;
+    st->error = 0;
+    st->ticket = 0u;
+}
+
+// ------------------------------------------------------------------ launch
+template <typename KernelT>
+cudaError_t run(KernelT kernel, const Args& a, uint64_t nvec, cudaStream_t s, int* grid_out) {
+    static int sms = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (sms == 0) {
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+    }
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+    uint64_t want = (nvec + kThreads - 1) / kThreads;
+    uint64_t cap = static_cast<uint64_t>(sms) * static_cast<uint64_t>(per_sm);
+    if (cap > static_cast<uint64_t>(kMaxBlocks)) cap = kMaxBlocks;
+    uint64_t grid = want < cap ? want : cap;
+    if (grid < 1) grid = 1;
+    if (grid_out) *grid_out = static_cast<int>(grid);
+    kernel<<<static_cast<unsigned>(grid), kThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <int DT, int W>
+cudaError_t launch_dw(Kind kind, const Args& a, cudaStream_t s, int* grid_out) {
+    const uint64_t nvec = a.count / W;
+    switch (kind) {
+        case Kind::kStepSpec: return run(k_step_spec<DT, W>, a, nvec, s, grid_out);
+        case Kind::kReduceWs: return run(k_reduce<DT, W, true>, a, nvec, s, grid_out);
+        case Kind::kReduceNoWs: return run(k_reduce<DT, W, false>, a, nvec, s, grid_out);
+        case Kind::kApplyWs: return run(k_apply<DT, W, true, false>, a, nvec, s, grid_out);
+        case Kind::kApplyReread: return run(k_apply<DT, W, false, false>, a, nvec, s, grid_out);
+        case Kind::kApplyWsShard: return run(k_apply<DT, W, true, true>, a, nvec, s, grid_out);
+        case Kind::kApplyStage0: return run(k_apply_stage0<DT, W>, a, nvec, s, grid_out);
+        case Kind::kRollbackReplicas: return run(k_rollback<DT, W, false>, a, nvec, s, grid_out);
+        case Kind::kRollbackShard: return run(k_rollback<DT, W, true>, a, nvec, s, grid_out);
+        case Kind::kGather: return run(k_gather<W>, a, nvec, s, grid_out);
+        case Kind::kRsSpec: return run(k_rs<DT, W, true>, a, nvec, s, grid_out);
+        case Kind::kRsWs: return run(k_rs<DT, W, false>, a, nvec, s, grid_out);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch(Kind kind, int dtype, bool vec8, const Args& a, cudaStream_t s, int* grid_out) {
+    if (dtype == kFp16) {
+        return vec8 ? launch_dw<kFp16, 8>(kind, a, s, grid_out) : launch_dw<kFp16, 1>(kind, a, s, grid_out);
+    }
+    return vec8 ? launch_dw<kBf16, 8>(kind, a, s, grid_out) : launch_dw<kBf16, 1>(kind, a, s, grid_out);
+}
+
+cudaError_t launch_finalize3(bool spec, const Args& a, cudaStream_t s) {
+    if (spec) k_finalize3<true><<<1, kThreads, 0, s>>>(a);
+    else k_finalize3<false><<<1, kThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_set_scaler(DevStatus* st, float loss_scale, int64_t t, int32_t slot, cudaStream_t s) {
+    k_set_scaler<<<1, 1, 0, s>>>(st, loss_scale, t, slot);
+    return cudaGetLastError();
+}
+
+}  // namespace zg
