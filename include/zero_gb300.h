@@ -227,6 +227,48 @@ ZERO_API int zero_get_status(zero_handle_t h, void* stream, zero_result_t* out);
  */
 ZERO_API int zero_bytes_moved(zero_handle_t h, zero_bytes_t* out);
 
+/*
+ * zero_step_noalloc -- the two-pass step of stages 1/2 for callers that
+ * cannot allocate device memory.  The ZeRO pages have no counterpart: this
+ * is a packaging of zero_step for such callers.
+ * Some callers may not call cudaMalloc: code inside a CUDA stream capture
+ * (allocation there is an error in the default capture mode), code in a
+ * framework whose caching allocator owns the device memory (a foreign
+ * cudaMalloc also synchronises the whole device), or code under a memory
+ * budget fixed before training starts.  zero_init_partition allocates a
+ * workspace, so those callers use this call instead.  It takes no handle
+ * and calls no cudaMalloc, cudaFree or other allocating routine.
+ *   Its scratch -- the status word, the per-block norm partials and the
+ *   fp32 averaged gradient -- lives in one static device array of
+ *   ZERO_NOALLOC_MAX_PSI_PAD floats plus 48 KiB and 256 bytes (about
+ *   16 MiB), which every GPU that loads the library holds until the
+ *   process exits.  psi_pad above ZERO_NOALLOC_MAX_PSI_PAD is rejected
+ *   with ZERO_EINVAL.
+ *   The first call on a device looks up that array's device address
+ *   (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   Every call shares the one array and overwrites what the last call left
+ *   there (it clears the status word first): calls that overlap on the GPU,
+ *   from any thread or stream, race and give wrong results.  Order them.
+ * Arguments are those of zero_init_partition and zero_step (stages 1/2,
+ * one state slot, updated in place), plus:
+ *   loss_scale, steps_applied  host values of the loss scale and of t
+ *           before this step (the caller keeps them between calls)
+ *   result  DEVICE pointer (8-byte aligned) receiving the step's
+ *           zero_result_t, stream-ordered: overflow, applied, norm, clip
+ *           factor, the loss scale after this step (halved on overflow,
+ *           floor 1.0), t after this step, and steps_skipped = 1 if this
+ *           call skipped its update (0 otherwise)
+ *   hyper->mode must be ZERO_MODE_AUTO or ZERO_MODE_TWO_PASS_WS.
+ * Errors: EINVAL (read zero_last_error(NULL)), ECUDA.
+ */
+#define ZERO_NOALLOC_MAX_PSI_PAD (1ull << 22)
+
+ZERO_API int zero_step_noalloc(uint64_t psi, int n_ranks, int stage, int dtype, int align,
+                      const void* const* grads, void* const* params,
+                      float* master, float* m, float* v, const zero_hyper_t* hyper,
+                      float loss_scale, int64_t steps_applied, zero_result_t* result,
+                      void* stream);
+
 /* Last error message of this handle (or of the last failed init when h is
  * NULL).  The string is owned by the library and valid until the next call. */
 ZERO_API const char* zero_last_error(zero_handle_t h);

@@ -19,7 +19,7 @@ STATUS_NAMES = {0: "ZERO_OK", 1: "ZERO_EINVAL", 2: "ZERO_ENOMEM", 3: "ZERO_ECUDA
 EXPORTS = (
     "zero_init_partition", "zero_partition_info", "zero_set_scaler", "zero_step",
     "zero_gather_bucket", "zero_reduce_scatter_bucket", "zero_get_status",
-    "zero_bytes_moved", "zero_last_error", "zero_destroy",
+    "zero_bytes_moved", "zero_last_error", "zero_destroy", "zero_step_noalloc",
 )
 
 
@@ -80,6 +80,8 @@ def load_library():
     lib.zero_bytes_moved.argtypes = [P, C.POINTER(Bytes)]
     lib.zero_last_error.argtypes = [P]
     lib.zero_last_error.restype = C.c_char_p
+    lib.zero_step_noalloc.argtypes = [U64, I32, I32, I32, I32, C.POINTER(P), C.POINTER(P), P, P, P,
+                                       C.POINTER(Hyper), C.c_float, C.c_int64, P, P]
     lib.zero_destroy.argtypes = [P]
     lib.zero_destroy.restype = None
     for name in EXPORTS:
@@ -191,6 +193,26 @@ def zero_bytes_moved(h) -> dict:
     b = Bytes()
     _check(load_library().zero_bytes_moved(h, C.byref(b)), h)
     return {f: getattr(b, f) for f, _ in Bytes._fields_}
+
+
+def zero_step_noalloc(psi: int, n_ranks: int, stage: int, dtype: int, align: int, grads, params,
+                      master, m, v, hyp: Hyper, loss_scale: float, steps_applied: int, result, stream=None):
+    """Two-pass step with all scratch in the library's static device array (no allocation).
+
+    result: device tensor of at least 56 bytes (8-byte aligned) that receives the
+    step's zero_result_t; read it with :func:`result_from_device`.
+    """
+    rc = load_library().zero_step_noalloc(psi, n_ranks, stage, dtype, align, _ptr_array(grads),
+                                          _ptr_array(params), _ptr(master), _ptr(m), _ptr(v), C.byref(hyp),
+                                          loss_scale, steps_applied, _ptr(result), _stream(stream))
+    _check(rc, None)
+
+
+def result_from_device(t) -> dict:
+    """Decode a zero_result_t written to a device (or host) uint8 tensor."""
+    raw = bytes(t.view(-1)[:C.sizeof(Result)].cpu().numpy().tobytes())
+    r = Result.from_buffer_copy(raw)
+    return {f: getattr(r, f) for f, _ in Result._fields_ if f != "reserved"}
 
 
 def zero_last_error(h) -> str:

@@ -153,6 +153,8 @@ bool same_hyper(const zero_hyper_t& x, const zero_hyper_t& y) {
 
 }  // namespace
 
+void zg::set_global_error(const char* msg) { g_init_error = msg ? msg : ""; }
+
 extern "C" {
 
 int zero_init_partition(uint64_t psi, int n_ranks, int stage, int dtype, int align, unsigned flags,

@@ -95,4 +95,7 @@ cudaError_t launch(Kind kind, int dtype, bool vec8, const Args& a, cudaStream_t 
 cudaError_t launch_finalize3(bool spec, const Args& a, cudaStream_t s);
 cudaError_t launch_set_scaler(DevStatus* st, float loss_scale, int64_t t, int32_t slot, cudaStream_t s);
 
+// Message returned by zero_last_error(NULL) for calls that take no handle.
+void set_global_error(const char* msg);
+
 }  // namespace zg
