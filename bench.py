@@ -175,10 +175,14 @@ def run_reference(args, ws, rank):
 
 
 # ---------------------------------------------------------------- GPU workloads
-def setup_flat15b(Z, S, torch):
-    """Buffers and four resident gradient sets of the 1.5B stage-1 workload."""
+def setup_flat15b(Z, S, torch, psi=None):
+    """Buffers and four resident gradient sets of the 1.5B stage-1 workload
+    (psi overrides the size for small profiling runs)."""
+    import dataclasses
     from zero_partitioned_mixed_gb300.buffers import RankBuffers
     w = S.FLAT15B
+    if psi is not None and psi != w.psi:
+        w = dataclasses.replace(w, psi=psi, name=f"flat_psi{psi}_n8_stage1_fp16_ls65536")
     buf = RankBuffers(w.psi, w.n_ranks, w.stage, w.dtype, double_buffer=True, alloc_grads=False)
     P = buf.psi_pad
     mv, mm, vv = buf.state(0)
@@ -215,7 +219,7 @@ def run_ours(args, ws, rank, local):
     if ws > 1:
         dist.barrier()
 
-    w, buf, sets = setup_flat15b(Z, S, torch)
+    w, buf, sets = setup_flat15b(Z, S, torch, args.psi)
     N, P = w.n_ranks, buf.psi_pad
     hyp = Z.hyper(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay, w.max_norm, Z.ZERO_MODE_AUTO)
     stream = torch.cuda.current_stream()
@@ -274,7 +278,7 @@ def run_ours(args, ws, rank, local):
         "data": "synthetic",
         "config": {"workload": w.name, "psi": w.psi, "n_ranks": N, "stage": w.stage, "mode": "speculative",
                    "grad_sets": nsets, "overflow_every": f"set {inject_set + 1} of {nsets} (+inf in rank 5)",
-                   "l2": "inputs larger than L2: 84 GB per step, no flush needed",
+                   "l2": f"inputs larger than L2: {alg_bytes / 1e9:.1f} GB per step, no flush needed",
                    "parallelism": "replicas only" if ws > 1 else "1 GPU"},
         "hbm_gbs_applied_step": achieved,
         "ms_per_applied_step": kernel_ms,
@@ -336,8 +340,213 @@ def e2e_flat(args, w, buf, sets, hyp, stream, torch, ws, dist):
             "d2h_bytes_per_step": RESULT_BYTES, "steps": K}
 
 
+# ---------------------------------------------------------------- other workloads
+class CallTimer:
+    """Sums the CUDA-event durations of library calls made on the current stream."""
+
+    def __init__(self, torch):
+        self.torch = torch
+        self.pairs = []
+
+    def __enter__(self):
+        a = self.torch.cuda.Event(enable_timing=True)
+        b = self.torch.cuda.Event(enable_timing=True)
+        a.record()
+        self.cur = (a, b)
+        return self
+
+    def __exit__(self, *exc):
+        self.cur[1].record()
+        self.pairs.append(self.cur)
+        return False
+
+    def total_ms(self):
+        self.torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in self.pairs)
+
+
+def _line(workload, value, ms, steps, warmup, bytes_per_step, dtype, extra=None):
+    peaks, src = measured_peaks()
+    gbs = bytes_per_step / (ms * 1e-3) / 1e9
+    out = {"metric": METRIC, "value": value, "unit": "params/s", "n_gpus": 1, "steps": steps,
+           "warmup": warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f32", "storage_dtype": dtype, "data": "synthetic",
+           "config": {"workload": workload}, "hbm_gbs": gbs,
+           "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                        "frac": gbs / peaks["hbm_gbs"], "algorithmic_bytes_per_step": bytes_per_step,
+                        "peak_source": f"{src} hbm_gbs (copy)"}}
+    if extra:
+        out["config"].update(extra)
+    return out
+
+
+def _bytes_delta(buf, before):
+    b = buf.bytes_moved()
+    return (b["hbm_read_total"] + b["hbm_write_total"]) - before
+
+
+def _bytes_total(buf):
+    b = buf.bytes_moved()
+    return b["hbm_read_total"] + b["hbm_write_total"]
+
+
+def bench_dense(w, stage, steps, warmup, torch, S, Z, flush_l2=False, sets_max=5):
+    """Stages 0-2: resident gradient sets, one zero_step per bench step."""
+    from zero_partitioned_mixed_gb300.buffers import RankBuffers
+    db = stage != 0 and w.max_norm == 0
+    buf = RankBuffers(w.psi, w.n_ranks, stage, w.dtype, double_buffer=db, alloc_grads=False)
+    P, N = buf.psi_pad, w.n_ranks
+    td = S.torch_dtype(w.dtype)
+    mv, mm, vv = buf.state(0)
+    if stage == 0:
+        S.draw_master(w, mv[0], w.psi)
+        S.draw_moments(w, mm[0], vv[0], w.psi)
+        mv[1:].copy_(mv[0].expand(N - 1, P)); mm[1:].copy_(mm[0].expand(N - 1, P)); vv[1:].copy_(vv[0].expand(N - 1, P))
+        buf.params[:, :P].copy_(mv.to(td))
+    else:
+        S.draw_master(w, mv, w.psi)
+        S.draw_moments(w, mm, vv, w.psi)
+        buf.params[:, :P].copy_(mv.to(td).unsqueeze(0).expand(N, P))
+    shapes = S.shapes_of(w)
+    sv = S.fan_in_scale(shapes, "cuda") if (w.fan_in_scaled and shapes) else None
+    nsets = max(1, min(w.steps, sets_max))
+    sets = torch.empty((nsets, N, buf.stride), dtype=td, device="cuda")
+    for k in range(nsets):
+        for r in range(N):
+            S.draw_grads(w, sets[k, r], w.psi, k + 1, r, w.loss_scale, sv)
+    del sv
+    buf.set_scaler(w.loss_scale, 0, 0)
+    hyp = Z.hyper(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay, w.max_norm, Z.ZERO_MODE_AUTO)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda") if flush_l2 else None
+    rows = lambda k: [sets[k, r] for r in range(N)]
+    for i in range(warmup):
+        buf.step(hyp, rows(i % nsets))
+    timer = CallTimer(torch)
+    before = _bytes_total(buf)
+    for i in range(steps):
+        if flush is not None:
+            flush.zero_()
+        with timer:
+            buf.step(hyp, rows((warmup + i) % nsets))
+    ms = timer.total_ms() / steps
+    per_step = _bytes_delta(buf, before) / steps
+    st = buf.status()
+    buf.close()
+    del sets
+    torch.cuda.empty_cache()
+    return ms, per_step, st
+
+
+def bench_stage3(w, buckets, steps, warmup, torch, S, Z, flush_l2=False):
+    """ZeRO-3: per step, gather every bucket (forward), then per bucket in reverse
+    gather again and reduce-scatter, then finish the step.  One drawn gradient
+    buffer of the largest bucket is reused for every bucket (timing only)."""
+    from zero_partitioned_mixed_gb300.buffers import RankBuffers
+    buf = RankBuffers(w.psi, w.n_ranks, 3, w.dtype, double_buffer=(w.max_norm == 0))
+    P, N = buf.psi_pad, w.n_ranks
+    td = S.torch_dtype(w.dtype)
+    mv, mm, vv = buf.state(0)
+    S.draw_master(w, mv, w.psi)
+    S.draw_moments(w, mm, vv, w.psi)
+    buf.params[:P].copy_(mv.to(td))
+    lmax = max(b - a for a, b in buckets)
+    lpad = (lmax + 7) // 8 * 8
+    gbuf = torch.empty((N, lpad), dtype=td, device="cuda")
+    for r in range(N):
+        S.draw_grads(w, gbuf[r], lmax, 1, r, w.loss_scale)
+    outs = torch.empty((N, lpad), dtype=td, device="cuda")
+    buf.set_scaler(w.loss_scale, 0, 0)
+    hyp = Z.hyper(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay, w.max_norm, Z.ZERO_MODE_AUTO)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda") if flush_l2 else None
+    grows = [gbuf[r] for r in range(N)]
+    orows = [outs[r] for r in range(N)]
+
+    def one_step(timer):
+        for (a, b) in buckets:
+            if flush is not None:
+                flush.zero_()
+            with timer:
+                buf.gather(a, b, orows)
+        for (a, b) in reversed(buckets):
+            if flush is not None:
+                flush.zero_()
+            with timer:
+                buf.gather(a, b, orows)
+                buf.reduce_scatter(a, b, grows, hyp)
+        with timer:
+            buf.step(hyp)
+
+    for _ in range(warmup):
+        one_step(CallTimer(torch))
+    torch.cuda.synchronize()
+    timer = CallTimer(torch)
+    before = _bytes_total(buf)
+    for _ in range(steps):
+        one_step(timer)
+    ms = timer.total_ms() / steps
+    per_step = _bytes_delta(buf, before) / steps
+    st = buf.status()
+    buf.close()
+    del gbuf, outs
+    torch.cuda.empty_cache()
+    return ms, per_step, st
+
+
 def run_other(args, ws, rank, local):
-    raise SystemExit(f"workload {args.workload}: not wired yet")
+    import dataclasses
+
+    import torch
+    import zero_partitioned_mixed_gb300 as Z
+    from zero_partitioned_mixed_gb300 import synth as S
+    from zero_partitioned_mixed_gb300.build import build_library
+
+    torch.cuda.set_device(local)
+    build_library()
+    lines = []
+    if args.workload == "toy":
+        base = S.TOY
+        for stage in (0, 1, 2, 3):
+            w = dataclasses.replace(base, stage=stage)
+            if stage == 3:
+                pp = S.flat_buckets(((w.psi + 255) // 256) * 256, w.n_ranks, 50_000)
+                ms, bps, st = bench_stage3(w, pp, args.steps, args.warmup, torch, S, Z, flush_l2=True)
+            else:
+                ms, bps, st = bench_dense(w, stage, args.steps, args.warmup, torch, S, Z, flush_l2=True)
+            lines.append(_line(f"{base.name}_stage{stage}", w.psi / (ms * 1e-3), ms, args.steps, args.warmup,
+                               bps, w.dtype, {"stage": stage, "l2": "256 MiB written between timed calls",
+                                              "note": "L2-resident size: latency-bound, not a roofline point"}))
+    elif args.workload == "gpt2":
+        w = S.GPT2
+        ms, bps, st = bench_dense(w, 2, args.steps, args.warmup, torch, S, Z)
+        lines.append(_line(w.name, w.psi / (ms * 1e-3), ms, args.steps, args.warmup, bps, w.dtype,
+                           {"stage": 2, "mode": "two-pass (clip 1.0)", "l2": "inputs larger than L2"}))
+    elif args.workload == "llama7b":
+        w = S.LLAMA7B
+        buckets = S.layer_buckets(S.llama7b_shapes(), w.psi)
+        ms, bps, st = bench_stage3(w, buckets, args.steps, args.warmup, torch, S, Z)
+        lines.append(_line(w.name, w.psi / (ms * 1e-3), ms, args.steps, args.warmup, bps, w.dtype,
+                           {"stage": 3, "buckets": len(buckets), "mode": "speculative, fused per bucket",
+                            "l2": "inputs larger than L2"}))
+    elif args.workload == "sweep":
+        for psi, n in S.sweep_points():
+            for stage in (1, 2, 3):
+                w = S.Workload(f"sweep_psi{psi}_n{n}_stage{stage}", psi, n, stage, "bf16", 1, grad_sigma=1e-3)
+                flush = psi * (4 * n + 24) < (512 << 20)
+                if stage == 3:
+                    pp = ((psi + n * 8 - 1) // (n * 8)) * (n * 8)
+                    ms, bps, st = bench_stage3(w, S.flat_buckets(pp, n, 50_000_000), args.steps, args.warmup,
+                                               torch, S, Z, flush_l2=flush)
+                else:
+                    ms, bps, st = bench_dense(w, stage, args.steps, args.warmup, torch, S, Z, flush_l2=flush,
+                                              sets_max=1)
+                lines.append(_line(w.name, psi / (ms * 1e-3), ms, args.steps, args.warmup, bps, "bf16",
+                                   {"psi": psi, "n_ranks": n, "stage": stage,
+                                    "l2": "256 MiB written between timed calls" if flush else "inputs larger than L2"}))
+                print(json.dumps(lines[-1]), flush=True)
+        return 0
+    for ln in lines:
+        print(json.dumps(ln), flush=True)
+    return 0
 
 
 def main(argv=None):
@@ -349,6 +558,7 @@ def main(argv=None):
     ap.add_argument("--workload", choices=["flat1.5b", "toy", "gpt2", "llama7b", "sweep"], default="flat1.5b")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--psi", type=int, default=None, help="override psi of the flat workload (profiling)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -202,3 +202,48 @@ def test_state_slot_and_resume():
     assert sa["state_slot"] == sb["state_slot"] == 1
     assert torch.equal(a.master, b.master) and torch.equal(a.params, b.params)
     a.close(); b.close()
+
+
+@pytest.mark.parametrize("stage", [1, 3])
+def test_state_only_16_byte_aligned_takes_the_128_bit_path(stage):
+    # master/m/v 16- but not 32-byte aligned: the kernels fall back to 128-bit
+    # fp32 accesses; results must equal the 256-bit path bit for bit
+    from zero_partitioned_mixed_gb300 import _binding as B
+    from zero_partitioned_mixed_gb300.buffers import RankBuffers
+    psi, n = 100_000, 4
+    a = RankBuffers(psi, n, stage, "bf16")
+    b = RankBuffers(psi, n, stage, "bf16")
+    P = a.psi_pad
+    torch.manual_seed(3)
+    a.master[:psi].normal_(0, 0.02)
+    a.m[:psi].normal_(0, 1e-4)
+    a.v[:psi].normal_(0, 1e-6).abs_()
+    if stage == 3:
+        a.params[:P].copy_(a.master[:P].to(torch.bfloat16))
+    else:
+        a.params[:, :P].copy_(a.master[:P].to(torch.bfloat16))
+    b.params.copy_(a.params)
+    off = {}
+    for name in ("master", "m", "v"):
+        big = torch.zeros(2 * P + 8, dtype=torch.float32, device="cuda")
+        view = big[4:4 + 2 * P]
+        assert view.data_ptr() % 32 == 16
+        view.copy_(getattr(a, name))
+        off[name] = view
+    b.master, b.m, b.v = off["master"], off["m"], off["v"]
+    g = torch.randn((n, a.stride), device="cuda").mul_(1e-2).to(torch.bfloat16)
+    g[:, psi:] = 0
+    h = B.hyper(weight_decay=0.1)
+    for buf in (a, b):
+        if stage == 3:
+            rows = [g[r] for r in range(n)]
+            buf.reduce_scatter(0, P, rows, h)
+            buf.step(h)
+        else:
+            buf.step(h, [g[r] for r in range(n)])
+    torch.cuda.synchronize()
+    assert torch.equal(a.master.view(torch.int32), b.master.view(torch.int32))
+    assert torch.equal(a.m.view(torch.int32), b.m.view(torch.int32))
+    assert torch.equal(a.v.view(torch.int32), b.v.view(torch.int32))
+    assert torch.equal(a.params.view(torch.int16), b.params.view(torch.int16))
+    a.close(); b.close()

@@ -53,7 +53,8 @@ _lib = None
 
 
 def library_path() -> str:
-    return LIB_PATH
+    """libzero_gb300.so to load: $ZERO_GB300_LIB if set, else the in-tree build."""
+    return os.environ.get("ZERO_GB300_LIB", LIB_PATH)
 
 
 def load_library():
@@ -61,14 +62,15 @@ def load_library():
     global _lib
     if _lib is not None:
         return _lib
-    if not os.path.exists(LIB_PATH):
-        raise ZeroError(3, f"{LIB_PATH} is missing: build it with "
+    path = library_path()
+    if not os.path.exists(path):
+        raise ZeroError(3, f"{path} is missing: build it with "
                            "`python -m zero_partitioned_mixed_gb300.build`")
     try:  # make torch's libcudart the one the library binds to, when torch is present
         import torch  # noqa: F401
     except Exception:
         pass
-    lib = C.CDLL(LIB_PATH)
+    lib = C.CDLL(path)
     P, U64, I32 = C.c_void_p, C.c_uint64, C.c_int
     lib.zero_init_partition.argtypes = [U64, I32, I32, I32, I32, C.c_uint, C.POINTER(P)]
     lib.zero_partition_info.argtypes = [P, C.POINTER(U64), C.POINTER(U64), C.POINTER(U64), C.POINTER(U64)]

@@ -125,8 +125,19 @@ zg::Args base_args(const zero_handle* h, const zero_hyper_t* hy) {
     return a;
 }
 
+bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
+
+// 8-wide launches use 256-bit fp32 accesses when every fp32 buffer of the
+// launch is 32-byte aligned (slot and replica strides are multiples of 8
+// floats whenever the 8-wide path runs), else 128-bit ones.
+zg::Vec pick_vec(bool vec8, const zg::Args& a) {
+    if (!vec8) return zg::Vec::k1;
+    const bool s32 = aligned32(a.master) && aligned32(a.m) && aligned32(a.v) && aligned32(a.ws.ghat);
+    return s32 ? zg::Vec::k8s32 : zg::Vec::k8s16;
+}
+
 int launch(zero_handle* h, zg::Kind kind, bool vec8, const zg::Args& a, cudaStream_t s, const char* what) {
-    cudaError_t e = zg::launch(kind, h->dtype, vec8, a, s, nullptr);
+    cudaError_t e = zg::launch(kind, h->dtype, pick_vec(vec8, a), a, s, nullptr);
     if (e != cudaSuccess) return cuda_fail(h, e, what);
     return ZERO_OK;
 }

@@ -90,8 +90,13 @@ enum class Kind : int {
     kRsWs,            // stage 3 bucket reduce-scatter into the workspace
 };
 
+// Per-thread vector width of a launch: 8 elements with 256-bit fp32 accesses
+// (state and g_hat 32-byte aligned), 8 elements with 128-bit fp32 accesses,
+// or one element.
+enum class Vec : int { k8s32, k8s16, k1 };
+
 // Launchers (zero_kernels.cu).  Return the cudaError_t of the launch.
-cudaError_t launch(Kind kind, int dtype, bool vec8, const Args& a, cudaStream_t s, int* grid_out);
+cudaError_t launch(Kind kind, int dtype, Vec vec, const Args& a, cudaStream_t s, int* grid_out);
 cudaError_t launch_finalize3(bool spec, const Args& a, cudaStream_t s);
 cudaError_t launch_set_scaler(DevStatus* st, float loss_scale, int64_t t, int32_t slot, cudaStream_t s);
 

@@ -9,8 +9,8 @@
 //                      order (a ticket counter, no spinning);
 //   all-gather / broadcast -> the thread writes the RNE-cast 16-bit result
 //                      to all N replicas.
-// Every kernel is an HBM-bound stream: 128-bit loads and stores of
-// contiguous 8-element groups, grid-stride over a persistent grid sized
+// Every kernel is an HBM-bound stream: 128-bit (16-bit data) and 256-bit
+// (fp32 data) loads and stores of contiguous 8-element groups, grid-stride over a persistent grid sized
 // from the SM count and the kernel's occupancy.  There is no contraction,
 // so no tensor-core path.
 //
@@ -54,12 +54,16 @@ __device__ __forceinline__ uint32_t narrow<kBf16>(float x) {
     return __bfloat16_as_ushort(__float2bfloat16_rn(x));
 }
 
-// W consecutive 16-bit values at element index i of buffer p.
-template <int W>
-struct Io;
-
-template <>
-struct Io<8> {
+// Vector I/O policies.  An IO type moves IO::W consecutive elements per
+// thread: 16-bit values (gradients, replicas) and fp32 values (master, m,
+// v, g_hat).
+//   Io8s32: 8 elements; 16-bit as one 128-bit access, fp32 as one 256-bit
+//           access (ld/st.global.v8.f32, sm_100 and later; 32-byte aligned);
+//   Io8s16: 8 elements; fp32 as two 128-bit accesses (16-byte aligned);
+//   Io1:    one element (any size, any offset).
+// All accesses carry the streaming hint (.cs): nothing is re-read within a step.
+struct Io8s16 {
+    static constexpr int W = 8;
     __device__ static __forceinline__ void ld16(const void* p, uint64_t i, uint32_t (&out)[8]) {
         const uint4 x = __ldcs(reinterpret_cast<const uint4*>(p) + (i >> 3));
         out[0] = x.x & 0xFFFFu; out[1] = x.x >> 16;
@@ -85,8 +89,23 @@ struct Io<8> {
     }
 };
 
-template <>
-struct Io<1> {
+struct Io8s32 : Io8s16 {
+    // one 256-bit access per thread: a warp covers 1 KiB contiguous in one instruction
+    __device__ static __forceinline__ void ldf(const float* p, uint64_t i, float (&o)[8]) {
+        asm("ld.global.cs.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+            : "=f"(o[0]), "=f"(o[1]), "=f"(o[2]), "=f"(o[3]), "=f"(o[4]), "=f"(o[5]), "=f"(o[6]), "=f"(o[7])
+            : "l"(p + i));
+    }
+    __device__ static __forceinline__ void stf(float* p, uint64_t i, const float (&x)[8]) {
+        asm volatile("st.global.cs.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+                     :: "l"(p + i), "f"(x[0]), "f"(x[1]), "f"(x[2]), "f"(x[3]), "f"(x[4]), "f"(x[5]),
+                        "f"(x[6]), "f"(x[7])
+                     : "memory");
+    }
+};
+
+struct Io1 {
+    static constexpr int W = 1;
     __device__ static __forceinline__ void ld16(const void* p, uint64_t i, uint32_t (&out)[1]) {
         out[0] = __ldcs(reinterpret_cast<const unsigned short*>(p) + i);
     }
@@ -164,8 +183,9 @@ __device__ __forceinline__ void prologue_reduce(const Args& a, Pro& pro, bool wi
 }
 
 // Sum of the N ranks' values of W elements at local index j, then unscale.
-template <int DT, int W>
-__device__ __forceinline__ void reduce_group(const Args& a, uint64_t j, const Pro& pro, float (&g)[W]) {
+template <int DT, class IO>
+__device__ __forceinline__ void reduce_group(const Args& a, uint64_t j, const Pro& pro, float (&g)[IO::W]) {
+    constexpr int W = IO::W;
     float s[W];
 #pragma unroll
     for (int k = 0; k < W; ++k) s[k] = 0.0f;
@@ -174,7 +194,7 @@ __device__ __forceinline__ void reduce_group(const Args& a, uint64_t j, const Pr
     for (; r + 8 <= n; r += 8) {
         uint32_t raw[8][W];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) Io<W>::ld16(a.grads[r + q], j, raw[q]);
+        for (int q = 0; q < 8; ++q) IO::ld16(a.grads[r + q], j, raw[q]);
 #pragma unroll
         for (int q = 0; q < 8; ++q)
 #pragma unroll
@@ -182,7 +202,7 @@ __device__ __forceinline__ void reduce_group(const Args& a, uint64_t j, const Pr
     }
     for (; r < n; ++r) {
         uint32_t raw[W];
-        Io<W>::ld16(a.grads[r], j, raw);
+        IO::ld16(a.grads[r], j, raw);
 #pragma unroll
         for (int k = 0; k < W; ++k) s[k] = __fadd_rn(s[k], widen<DT>(raw[k]));
     }
@@ -319,8 +339,9 @@ __device__ __forceinline__ uint64_t thread_id() {
 // AdamW from the live slot into the shadow slot + cast + all-gather.  The
 // last block commits the shadow slot, or records the overflow (the
 // rollback kernel then restores the replicas).
-template <int DT, int W>
+template <int DT, class IO>
 __global__ void __launch_bounds__(kThreads) k_step_spec(const __grid_constant__ Args a) {
+    constexpr int W = IO::W;
     __shared__ Pro pro;
     prologue_reduce(a, pro, true);
     const uint64_t src = static_cast<uint64_t>(pro.live) * a.slot_stride;
@@ -331,10 +352,10 @@ __global__ void __launch_bounds__(kThreads) k_step_spec(const __grid_constant__ 
     for (uint64_t vi = thread_id(); vi < nvec; vi += grid_threads()) {
         const uint64_t gi = vi * W;
         float g[W], p[W], m[W], v[W];
-        reduce_group<DT, W>(a, gi, pro, g);
-        Io<W>::ldf(a.master + src, gi, p);
-        Io<W>::ldf(a.m + src, gi, m);
-        Io<W>::ldf(a.v + src, gi, v);
+        reduce_group<DT, IO>(a, gi, pro, g);
+        IO::ldf(a.master + src, gi, p);
+        IO::ldf(a.m + src, gi, m);
+        IO::ldf(a.v + src, gi, v);
         const int valid = valid_count(gi, W, a.psi);
         norm_group<W>(g, valid, acc, bad);
         uint32_t q[W];
@@ -347,10 +368,10 @@ __global__ void __launch_bounds__(kThreads) k_step_spec(const __grid_constant__ 
             }
             q[k] = narrow<DT>(p[k]);
         }
-        Io<W>::stf(a.master + dst, gi, p);
-        Io<W>::stf(a.m + dst, gi, m);
-        Io<W>::stf(a.v + dst, gi, v);
-        for (int r = 0; r < a.n_ranks; ++r) Io<W>::st16(a.params[r], gi, q);
+        IO::stf(a.master + dst, gi, p);
+        IO::stf(a.m + dst, gi, m);
+        IO::stf(a.v + dst, gi, v);
+        for (int r = 0; r < a.n_ranks; ++r) IO::st16(a.params[r], gi, q);
     }
     const double blk = block_sum(acc);
     const int flag = __syncthreads_or(bad);
@@ -370,8 +391,9 @@ __global__ void __launch_bounds__(kThreads) k_step_spec(const __grid_constant__ 
 // Two-pass, pass 1: reduce + unscale + flag + norm partial (+ fp32 g_hat to
 // the workspace).  The last block decides: skip, or clip factor and step
 // scalars for pass 2.
-template <int DT, int W, bool WS>
+template <int DT, class IO, bool WS>
 __global__ void __launch_bounds__(kThreads) k_reduce(const __grid_constant__ Args a) {
+    constexpr int W = IO::W;
     __shared__ Pro pro;
     prologue_reduce(a, pro, false);
     const uint64_t nvec = a.count / W;
@@ -380,14 +402,14 @@ __global__ void __launch_bounds__(kThreads) k_reduce(const __grid_constant__ Arg
     for (uint64_t vi = thread_id(); vi < nvec; vi += grid_threads()) {
         const uint64_t gi = vi * W;
         float g[W];
-        reduce_group<DT, W>(a, gi, pro, g);
+        reduce_group<DT, IO>(a, gi, pro, g);
         const int valid = valid_count(gi, W, a.psi);
         norm_group<W>(g, valid, acc, bad);
         if (WS) {
 #pragma unroll
             for (int k = 0; k < W; ++k)
                 if (k >= valid) g[k] = 0.0f;
-            Io<W>::stf(a.ws.ghat, gi, g);
+            IO::stf(a.ws.ghat, gi, g);
         }
     }
     const double blk = block_sum(acc);
@@ -409,8 +431,9 @@ __global__ void __launch_bounds__(kThreads) k_reduce(const __grid_constant__ Arg
 // the live slot with g_hat from the workspace (SRC_WS) or re-reduced from
 // the N gradients, clipped if decided, then the 16-bit result to the N
 // replicas (stages 1/2) or to the shard (stage 3, TO_SHARD).
-template <int DT, int W, bool SRC_WS, bool TO_SHARD>
+template <int DT, class IO, bool SRC_WS, bool TO_SHARD>
 __global__ void __launch_bounds__(kThreads) k_apply(const __grid_constant__ Args a) {
+    constexpr int W = IO::W;
     __shared__ Pro pro;
     prologue_reduce(a, pro, false);
     if (pro.overflow) return;
@@ -419,11 +442,11 @@ __global__ void __launch_bounds__(kThreads) k_apply(const __grid_constant__ Args
     for (uint64_t vi = thread_id(); vi < nvec; vi += grid_threads()) {
         const uint64_t gi = vi * W;
         float g[W], p[W], m[W], v[W];
-        if (SRC_WS) Io<W>::ldf(a.ws.ghat, gi, g);
-        else reduce_group<DT, W>(a, gi, pro, g);
-        Io<W>::ldf(a.master + off, gi, p);
-        Io<W>::ldf(a.m + off, gi, m);
-        Io<W>::ldf(a.v + off, gi, v);
+        if (SRC_WS) IO::ldf(a.ws.ghat, gi, g);
+        else reduce_group<DT, IO>(a, gi, pro, g);
+        IO::ldf(a.master + off, gi, p);
+        IO::ldf(a.m + off, gi, m);
+        IO::ldf(a.v + off, gi, v);
         const int valid = valid_count(gi, W, a.psi);
         uint32_t q[W];
 #pragma unroll
@@ -436,21 +459,22 @@ __global__ void __launch_bounds__(kThreads) k_apply(const __grid_constant__ Args
             }
             q[k] = narrow<DT>(p[k]);
         }
-        Io<W>::stf(a.master + off, gi, p);
-        Io<W>::stf(a.m + off, gi, m);
-        Io<W>::stf(a.v + off, gi, v);
+        IO::stf(a.master + off, gi, p);
+        IO::stf(a.m + off, gi, m);
+        IO::stf(a.v + off, gi, v);
         if (TO_SHARD) {
-            Io<W>::st16(a.params[0], gi, q);
+            IO::st16(a.params[0], gi, q);
         } else {
-            for (int r = 0; r < a.n_ranks; ++r) Io<W>::st16(a.params[r], gi, q);
+            for (int r = 0; r < a.n_ranks; ++r) IO::st16(a.params[r], gi, q);
         }
     }
 }
 
 // Stage 0, pass 2: every rank holds the full averaged gradient and its own
 // full replica of master/m/v (rank r at r*psi_pad) and updates all of it.
-template <int DT, int W>
+template <int DT, class IO>
 __global__ void __launch_bounds__(kThreads) k_apply_stage0(const __grid_constant__ Args a) {
+    constexpr int W = IO::W;
     __shared__ Pro pro;
     prologue_reduce(a, pro, false);
     if (pro.overflow) return;
@@ -458,7 +482,7 @@ __global__ void __launch_bounds__(kThreads) k_apply_stage0(const __grid_constant
     for (uint64_t vi = thread_id(); vi < nvec; vi += grid_threads()) {
         const uint64_t gi = vi * W;
         float g[W];
-        Io<W>::ldf(a.ws.ghat, gi, g);
+        IO::ldf(a.ws.ghat, gi, g);
         const int valid = valid_count(gi, W, a.psi);
 #pragma unroll
         for (int k = 0; k < W; ++k)
@@ -466,9 +490,9 @@ __global__ void __launch_bounds__(kThreads) k_apply_stage0(const __grid_constant
         for (int r = 0; r < a.n_ranks; ++r) {
             const uint64_t ri = static_cast<uint64_t>(r) * a.psi_pad + gi;
             float p[W], m[W], v[W];
-            Io<W>::ldf(a.master, ri, p);
-            Io<W>::ldf(a.m, ri, m);
-            Io<W>::ldf(a.v, ri, v);
+            IO::ldf(a.master, ri, p);
+            IO::ldf(a.m, ri, m);
+            IO::ldf(a.v, ri, v);
             uint32_t q[W];
 #pragma unroll
             for (int k = 0; k < W; ++k) {
@@ -479,18 +503,19 @@ __global__ void __launch_bounds__(kThreads) k_apply_stage0(const __grid_constant
                 }
                 q[k] = narrow<DT>(p[k]);
             }
-            Io<W>::stf(a.master, ri, p);
-            Io<W>::stf(a.m, ri, m);
-            Io<W>::stf(a.v, ri, v);
-            Io<W>::st16(a.params[r], gi, q);
+            IO::stf(a.master, ri, p);
+            IO::stf(a.m, ri, m);
+            IO::stf(a.v, ri, v);
+            IO::st16(a.params[r], gi, q);
         }
     }
 }
 
 // After a speculative pass: when the step overflowed, rewrite the 16-bit
 // copies from the live (old) master; otherwise exit at once.
-template <int DT, int W, bool TO_SHARD>
+template <int DT, class IO, bool TO_SHARD>
 __global__ void __launch_bounds__(kThreads) k_rollback(const __grid_constant__ Args a) {
+    constexpr int W = IO::W;
     const DevStatus* st = a.ws.status;
     if (!st->overflow) return;
     const uint64_t off = static_cast<uint64_t>(st->live_slot) * a.slot_stride;
@@ -498,27 +523,28 @@ __global__ void __launch_bounds__(kThreads) k_rollback(const __grid_constant__ A
     for (uint64_t vi = thread_id(); vi < nvec; vi += grid_threads()) {
         const uint64_t gi = a.base + vi * W;
         float p[W];
-        Io<W>::ldf(a.master + off, gi, p);
+        IO::ldf(a.master + off, gi, p);
         uint32_t q[W];
 #pragma unroll
         for (int k = 0; k < W; ++k) q[k] = narrow<DT>(p[k]);
         if (TO_SHARD) {
-            Io<W>::st16(a.params[0], gi, q);
+            IO::st16(a.params[0], gi, q);
         } else {
-            for (int r = 0; r < a.n_ranks; ++r) Io<W>::st16(a.params[r], gi, q);
+            for (int r = 0; r < a.n_ranks; ++r) IO::st16(a.params[r], gi, q);
         }
     }
 }
 
 // ZeRO-3 gather of [base, base+count): out[r][j] = shard[base + j].
-template <int W>
+template <class IO>
 __global__ void __launch_bounds__(kThreads) k_gather(const __grid_constant__ Args a) {
+    constexpr int W = IO::W;
     const uint64_t nvec = a.count / W;
     for (uint64_t vi = thread_id(); vi < nvec; vi += grid_threads()) {
         const uint64_t j = vi * W;
         uint32_t x[W];
-        Io<W>::ld16(a.grads[0], a.base + j, x);
-        for (int r = 0; r < a.n_ranks; ++r) Io<W>::st16(a.params[r], j, x);
+        IO::ld16(a.grads[0], a.base + j, x);
+        for (int r = 0; r < a.n_ranks; ++r) IO::st16(a.params[r], j, x);
     }
 }
 
@@ -526,8 +552,9 @@ __global__ void __launch_bounds__(kThreads) k_gather(const __grid_constant__ Arg
 // AdamW update runs here into the shadow slot and the 16-bit shard; else
 // g_hat goes to the workspace.  The last block stores the bucket's norm
 // partial and flag for the step's finaliser.
-template <int DT, int W, bool SPEC>
+template <int DT, class IO, bool SPEC>
 __global__ void __launch_bounds__(kThreads) k_rs(const __grid_constant__ Args a) {
+    constexpr int W = IO::W;
     __shared__ Pro pro;
     prologue_reduce(a, pro, SPEC);
     const uint64_t src = static_cast<uint64_t>(pro.live) * a.slot_stride;
@@ -539,13 +566,13 @@ __global__ void __launch_bounds__(kThreads) k_rs(const __grid_constant__ Args a)
         const uint64_t j = vi * W;
         const uint64_t gi = a.base + j;
         float g[W];
-        reduce_group<DT, W>(a, j, pro, g);
+        reduce_group<DT, IO>(a, j, pro, g);
         const int valid = valid_count(gi, W, a.psi);
         if (SPEC) {
             float p[W], m[W], v[W];
-            Io<W>::ldf(a.master + src, gi, p);
-            Io<W>::ldf(a.m + src, gi, m);
-            Io<W>::ldf(a.v + src, gi, v);
+            IO::ldf(a.master + src, gi, p);
+            IO::ldf(a.m + src, gi, m);
+            IO::ldf(a.v + src, gi, v);
             norm_group<W>(g, valid, acc, bad);
             uint32_t q[W];
 #pragma unroll
@@ -557,16 +584,16 @@ __global__ void __launch_bounds__(kThreads) k_rs(const __grid_constant__ Args a)
                 }
                 q[k] = narrow<DT>(p[k]);
             }
-            Io<W>::stf(a.master + dst, gi, p);
-            Io<W>::stf(a.m + dst, gi, m);
-            Io<W>::stf(a.v + dst, gi, v);
-            Io<W>::st16(a.params[0], gi, q);
+            IO::stf(a.master + dst, gi, p);
+            IO::stf(a.m + dst, gi, m);
+            IO::stf(a.v + dst, gi, v);
+            IO::st16(a.params[0], gi, q);
         } else {
             norm_group<W>(g, valid, acc, bad);
 #pragma unroll
             for (int k = 0; k < W; ++k)
                 if (k >= valid) g[k] = 0.0f;
-            Io<W>::stf(a.ws.ghat, gi, g);
+            IO::stf(a.ws.ghat, gi, g);
         }
     }
     const double blk = block_sum(acc);
@@ -638,33 +665,39 @@ cudaError_t run(KernelT kernel, const Args& a, uint64_t nvec, cudaStream_t s, in
     return cudaGetLastError();
 }
 
-template <int DT, int W>
+template <int DT, class IO>
 cudaError_t launch_dw(Kind kind, const Args& a, cudaStream_t s, int* grid_out) {
-    const uint64_t nvec = a.count / W;
+    const uint64_t nvec = a.count / IO::W;
     switch (kind) {
-        case Kind::kStepSpec: return run(k_step_spec<DT, W>, a, nvec, s, grid_out);
-        case Kind::kReduceWs: return run(k_reduce<DT, W, true>, a, nvec, s, grid_out);
-        case Kind::kReduceNoWs: return run(k_reduce<DT, W, false>, a, nvec, s, grid_out);
-        case Kind::kApplyWs: return run(k_apply<DT, W, true, false>, a, nvec, s, grid_out);
-        case Kind::kApplyReread: return run(k_apply<DT, W, false, false>, a, nvec, s, grid_out);
-        case Kind::kApplyWsShard: return run(k_apply<DT, W, true, true>, a, nvec, s, grid_out);
-        case Kind::kApplyStage0: return run(k_apply_stage0<DT, W>, a, nvec, s, grid_out);
-        case Kind::kRollbackReplicas: return run(k_rollback<DT, W, false>, a, nvec, s, grid_out);
-        case Kind::kRollbackShard: return run(k_rollback<DT, W, true>, a, nvec, s, grid_out);
-        case Kind::kGather: return run(k_gather<W>, a, nvec, s, grid_out);
-        case Kind::kRsSpec: return run(k_rs<DT, W, true>, a, nvec, s, grid_out);
-        case Kind::kRsWs: return run(k_rs<DT, W, false>, a, nvec, s, grid_out);
+        case Kind::kStepSpec: return run(k_step_spec<DT, IO>, a, nvec, s, grid_out);
+        case Kind::kReduceWs: return run(k_reduce<DT, IO, true>, a, nvec, s, grid_out);
+        case Kind::kReduceNoWs: return run(k_reduce<DT, IO, false>, a, nvec, s, grid_out);
+        case Kind::kApplyWs: return run(k_apply<DT, IO, true, false>, a, nvec, s, grid_out);
+        case Kind::kApplyReread: return run(k_apply<DT, IO, false, false>, a, nvec, s, grid_out);
+        case Kind::kApplyWsShard: return run(k_apply<DT, IO, true, true>, a, nvec, s, grid_out);
+        case Kind::kApplyStage0: return run(k_apply_stage0<DT, IO>, a, nvec, s, grid_out);
+        case Kind::kRollbackReplicas: return run(k_rollback<DT, IO, false>, a, nvec, s, grid_out);
+        case Kind::kRollbackShard: return run(k_rollback<DT, IO, true>, a, nvec, s, grid_out);
+        case Kind::kGather: return run(k_gather<IO>, a, nvec, s, grid_out);
+        case Kind::kRsSpec: return run(k_rs<DT, IO, true>, a, nvec, s, grid_out);
+        case Kind::kRsWs: return run(k_rs<DT, IO, false>, a, nvec, s, grid_out);
     }
     return cudaErrorInvalidValue;
 }
 
+template <int DT>
+cudaError_t launch_d(Kind kind, Vec vec, const Args& a, cudaStream_t s, int* grid_out) {
+    switch (vec) {
+        case Vec::k8s32: return launch_dw<DT, Io8s32>(kind, a, s, grid_out);
+        case Vec::k8s16: return launch_dw<DT, Io8s16>(kind, a, s, grid_out);
+        default: return launch_dw<DT, Io1>(kind, a, s, grid_out);
+    }
+}
+
 }  // namespace
 
-cudaError_t launch(Kind kind, int dtype, bool vec8, const Args& a, cudaStream_t s, int* grid_out) {
-    if (dtype == kFp16) {
-        return vec8 ? launch_dw<kFp16, 8>(kind, a, s, grid_out) : launch_dw<kFp16, 1>(kind, a, s, grid_out);
-    }
-    return vec8 ? launch_dw<kBf16, 8>(kind, a, s, grid_out) : launch_dw<kBf16, 1>(kind, a, s, grid_out);
+cudaError_t launch(Kind kind, int dtype, Vec vec, const Args& a, cudaStream_t s, int* grid_out) {
+    return dtype == kFp16 ? launch_d<kFp16>(kind, vec, a, s, grid_out) : launch_d<kBf16>(kind, vec, a, s, grid_out);
 }
 
 cudaError_t launch_finalize3(bool spec, const Args& a, cudaStream_t s) {

@@ -35,8 +35,8 @@ constexpr size_t kFlagBytes = static_cast<size_t>(zg::kMaxBlocks) * sizeof(int32
 constexpr size_t kGhatBytes = static_cast<size_t>(kNoAllocMaxPsiPad) * sizeof(float);
 constexpr size_t kScratchBytes = kStatusBytes + kPartialBytes + kFlagBytes + kGhatBytes;
 static_assert(sizeof(zg::DevStatus) <= kStatusBytes, "status must fit its slot");
-static_assert(kStatusBytes % 16 == 0 && kPartialBytes % 16 == 0 && kFlagBytes % 16 == 0,
-              "scratch regions stay 16-byte aligned");
+static_assert(kStatusBytes % 32 == 0 && kPartialBytes % 32 == 0 && kFlagBytes % 32 == 0,
+              "scratch regions stay 32-byte aligned");
 
 // The scratch.  Host code must not pass &g_noalloc_scratch to a kernel: on
 // the host that name is a stand-in, not a device address.  Its device
@@ -160,12 +160,16 @@ extern "C" int zero_step_noalloc(uint64_t psi, int n_ranks, int stage, int dtype
     a.ws.ghat = reinterpret_cast<float*>(base + kStatusBytes + kPartialBytes + kFlagBytes);
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const bool vec8 = (P % 8) == 0;
+    // 8-wide with 256-bit fp32 accesses when the caller's state is 32-byte
+    // aligned (the scratch's g_hat region is); 128-bit otherwise
+    const bool s32 = ((reinterpret_cast<uintptr_t>(master) | reinterpret_cast<uintptr_t>(m) |
+                       reinterpret_cast<uintptr_t>(v)) & 31u) == 0;
+    const zg::Vec vec = (P % 8) != 0 ? zg::Vec::k1 : (s32 ? zg::Vec::k8s32 : zg::Vec::k8s16);
     // the status word (and its last-block ticket) must start from zero
     e = cudaMemsetAsync(a.ws.status, 0, kStatusBytes, s);
     if (e == cudaSuccess) e = zg::launch_set_scaler(a.ws.status, loss_scale, steps_applied, 0, s);
-    if (e == cudaSuccess) e = zg::launch(zg::Kind::kReduceWs, dtype, vec8, a, s, nullptr);
-    if (e == cudaSuccess) e = zg::launch(zg::Kind::kApplyWs, dtype, vec8, a, s, nullptr);
+    if (e == cudaSuccess) e = zg::launch(zg::Kind::kReduceWs, dtype, vec, a, s, nullptr);
+    if (e == cudaSuccess) e = zg::launch(zg::Kind::kApplyWs, dtype, vec, a, s, nullptr);
     if (e == cudaSuccess) {
         k_export_result<<<1, 1, 0, s>>>(a.ws.status, result);
         e = cudaGetLastError();
