@@ -313,8 +313,17 @@ def run_ours(args, ws, rank, local):
 
 
 def e2e_flat(args, w, buf, sets, hyp, stream, torch, ws, dist):
-    """Same step through the public API with the gradients coming from pinned host memory."""
-    N, P = w.n_ranks, buf.psi_pad
+    """Same step through the public API with the gradients coming from pinned host memory.
+
+    Three ways to bring a step's 24 GB of gradients in, each timed with the
+    step and the device->host read of its result:
+      copy     one cudaMemcpyAsync of all N rank rows, then zero_step;
+      streams  one copy per rank row spread over four side streams, then zero_step;
+      direct   zero_step reads the pinned host rows itself (unified addresses,
+               over NVLink-C2C), so the transfer overlaps the HBM stream.
+    The line's value is the fastest; every mode is reported.
+    """
+    N = w.n_ranks
     try:
         host = torch.empty((N, buf.stride), dtype=sets.dtype, pin_memory=True)
     except Exception as e:  # not enough pinnable host memory
@@ -322,22 +331,52 @@ def e2e_flat(args, w, buf, sets, hyp, stream, torch, ws, dist):
     host.copy_(sets[0])
     dev = sets[0]
     K = max(3, min(args.steps, 10))
-    torch.cuda.synchronize()
-    if ws > 1:
-        dist.barrier()
-    t0 = time.perf_counter()
-    for _ in range(K):
+    side = [torch.cuda.Stream() for _ in range(4)]
+
+    def step_copy():
         dev.copy_(host, non_blocking=True)
         buf.step(hyp, [dev[r] for r in range(N)])
-        buf.status(stream)          # device->host read of the step's result, synchronises
-    t = time.perf_counter() - t0
-    if ws > 1:
-        tt = torch.tensor([t], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t = float(tt.item())
+
+    def step_streams():
+        ev = torch.cuda.Event()
+        ev.record(stream)
+        done = []
+        for r in range(N):
+            s = side[r % len(side)]
+            s.wait_event(ev)
+            with torch.cuda.stream(s):
+                dev[r].copy_(host[r], non_blocking=True)
+                e = torch.cuda.Event()
+                e.record(s)
+                done.append(e)
+        for e in done:
+            stream.wait_event(e)
+        buf.step(hyp, [dev[r] for r in range(N)])
+
+    def step_direct():
+        buf.step(hyp, [host[r] for r in range(N)])
+
+    out = {}
+    for name, fn in (("copy", step_copy), ("streams", step_streams), ("direct", step_direct)):
+        fn()
+        buf.status(stream)
+        torch.cuda.synchronize()
+        if ws > 1:
+            dist.barrier()
+        t0 = time.perf_counter()
+        for _ in range(K):
+            fn()
+            buf.status(stream)          # device->host read of the step's result, synchronises
+        t = time.perf_counter() - t0
+        if ws > 1:
+            tt = torch.tensor([t], device="cuda")
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            t = float(tt.item())
+        out[name] = w.psi * K * ws / t
     del host
-    return {"value": w.psi * K * ws / t, "unit": "params/s", "h2d_bytes_per_step": N * buf.stride * 2,
-            "d2h_bytes_per_step": RESULT_BYTES, "steps": K}
+    best = max(out, key=out.get)
+    return {"value": out[best], "unit": "params/s", "mode": best, "modes": out,
+            "h2d_bytes_per_step": N * buf.stride * 2, "d2h_bytes_per_step": RESULT_BYTES, "steps": K}
 
 
 # ---------------------------------------------------------------- other workloads

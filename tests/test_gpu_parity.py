@@ -247,3 +247,43 @@ def test_state_only_16_byte_aligned_takes_the_128_bit_path(stage):
     assert torch.equal(a.v.view(torch.int32), b.v.view(torch.int32))
     assert torch.equal(a.params.view(torch.int16), b.params.view(torch.int16))
     a.close(); b.close()
+
+
+@pytest.mark.parametrize("stage", [1, 3])
+def test_gradients_in_pinned_host_memory(stage):
+    # the kernels may read the ranks' gradients straight from pinned host memory
+    # (unified addresses); results must equal those from device-resident gradients
+    from zero_partitioned_mixed_gb300 import _binding as B
+    from zero_partitioned_mixed_gb300.buffers import RankBuffers
+    psi, n = 300_000, 8
+    a = RankBuffers(psi, n, stage, "fp16")
+    b = RankBuffers(psi, n, stage, "fp16")
+    P = a.psi_pad
+    torch.manual_seed(4)
+    a.master[:psi].normal_(0, 0.02)
+    b.master.copy_(a.master)
+    q = a.master[:P].to(torch.float16)
+    for buf in (a, b):
+        if stage == 3:
+            buf.params[:P].copy_(q)
+        else:
+            buf.params[:, :P].copy_(q.unsqueeze(0).expand(n, P))
+    g_dev = (torch.randn((n, a.stride), device="cuda") * 1e-2 * 1024).to(torch.float16)
+    g_dev[:, psi:] = 0
+    g_host = torch.empty((n, a.stride), dtype=torch.float16, pin_memory=True)
+    g_host.copy_(g_dev)
+    h = B.hyper(weight_decay=0.01)
+    for buf, g in ((a, g_dev), (b, g_host)):
+        buf.set_scaler(1024.0, 0, 0)
+        for _ in range(2):
+            if stage == 3:
+                buf.reduce_scatter(0, P, [g[r] for r in range(n)], h)
+                buf.step(h)
+            else:
+                buf.step(h, [g[r] for r in range(n)])
+    torch.cuda.synchronize()
+    assert a.status()["grad_norm"] == b.status()["grad_norm"]
+    for x, y in ((a.master, b.master), (a.m, b.m), (a.v, b.v)):
+        assert torch.equal(x.view(torch.int32), y.view(torch.int32))
+    assert torch.equal(a.params.view(torch.int16), b.params.view(torch.int16))
+    a.close(); b.close()
