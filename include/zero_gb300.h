@@ -154,7 +154,8 @@ ZERO_API int zero_set_scaler(zero_handle_t h, float loss_scale, int64_t steps_ap
  *   N full replicas of the state (ZeRO summary Sec. 7, baseline DP).
  *   Stage 3: grads must be NULL; the N gradients were already consumed by
  *   zero_reduce_scatter_bucket calls covering [0, psi_pad) exactly once
- *   since the last step.  This call finishes the norm/overflow/clip and
+ *   since the last step.  Stage 2 with grads NULL: the same, after
+ *   zero_reduce_scatter_bucket_replicas calls.  This call finishes the norm/overflow/clip and
  *   (two-pass modes) applies Adam and writes the 16-bit shard.
  * On overflow nothing of master/m/v/params changes, the scale halves and t
  * is not advanced.
@@ -209,6 +210,30 @@ ZERO_API int zero_gather_bucket(zero_handle_t h, uint64_t a, uint64_t b, const v
 ZERO_API int zero_reduce_scatter_bucket(zero_handle_t h, uint64_t a, uint64_t b,
                                const void* const* grads, float* master, float* m, float* v,
                                void* shard16, const zero_hyper_t* hyper, void* stream);
+
+/*
+ * zero_reduce_scatter_bucket_replicas -- ZeRO-2 with the gradients reduced
+ * during backward: the reduce-scatter of bucket [a, b) as its gradients
+ * appear, after which the ranks may release or reuse their gradient
+ * buffers for the next bucket (a constant-size buffer per rank).
+ *   (ZeRO summary Sec. 5, P_os+g: reduce-scatter during backward, bucketized
+ *    per partition, gradient memory freed; Sec. 6 CB: constant-size fused
+ *    buffers; CMU notes, ZeRO-2: reduce each segment to its owner, delete.)
+ * With ZERO_F_DOUBLE_BUFFER and no clipping the bucket's AdamW update and
+ * its all-gather into every replica are fused here (shadow slot; replicas
+ * written at once); zero_step(h, NULL grads, params, ...) then commits, or
+ * on overflow restores the replicas from the old master.  Otherwise g_hat
+ * goes to the fp32 workspace and that zero_step applies AdamW and writes
+ * the replicas.  The buckets of one step must tile [0, psi_pad) without
+ * overlap (at most 4096) and pass the same hyper.
+ *   grads: host array of N device pointers, b - a 16-bit elements each
+ *   params: host array of N device pointers to the psi_pad replicas
+ *   master, m, v: as for zero_step (may be NULL in two-pass modes)
+ * Stage 2 only.  Errors: EINVAL, ESTATE, ECUDA, ENOMEM.
+ */
+ZERO_API int zero_reduce_scatter_bucket_replicas(zero_handle_t h, uint64_t a, uint64_t b,
+                                        const void* const* grads, float* master, float* m, float* v,
+                                        void* const* params, const zero_hyper_t* hyper, void* stream);
 
 /*
  * zero_get_status -- a11: copy the device status of the last step to the

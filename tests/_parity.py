@@ -158,6 +158,16 @@ def run_case(psi: int, n: int, stage: int, dtype: str = "bf16", steps: int = 2, 
                 for r in range(n):
                     assert np.array_equal(res_gather_fwd[bi][r], ores.gathered_fwd[bi][r])
                     assert np.array_equal(res_gather_bwd[bi][r], ores.gathered_bwd[bi][r])
+        elif stage == 2 and buckets is not None:
+            # ZeRO-2 reduced during backward: buckets in reverse order, each
+            # copied into one constant-size buffer per rank that is reused
+            lmax = max(b - a for a, b in buckets)
+            cb = torch.zeros((n, max(8, (lmax + 7) // 8 * 8)), dtype=td, device="cuda")
+            for (a, b) in reversed(buckets):
+                cb[:, :b - a].copy_(grads[:, a:b])
+                buf.reduce_scatter(a, b, [cb[r] for r in range(n)], hb)
+            buf.finish_bucketed_step(hb)
+            ost, ores = O.step(ost, gbits, ho)
         else:
             buf.step(hb, buf_grads_rows(grads, n))
             ost, ores = O.step(ost, gbits, ho)

@@ -287,3 +287,40 @@ def test_gradients_in_pinned_host_memory(stage):
         assert torch.equal(x.view(torch.int32), y.view(torch.int32))
     assert torch.equal(a.params.view(torch.int16), b.params.view(torch.int16))
     a.close(); b.close()
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("double_buffer", [True, False])
+def test_stage2_reduced_during_backward_constant_buffer(dtype, double_buffer):
+    # ZeRO-2 with the reduce-scatter interleaved with backward, one constant-size
+    # gradient buffer per rank reused for every bucket; same result as one step
+    psi, n = 200_003, 4
+    pp = (psi + 31) // 32 * 32
+    buckets = [(0, 65_536), (65_536, 65_544), (65_544, 131_072), (131_072, 131_073), (131_073, pp)]
+    inject = [(1, 2, 70_000, INF)]
+    st = run_case(psi, n, 2, dtype, steps=3, buckets=buckets, double_buffer=double_buffer,
+                  loss_scale=256.0, inject=inject, hyper_kw=dict(weight_decay=0.1))
+    st.check()
+    assert st.mismatches == 0, st
+
+
+def test_stage2_bucketed_with_clipping_and_errors():
+    from zero_partitioned_mixed_gb300 import _binding as B
+    from zero_partitioned_mixed_gb300.buffers import RankBuffers
+    st = run_case(100_000, 4, 2, "bf16", steps=2, buckets=[(0, 50_000), (50_000, 100_000)],
+                  double_buffer=False, hyper_kw=dict(max_norm=0.05))
+    st.check()
+    b2 = RankBuffers(1024, 2, 2, "bf16")
+    g = [torch.zeros(512, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    b2.reduce_scatter(0, 512, g, B.hyper())
+    with pytest.raises(B.ZeroError) as e:
+        b2.finish_bucketed_step(B.hyper())      # half the buffer not reduced yet
+    assert e.value.code == 5
+    with pytest.raises(B.ZeroError) as e:
+        b2.reduce_scatter(512, 1024, g, B.hyper(mode=B.ZERO_MODE_TWO_PASS_REREAD))
+    assert e.value.code == 1                    # hyper differs within the step
+    b2.close()
+    b1 = RankBuffers(1024, 2, 1, "bf16")
+    with pytest.raises(B.ZeroError):
+        B.zero_reduce_scatter_bucket_replicas(b1.h, 0, 512, g, b1.master, b1.m, b1.v, b1.param_rows(), B.hyper())
+    b1.close()

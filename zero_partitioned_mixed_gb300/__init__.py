@@ -14,6 +14,7 @@ from ._binding import (  # noqa: F401
     ZERO_MODE_TWO_PASS_WS, ZeroError, exported_symbols, hyper, library_path,
     load_library, zero_bytes_moved, zero_destroy, zero_gather_bucket,
     zero_get_status, zero_init_partition, zero_last_error, zero_partition_info,
-    zero_reduce_scatter_bucket, zero_set_scaler, zero_step, zero_step_noalloc,
+    zero_reduce_scatter_bucket, zero_reduce_scatter_bucket_replicas, zero_set_scaler, zero_step,
+    zero_step_noalloc,
     result_from_device,
 )

@@ -20,6 +20,7 @@ EXPORTS = (
     "zero_init_partition", "zero_partition_info", "zero_set_scaler", "zero_step",
     "zero_gather_bucket", "zero_reduce_scatter_bucket", "zero_get_status",
     "zero_bytes_moved", "zero_last_error", "zero_destroy", "zero_step_noalloc",
+    "zero_reduce_scatter_bucket_replicas",
 )
 
 
@@ -78,6 +79,8 @@ def load_library():
     lib.zero_step.argtypes = [P, C.POINTER(P), C.POINTER(P), P, P, P, C.POINTER(Hyper), P]
     lib.zero_gather_bucket.argtypes = [P, U64, U64, P, C.POINTER(P), P]
     lib.zero_reduce_scatter_bucket.argtypes = [P, U64, U64, C.POINTER(P), P, P, P, P, C.POINTER(Hyper), P]
+    lib.zero_reduce_scatter_bucket_replicas.argtypes = [P, U64, U64, C.POINTER(P), P, P, P, C.POINTER(P),
+                                                         C.POINTER(Hyper), P]
     lib.zero_get_status.argtypes = [P, P, C.POINTER(Result)]
     lib.zero_bytes_moved.argtypes = [P, C.POINTER(Bytes)]
     lib.zero_last_error.argtypes = [P]
@@ -182,6 +185,14 @@ def zero_gather_bucket(h, a: int, b: int, shard16, out, stream=None):
 def zero_reduce_scatter_bucket(h, a: int, b: int, grads, master, m, v, shard16, hyp: Hyper, stream=None):
     rc = load_library().zero_reduce_scatter_bucket(h, a, b, _ptr_array(grads), _ptr(master), _ptr(m),
                                                    _ptr(v), _ptr(shard16), C.byref(hyp), _stream(stream))
+    _check(rc, h)
+
+
+def zero_reduce_scatter_bucket_replicas(h, a: int, b: int, grads, master, m, v, params, hyp: Hyper,
+                                        stream=None):
+    rc = load_library().zero_reduce_scatter_bucket_replicas(h, a, b, _ptr_array(grads), _ptr(master), _ptr(m),
+                                                            _ptr(v), _ptr_array(params), C.byref(hyp),
+                                                            _stream(stream))
     _check(rc, h)
 
 

@@ -86,7 +86,17 @@ class RankBuffers:
         B.zero_gather_bucket(self.h, a, b, self.params, out, stream)
 
     def reduce_scatter(self, a: int, b: int, grads: List, hyp, stream=None):
-        B.zero_reduce_scatter_bucket(self.h, a, b, grads, self.master, self.m, self.v, self.params, hyp, stream)
+        """Reduce-scatter of one bucket: stage 3, or stage 2 reduced during backward."""
+        if self.stage == 2:
+            B.zero_reduce_scatter_bucket_replicas(self.h, a, b, grads, self.master, self.m, self.v,
+                                                  self.param_rows(), hyp, stream)
+        else:
+            B.zero_reduce_scatter_bucket(self.h, a, b, grads, self.master, self.m, self.v, self.params, hyp,
+                                         stream)
+
+    def finish_bucketed_step(self, hyp, stream=None):
+        """zero_step after the step's buckets were reduce-scattered (stages 2 and 3)."""
+        B.zero_step(self.h, None, self.param_rows(), self.master, self.m, self.v, hyp, stream)
 
     def status(self, stream=None) -> dict:
         return B.zero_get_status(self.h, stream)

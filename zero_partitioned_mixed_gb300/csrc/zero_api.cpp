@@ -162,6 +162,78 @@ bool same_hyper(const zero_hyper_t& x, const zero_hyper_t& y) {
     return std::memcmp(&x, &y, sizeof(zero_hyper_t)) == 0;
 }
 
+// Reduce-scatter of one bucket of a step whose gradients arrive bucket by
+// bucket (stage 3 always; stage 2 when the caller reduces during backward).
+// outs: the 16-bit shard (stage 3) or the N replicas (stage 2).
+int rs_bucket(zero_handle* h, uint64_t a0, uint64_t b0, const void* const* grads, float* master, float* m,
+              float* v, void* const* outs, const zero_hyper_t* hyper, void* stream) {
+    int rc = check_hyper(h, hyper);
+    if (rc) return rc;
+    if (a0 > b0 || b0 > h->psi_pad) return fail(h, ZERO_EINVAL, "bucket must satisfy 0 <= a <= b <= psi_pad");
+    const uint64_t L = b0 - a0, N = static_cast<uint64_t>(h->n);
+    for (auto& iv : h->covered)
+        if (a0 < iv.second && iv.first < b0)
+            return fail(h, ZERO_ESTATE, "bucket overlaps one already reduced this step");
+    if (h->rs_calls >= zg::kMaxBuckets) return fail(h, ZERO_ESTATE, "more than 4096 buckets in one step");
+    int mode = 0;
+    if (h->rs_calls == 0) {
+        if ((rc = resolve_mode(h, hyper, &mode))) return rc;
+        // the gradients are gone once their bucket is reduced: no re-read pass
+        if (mode == ZERO_MODE_TWO_PASS_REREAD) {
+            if (hyper->mode == ZERO_MODE_TWO_PASS_REREAD)
+                return fail(h, ZERO_EINVAL, "bucketed reduce-scatter keeps g_hat in the workspace: no REREAD mode");
+            mode = ZERO_MODE_TWO_PASS_WS;
+        }
+    } else {
+        if (!same_hyper(*hyper, h->rs_hyper))
+            return fail(h, ZERO_EINVAL, "every reduce-scatter of one step must pass the same hyper");
+        mode = h->rs_mode;
+    }
+    if (L == 0) {
+        count(h, 0, 0);
+        return ZERO_OK;
+    }
+    if (!grads) return fail(h, ZERO_EINVAL, "grads is NULL");
+    zg::Args a = base_args(h, hyper);
+    for (int r = 0; r < h->n; ++r) {
+        if ((rc = check_ptr(h, grads[r], "grads[r]"))) return rc;
+        a.grads[r] = grads[r];
+    }
+    const bool spec = mode == ZERO_MODE_SPECULATIVE;
+    const int n_out = h->stage == 3 ? 1 : h->n;
+    if (spec) {
+        if ((rc = check_ptr(h, master, "master")) || (rc = check_ptr(h, m, "m")) || (rc = check_ptr(h, v, "v")))
+            return rc;
+        if (!outs) return fail(h, ZERO_EINVAL, "params is NULL");
+        for (int r = 0; r < n_out; ++r) {
+            if ((rc = check_ptr(h, outs[r], h->stage == 3 ? "shard16" : "params[r]"))) return rc;
+            a.params[r] = outs[r];
+        }
+    } else {
+        if ((rc = ensure_ghat(h))) return rc;
+    }
+    a.master = master;
+    a.m = m;
+    a.v = v;
+    a.ws = h->ws;
+    a.slot_stride = double_buffered(h) ? h->psi_pad : 0;
+    a.base = a0;
+    a.count = L;
+    a.bucket_index = h->rs_calls;
+    const bool vec8 = (a0 % 8) == 0 && (L % 8) == 0;
+    const zg::Kind kind = !spec ? zg::Kind::kRsWs : (h->stage == 3 ? zg::Kind::kRsSpec : zg::Kind::kRsSpecReplicas);
+    if ((rc = launch(h, kind, vec8, a, static_cast<cudaStream_t>(stream), "reduce-scatter"))) return rc;
+    if (h->rs_calls == 0) {
+        h->rs_mode = mode;
+        h->rs_hyper = *hyper;
+    }
+    h->rs_calls += 1;
+    h->covered.emplace_back(a0, b0);
+    if (spec) count(h, 2 * N * L + 12 * L, 12 * L + 2 * static_cast<uint64_t>(n_out) * L);
+    else count(h, 2 * N * L, 4 * L);
+    return ZERO_OK;
+}
+
 }  // namespace
 
 void zg::set_global_error(const char* msg) { g_init_error = msg ? msg : ""; }
@@ -275,44 +347,57 @@ int zero_step(zero_handle_t h, const void* const* grads, void* const* params, fl
     a.count = P;
     a.slot_stride = double_buffered(h) ? P : 0;
 
-    if (h->stage == 3) {
+    // Bucketed steps (stage 3 always; stage 2 when grads is NULL): the
+    // gradients were consumed by the reduce-scatter calls of this step.
+    if (h->stage == 3 || (h->stage == 2 && !grads)) {
+        const bool st3 = h->stage == 3;
         if (grads) return fail(h, ZERO_EINVAL, "stage 3: grads must be NULL (use zero_reduce_scatter_bucket)");
         if (!params) return fail(h, ZERO_EINVAL, "params is NULL");
         uint64_t covered = 0;
         for (auto& iv : h->covered) covered += iv.second - iv.first;
         if (covered != P)
-            return fail(h, ZERO_ESTATE, "stage 3: reduce-scatter buckets cover " + std::to_string(covered) +
-                                            " of " + std::to_string(P) + " elements this step");
+            return fail(h, ZERO_ESTATE, std::string(st3 ? "stage 3" : "stage 2 (bucketed)") +
+                                            ": reduce-scatter buckets cover " + std::to_string(covered) + " of " +
+                                            std::to_string(P) + " elements this step");
         int mode = h->rs_mode;
         if (P == 0) {
             rc = resolve_mode(h, hyper, &mode);
             if (rc) return rc;
+            if (mode == ZERO_MODE_TWO_PASS_REREAD) mode = ZERO_MODE_TWO_PASS_WS;
         } else if (!same_hyper(*hyper, h->rs_hyper)) {
-            return fail(h, ZERO_EINVAL, "stage 3: zero_step hyper differs from the reduce-scatter calls'");
+            return fail(h, ZERO_EINVAL, "zero_step hyper differs from the reduce-scatter calls'");
         }
+        const int n_out = st3 ? 1 : h->n;
         if (any) {
-            if ((rc = check_ptr(h, params[0], "params[0]")) || (rc = check_ptr(h, master, "master")) ||
-                (rc = check_ptr(h, m, "m")) || (rc = check_ptr(h, v, "v")))
+            for (int r = 0; r < n_out; ++r) {
+                if ((rc = check_ptr(h, params[r], "params[r]"))) return rc;
+                a.params[r] = params[r];
+            }
+            if ((rc = check_ptr(h, master, "master")) || (rc = check_ptr(h, m, "m")) || (rc = check_ptr(h, v, "v")))
                 return rc;
         }
-        a.params[0] = any ? params[0] : nullptr;
         a.master = master;
         a.m = m;
         a.v = v;
         a.bucket_index = h->rs_calls;
         const bool spec = mode == ZERO_MODE_SPECULATIVE;
+        if (!spec && any) {
+            if ((rc = ensure_ghat(h))) return rc;
+            a.ws = h->ws;
+        }
         cudaError_t e = zg::launch_finalize3(spec, a, s);
         if (e != cudaSuccess) return cuda_fail(h, e, "finalize");
         if (any) {
-            rc = launch(h, spec ? zg::Kind::kRollbackShard : zg::Kind::kApplyWsShard, vec8, a, s,
-                        spec ? "rollback" : "apply");
+            zg::Kind kind = spec ? (st3 ? zg::Kind::kRollbackShard : zg::Kind::kRollbackReplicas)
+                                 : (st3 ? zg::Kind::kApplyWsShard : zg::Kind::kApplyWs);
+            rc = launch(h, kind, vec8, a, s, spec ? "rollback" : "apply");
             if (rc) return rc;
         }
         h->covered.clear();
         h->rs_calls = 0;
         h->rs_mode = -1;
         if (spec) count(h, 0, 0);
-        else count(h, 16 * P, 14 * P);
+        else count(h, 16 * P, 12 * P + 2 * static_cast<uint64_t>(n_out) * P);
         return ZERO_OK;
     }
 
@@ -393,62 +478,16 @@ int zero_reduce_scatter_bucket(zero_handle_t h, uint64_t a0, uint64_t b0, const 
                                void* stream) {
     if (!h) return fail(nullptr, ZERO_EINVAL, "handle is NULL");
     if (h->stage != 3) return fail(h, ZERO_EINVAL, "zero_reduce_scatter_bucket is for stage 3");
-    int rc = check_hyper(h, hyper);
-    if (rc) return rc;
-    if (a0 > b0 || b0 > h->psi_pad) return fail(h, ZERO_EINVAL, "bucket must satisfy 0 <= a <= b <= psi_pad");
-    const uint64_t L = b0 - a0, N = static_cast<uint64_t>(h->n);
-    for (auto& iv : h->covered)
-        if (a0 < iv.second && iv.first < b0)
-            return fail(h, ZERO_ESTATE, "bucket overlaps one already reduced this step");
-    if (h->rs_calls >= zg::kMaxBuckets) return fail(h, ZERO_ESTATE, "more than 4096 buckets in one step");
-    int mode = 0;
-    if (h->rs_calls == 0) {
-        if ((rc = resolve_mode(h, hyper, &mode))) return rc;
-    } else {
-        if (!same_hyper(*hyper, h->rs_hyper))
-            return fail(h, ZERO_EINVAL, "every reduce-scatter of one step must pass the same hyper");
-        mode = h->rs_mode;
-    }
-    if (L == 0) {
-        count(h, 0, 0);
-        return ZERO_OK;
-    }
-    if (!grads) return fail(h, ZERO_EINVAL, "grads is NULL");
-    zg::Args a = base_args(h, hyper);
-    for (int r = 0; r < h->n; ++r) {
-        if ((rc = check_ptr(h, grads[r], "grads[r]"))) return rc;
-        a.grads[r] = grads[r];
-    }
-    const bool spec = mode == ZERO_MODE_SPECULATIVE;
-    if (spec) {
-        if ((rc = check_ptr(h, master, "master")) || (rc = check_ptr(h, m, "m")) || (rc = check_ptr(h, v, "v")) ||
-            (rc = check_ptr(h, shard16, "shard16")))
-            return rc;
-    } else {
-        if ((rc = ensure_ghat(h))) return rc;
-    }
-    a.master = master;
-    a.m = m;
-    a.v = v;
-    a.params[0] = shard16;
-    a.ws = h->ws;
-    a.slot_stride = double_buffered(h) ? h->psi_pad : 0;
-    a.base = a0;
-    a.count = L;
-    a.bucket_index = h->rs_calls;
-    const bool vec8 = (a0 % 8) == 0 && (L % 8) == 0;
-    if ((rc = launch(h, spec ? zg::Kind::kRsSpec : zg::Kind::kRsWs, vec8, a, static_cast<cudaStream_t>(stream),
-                     "reduce-scatter")))
-        return rc;
-    if (h->rs_calls == 0) {
-        h->rs_mode = mode;
-        h->rs_hyper = *hyper;
-    }
-    h->rs_calls += 1;
-    h->covered.emplace_back(a0, b0);
-    if (spec) count(h, 2 * N * L + 12 * L, 12 * L + 2 * L);
-    else count(h, 2 * N * L, 4 * L);
-    return ZERO_OK;
+    void* outs[1] = {shard16};
+    return rs_bucket(h, a0, b0, grads, master, m, v, outs, hyper, stream);
+}
+
+int zero_reduce_scatter_bucket_replicas(zero_handle_t h, uint64_t a0, uint64_t b0, const void* const* grads,
+                                        float* master, float* m, float* v, void* const* params,
+                                        const zero_hyper_t* hyper, void* stream) {
+    if (!h) return fail(nullptr, ZERO_EINVAL, "handle is NULL");
+    if (h->stage != 2) return fail(h, ZERO_EINVAL, "zero_reduce_scatter_bucket_replicas is for stage 2");
+    return rs_bucket(h, a0, b0, grads, master, m, v, params, hyper, stream);
 }
 
 int zero_get_status(zero_handle_t h, void* stream, zero_result_t* out) {

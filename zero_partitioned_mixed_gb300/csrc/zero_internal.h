@@ -87,7 +87,8 @@ enum class Kind : int {
     kRollbackShard,
     kGather,
     kRsSpec,          // stage 3 bucket reduce-scatter + fused speculative Adam
-    kRsWs,            // stage 3 bucket reduce-scatter into the workspace
+    kRsWs,            // bucket reduce-scatter into the workspace (stages 2/3)
+    kRsSpecReplicas,  // stage 2 bucket reduce-scatter + fused speculative Adam + all-gather
 };
 
 // Per-thread vector width of a launch: 8 elements with 256-bit fp32 accesses

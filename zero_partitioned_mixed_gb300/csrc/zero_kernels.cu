@@ -548,11 +548,14 @@ __global__ void __launch_bounds__(kThreads) k_gather(const __grid_constant__ Arg
     }
 }
 
-// ZeRO-3 reduce-scatter of bucket [base, base+count).  SPEC: the bucket's
-// AdamW update runs here into the shadow slot and the 16-bit shard; else
-// g_hat goes to the workspace.  The last block stores the bucket's norm
-// partial and flag for the step's finaliser.
-template <int DT, class IO, bool SPEC>
+// Reduce-scatter of bucket [base, base+count) into the owners' shards
+// (ZeRO-3; and ZeRO-2 when the gradients arrive bucket by bucket during
+// backward).  SPEC: the bucket's AdamW update runs here into the shadow
+// slot and its 16-bit result goes to the shard (stage 3) or to every
+// rank's replica (TO_REPLICAS, stage 2); else g_hat goes to the workspace.
+// The last block stores the bucket's norm partial and flag for the step's
+// finaliser.
+template <int DT, class IO, bool SPEC, bool TO_REPLICAS>
 __global__ void __launch_bounds__(kThreads) k_rs(const __grid_constant__ Args a) {
     constexpr int W = IO::W;
     __shared__ Pro pro;
@@ -587,7 +590,11 @@ __global__ void __launch_bounds__(kThreads) k_rs(const __grid_constant__ Args a)
             IO::stf(a.master + dst, gi, p);
             IO::stf(a.m + dst, gi, m);
             IO::stf(a.v + dst, gi, v);
-            IO::st16(a.params[0], gi, q);
+            if (TO_REPLICAS) {
+                for (int r = 0; r < a.n_ranks; ++r) IO::st16(a.params[r], gi, q);
+            } else {
+                IO::st16(a.params[0], gi, q);
+            }
         } else {
             norm_group<W>(g, valid, acc, bad);
 #pragma unroll
@@ -679,8 +686,9 @@ cudaError_t launch_dw(Kind kind, const Args& a, cudaStream_t s, int* grid_out) {
         case Kind::kRollbackReplicas: return run(k_rollback<DT, IO, false>, a, nvec, s, grid_out);
         case Kind::kRollbackShard: return run(k_rollback<DT, IO, true>, a, nvec, s, grid_out);
         case Kind::kGather: return run(k_gather<IO>, a, nvec, s, grid_out);
-        case Kind::kRsSpec: return run(k_rs<DT, IO, true>, a, nvec, s, grid_out);
-        case Kind::kRsWs: return run(k_rs<DT, IO, false>, a, nvec, s, grid_out);
+        case Kind::kRsSpec: return run(k_rs<DT, IO, true, false>, a, nvec, s, grid_out);
+        case Kind::kRsSpecReplicas: return run(k_rs<DT, IO, true, true>, a, nvec, s, grid_out);
+        case Kind::kRsWs: return run(k_rs<DT, IO, false, false>, a, nvec, s, grid_out);
     }
     return cudaErrorInvalidValue;
 }
