@@ -122,6 +122,21 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(self.samples)}
 
 
+def max_over_ranks(x: float, dist=None, device="cpu") -> float:
+    """The slowest rank's value (timings are max-reduced across ranks)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, world_size: int, seconds: float) -> float:
+    """Whole-job throughput: every rank processed units_per_rank in the max-over-ranks time."""
+    return units_per_rank * world_size / seconds
+
+
 # ---------------------------------------------------------------- CPU oracle timing
 def oracle_timing(psi_sample: int, n: int, stage: int, dtype: str, steps: int, warmup: int,
                   budget_s: float = None):
@@ -255,9 +270,7 @@ def run_ours(args, ws, rank, local):
     total_ms = t0.elapsed_time(t1)
     step_ms = [a.elapsed_time(b) for a, b in ev]
     if ws > 1:
-        tt = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+        total_ms = max_over_ranks(total_ms, dist, "cuda")
     status = buf.status()
 
     inject_set = w.inject_step - 1
@@ -270,7 +283,7 @@ def run_ours(args, ws, rank, local):
     achieved = alg_bytes / (kernel_ms * 1e-3) / 1e9
     traffic = ncu_traffic("step_spec_flat1.5b_n8.md")
 
-    value = w.psi * K * ws / (total_ms * 1e-3)
+    value = job_throughput(w.psi * K, ws, total_ms * 1e-3)
     line = {
         "metric": METRIC, "value": value, "unit": "params/s", "n_gpus": ws, "steps": K,
         "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True,
@@ -369,10 +382,8 @@ def e2e_flat(args, w, buf, sets, hyp, stream, torch, ws, dist):
             buf.status(stream)          # device->host read of the step's result, synchronises
         t = time.perf_counter() - t0
         if ws > 1:
-            tt = torch.tensor([t], device="cuda")
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            t = float(tt.item())
-        out[name] = w.psi * K * ws / t
+            t = max_over_ranks(t, dist, "cuda")
+        out[name] = job_throughput(w.psi * K, ws, t)
     del host
     best = max(out, key=out.get)
     return {"value": out[best], "unit": "params/s", "mode": best, "modes": out,

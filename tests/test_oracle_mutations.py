@@ -1,0 +1,187 @@
+"""Plant plausible mistakes in the oracle (on the CPU) and check that the pins
+catch each one.  A pin set that lets a dropped term, a wrong sign or index,
+or a swapped operand through would not pin the oracle."""
+
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import oracle.zero_oracle as Z
+import test_oracle_pins as pins
+
+
+def _patch(monkeypatch, name, fn):
+    monkeypatch.setattr(Z, name, fn)
+    monkeypatch.setattr(oracle, name, fn, raising=False)
+    monkeypatch.setattr(pins.O, name, fn, raising=False)
+
+
+PIN_RUNS = [
+    (pins.test_partition_brute_force, dict(n=3, align=2)),
+    (pins.test_partition_toy_numbers, {}),
+    (pins.test_model_state_tables_printed_on_pages, {}),
+    (pins.test_exact_formulas_on_integers, {}),
+    (pins.test_comm_ring_printed, {}),
+    (pins.test_comm_paper_printed, {}),
+    (pins.test_rne16_fp16_vectors, {}),
+    (pins.test_rne16_bf16_vectors, {}),
+    (pins.test_tiny_case_by_hand, dict(stage=1, dt="fp16")),
+    (pins.test_tiny_case_by_hand, dict(stage=3, dt="bf16")),
+    (pins.test_tiny_case_by_hand, dict(stage=0, dt="fp16")),
+    (pins.test_loss_scale_divides_out, dict(stage=2)),
+    (pins.test_all_stages_identical, dict(dt="bf16")),
+    (pins.test_all_reduce_is_reduce_scatter_then_all_gather, {}),
+    (pins.test_adam_step1_is_lr_times_sign, {}),
+    (pins.test_zero_gradient_only_decays, {}),
+    (pins.test_adam_against_high_precision, {}),
+    (pins.test_overflow_skips_step_and_halves_scale, dict(stage=1, bad=np.inf)),
+    (pins.test_overflow_skips_step_and_halves_scale, dict(stage=3, bad=np.nan)),
+    (pins.test_norm_of_constant_gradient, {}),
+    (pins.test_clip_scales_gradient_to_max_norm, {}),
+    (pins.test_replicas_equal_cast_of_master, {}),
+]
+
+
+def _caught() -> list:
+    failed = []
+    for fn, kw in PIN_RUNS:
+        try:
+            fn(**kw)
+        except (AssertionError, ValueError, IndexError, ZeroDivisionError) as e:
+            failed.append(fn.__name__)
+    return failed
+
+
+# ---------------------------------------------------------------- mutants
+orig_adam = Z.adam_update
+orig_scalars = Z.step_scalars
+orig_rank_sum = Z.rank_sum
+orig_unscale = Z.unscale
+orig_partition = Z.partition
+orig_rne16 = Z.rne16
+orig_msb = Z.model_state_bytes
+orig_clip = Z.clip_factor
+orig_norm_shards = Z._norm_from_shards
+orig_skip = Z._skip
+
+
+def adam_swapped_beta(p, m, v, g, sc):
+    sc2 = Z.StepScalars(sc.a1, sc.b2, sc.b1, sc.a2, sc.eps, sc.dfac, sc.step_size, sc.bc2s)
+    return orig_adam(p, m, v, g, sc2)
+
+
+def adam_no_decay(p, m, v, g, sc):
+    sc2 = Z.StepScalars(sc.b1, sc.b2, sc.a1, sc.a2, sc.eps, np.float32(1.0), sc.step_size, sc.bc2s)
+    return orig_adam(p, m, v, g, sc2)
+
+
+def adam_wrong_sign(p, m, v, g, sc):
+    sc2 = Z.StepScalars(sc.b1, sc.b2, sc.a1, sc.a2, sc.eps, sc.dfac, -sc.step_size, sc.bc2s)
+    return orig_adam(p, m, v, g, sc2)
+
+
+def adam_eps_inside_sqrt(p, m, v, g, sc):
+    p = np.asarray(p, np.float32) * sc.dfac
+    m = sc.b1 * np.asarray(m, np.float32) + sc.a1 * np.asarray(g, np.float32)
+    v = sc.b2 * np.asarray(v, np.float32) + sc.a2 * (np.asarray(g, np.float32) ** 2)
+    den = np.sqrt(v + sc.eps) / sc.bc2s
+    return (p - sc.step_size * (m / den)).astype(np.float32), m.astype(np.float32), v.astype(np.float32)
+
+
+def scalars_no_bias_correction(h, t):
+    s = orig_scalars(h, t)
+    return Z.StepScalars(s.b1, s.b2, s.a1, s.a2, s.eps, s.dfac, np.float32(h.lr), np.float32(1.0))
+
+
+def scalars_t_off_by_one(h, t):
+    return orig_scalars(h, t + 1)
+
+
+def rank_sum_drops_last(gs):
+    return orig_rank_sum(list(gs)[:-1]) if len(gs) > 1 else orig_rank_sum(gs)
+
+
+def unscale_forgets_scale(s, n, scale):
+    return orig_unscale(s, n, 1.0)
+
+
+def unscale_forgets_n(s, n, scale):
+    return orig_unscale(s, 1, scale)
+
+
+def partition_off_by_one(psi, n, align=8):
+    p = orig_partition(psi, n, align)
+    offs = tuple(o + (1 if i else 0) for i, o in enumerate(p.offsets))
+    return Z.Partition(p.psi, p.n_ranks, p.align, p.psi_pad, p.shard, offs, p.real)
+
+
+def partition_no_padding(psi, n, align=8):
+    p = orig_partition(psi, n, align)
+    shard = -(-psi // n) if psi else 0
+    offs = tuple(r * shard for r in range(n))
+    real = tuple(max(0, min(psi - o, shard)) for o in offs)
+    return Z.Partition(psi, n, align, shard * n, shard, offs, real)
+
+
+def rne16_truncates(x, dtype):
+    if dtype == Z.BF16:
+        u = np.asarray(x, np.float32).view(np.uint32)
+        return (u >> np.uint32(16)).astype(np.uint16)
+    return orig_rne16(x, dtype)
+
+
+def msb_drops_grad_term(psi, n, stage, k=12):
+    if stage == 2:
+        return 2 * psi + (k * psi) // n
+    return orig_msb(psi, n, stage, k)
+
+
+def clip_wrong_comparison(norm, max_norm):
+    if Z._f32(max_norm) <= 0.0:
+        return None
+    c = Z._f32(max_norm) / (norm + 1e-6)
+    return np.float32(c) if c > 1.0 else None
+
+
+def norm_wrong_shard_index(shards, part):
+    total = 0.0
+    for r, real in enumerate(part.real):
+        x = np.asarray(shards[(r + 1) % part.n_ranks][:real], np.float64)
+        total += float(np.sum(x * x))
+    return math.sqrt(total)
+
+
+def skip_keeps_scale(state):
+    return state.copy()
+
+
+MUTANTS = [
+    ("adam_update", adam_swapped_beta),
+    ("adam_update", adam_no_decay),
+    ("adam_update", adam_wrong_sign),
+    ("adam_update", adam_eps_inside_sqrt),
+    ("step_scalars", scalars_no_bias_correction),
+    ("step_scalars", scalars_t_off_by_one),
+    ("rank_sum", rank_sum_drops_last),
+    ("unscale", unscale_forgets_scale),
+    ("unscale", unscale_forgets_n),
+    ("partition", partition_off_by_one),
+    ("partition", partition_no_padding),
+    ("rne16", rne16_truncates),
+    ("model_state_bytes", msb_drops_grad_term),
+    ("clip_factor", clip_wrong_comparison),
+    ("_norm_from_shards", norm_wrong_shard_index),
+    ("_skip", skip_keeps_scale),
+]
+
+
+def test_unmutated_oracle_passes_every_pin():
+    assert _caught() == []
+
+
+@pytest.mark.parametrize("name,mutant", MUTANTS, ids=[m.__name__ for _, m in MUTANTS])
+def test_each_planted_mistake_is_caught(monkeypatch, name, mutant):
+    _patch(monkeypatch, name, mutant)
+    assert _caught(), f"no pin catches the mutant {mutant.__name__}"

@@ -216,6 +216,23 @@ def test_tiny_case_by_hand(stage, dt):
         assert np.array_equal(res.gathered_bwd[1][0], before[3:8])
 
 
+@pytest.mark.parametrize("stage", [1, 2, 3])
+def test_loss_scale_divides_out(stage):
+    # Loss scaling: gradients computed at scale 2^10 and unscaled by 2^10 give
+    # the hand-worked result exactly (powers of two: every product is exact).
+    part = O.partition(5, 2, 2)
+    h = O.Hyper(lr=2.0 ** -6, beta1=0.5, beta2=0.75, eps=0.0)
+    p0 = [0.5, 0.25, 0.0, -0.5, 1.0]
+    st = O.init_state(stage, O.BF16, part, np.array(p0, np.float32), loss_scale=1024.0)
+    g = np.stack([_bits(np.array([1, 2, -1, 0.5, 4, 0, 0, 0]) * 1024, O.BF16),
+                  _bits(np.array([3, 2, -3, -2.5, 0, 0, 0, 0]) * 1024, O.BF16)])
+    new, res = O.step(st, g, h, [(0, 8)] if stage == 3 else None)
+    assert res.norm == math.sqrt(17.0)
+    want = np.array([0.484375, 0.234375, 0.015625, -0.484375, 0.984375], np.float32)
+    assert np.array_equal(new.master[:5], want)
+    assert new.loss_scale == 1024.0
+
+
 # ---------------------------------------------------------------- equivalence
 def _random_case(seed, psi, n, dt, scale=1.0, sigma=1e-2):
     rng = np.random.default_rng(seed)
