@@ -69,6 +69,8 @@ __all__ = [
     "adam_update", "State", "StepResult", "init_state", "step",
     "step_stage0", "step_stage1", "step_stage2", "step_stage3",
     "all_reduce_mean", "reduce_scatter_mean", "all_gather",
+    "Q_BLOCK", "quantize_blocks", "dequantize_blocks", "pack_int4", "unpack_int4",
+    "quantized_gather", "step_stage3_quantized",
 ]
 
 
@@ -587,3 +589,111 @@ def step(state: State, grads_bits: np.ndarray, h: Hyper,
         bg = [np.asarray(grads_bits)[:, a:b] for (a, b) in buckets]
         return step_stage3(state, bg, buckets, h)
     raise ValueError("stage must be 0..3")
+
+
+# ---------------------------------------------------------------------------
+# ZeRO++ quantized collectives (block-wise zero-point quantization)
+# ---------------------------------------------------------------------------
+Q_BLOCK = 256
+
+
+def quantize_blocks(x: np.ndarray, bits: int, block: int = Q_BLOCK):
+    """Block-wise zero-point (asymmetric) quantization of fp32 values.
+
+    "CMU 11-868 L18" notes, other memory optimizations (ZeRO++): parameters
+    are block-quantized from FP16 to INT8 with zero-point quantization for
+    the forward gather, and the backward reduce-scatter is quantized to INT8
+    or INT4.  Reading taken: blocks of `block` consecutive elements from the
+    start of the buffer (the last one may be short); per block lo = min,
+    hi = max, scale = (hi - lo) / (2^bits - 1) in fp32; code
+    q = rint((x - lo) / scale) clamped to [0, 2^bits - 1], or 0 when scale
+    is 0.  min/max propagate NaN (a NaN element makes its whole block NaN
+    after dequantization, so overflow detection still sees it).  Returns
+    (codes uint8, one per element; scale fp32; lo fp32).
+    """
+    if bits not in (4, 8):
+        raise ValueError("bits must be 4 or 8")
+    x = np.asarray(x, np.float32)
+    n = x.size
+    nb = (n + block - 1) // block
+    qmax = np.float32((1 << bits) - 1)
+    codes = np.zeros(n, np.uint8)
+    scale = np.zeros(nb, np.float32)
+    lo = np.zeros(nb, np.float32)
+    for k in range(nb):
+        blk = x[k * block:(k + 1) * block]
+        l, hgh = np.float32(blk.min()), np.float32(blk.max())
+        s = np.float32(hgh - l) / qmax
+        scale[k], lo[k] = s, l
+        if s != 0:
+            q = np.rint((blk - l) / s)
+            codes[k * block:(k + 1) * block] = np.clip(q, 0, qmax).astype(np.uint8)
+    return codes, scale, lo
+
+
+def dequantize_blocks(codes: np.ndarray, scale: np.ndarray, lo: np.ndarray, block: int = Q_BLOCK) -> np.ndarray:
+    """x' = lo + q * scale per block, in fp32 (a multiply, then an add)."""
+    codes = np.asarray(codes)
+    k = np.arange(codes.size) // block
+    return (lo[k] + codes.astype(np.float32) * scale[k]).astype(np.float32)
+
+
+def pack_int4(codes: np.ndarray) -> np.ndarray:
+    """Two 4-bit codes per byte: element 2i in the low nibble, 2i+1 in the high one."""
+    c = np.asarray(codes, np.uint8)
+    if c.size % 2:
+        c = np.concatenate([c, np.zeros(1, np.uint8)])
+    return (c[0::2] & 0x0F) | ((c[1::2] & 0x0F) << 4)
+
+
+def unpack_int4(packed: np.ndarray, n: int) -> np.ndarray:
+    p = np.asarray(packed, np.uint8)
+    out = np.empty(p.size * 2, np.uint8)
+    out[0::2] = p & 0x0F
+    out[1::2] = p >> 4
+    return out[:n]
+
+
+def quantized_gather(shard16: np.ndarray, a: int, b: int, dtype: str, n_ranks: int):
+    """ZeRO++ weight gather of bucket [a, b): the owners' 16-bit values are
+    block-quantized to INT8 once and every rank receives codes and scales;
+    a rank's view of the parameters is their dequantization, cast to 16 bits."""
+    x = widen16(np.asarray(shard16)[a:b], dtype)
+    codes, scale, lo = quantize_blocks(x, 8)
+    view16 = rne16(dequantize_blocks(codes, scale, lo), dtype)
+    return [(codes.copy(), scale.copy(), lo.copy()) for _ in range(n_ranks)], view16
+
+
+def step_stage3_quantized(state: "State", bucket_grads: Sequence[np.ndarray],
+                          buckets: Sequence[Tuple[int, int]], h: "Hyper", bits: int) -> Tuple["State", "StepResult"]:
+    """ZeRO-3 step whose gradient reduce-scatter is quantized (ZeRO++ qgZ).
+
+    Each rank block-quantizes its bucket gradient (blocks from the bucket's
+    start) to `bits`; the owner sums the N dequantized gradients in rank order
+    and the step proceeds exactly as step_stage3 (unscale, flag, norm, clip,
+    AdamW, cast).  Gathers are not modelled here (see quantized_gather).
+    """
+    part, n, psi = state.part, state.part.n_ranks, state.part.psi
+    pp = part.psi_pad
+    ghat = np.zeros(pp, np.float32)
+    for idx in range(len(buckets) - 1, -1, -1):
+        a, b = buckets[idx]
+        gb = np.asarray(bucket_grads[idx])
+        g = []
+        lo_i = max(0, min(psi, b) - a)
+        for r in range(n):
+            x = widen16(gb[r][:b - a], state.dtype)
+            codes, scale, lo = quantize_blocks(x, bits)
+            xq = dequantize_blocks(codes, scale, lo)
+            xq[lo_i:] = 0.0          # padding reads as zero after the exchange
+            g.append(xq)
+        ghat[a:b] = unscale(rank_sum(g), n, state.loss_scale)
+    res = StepResult(False, True, 0.0, None)
+    if has_overflow(ghat[:psi]):
+        return _skip(state), StepResult(True, False, float("nan"), None)
+    shards = [ghat[off:off + part.shard] for off in part.offsets]
+    norm = _norm_from_shards(shards, part)
+    out, c = _update_shards(state, shards, h, norm)
+    out.params[:psi] = rne16(out.master[:psi], state.dtype)
+    res.norm, res.clip = norm, c
+    return out, res

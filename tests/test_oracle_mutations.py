@@ -41,6 +41,11 @@ PIN_RUNS = [
     (pins.test_norm_of_constant_gradient, {}),
     (pins.test_clip_scales_gradient_to_max_norm, {}),
     (pins.test_replicas_equal_cast_of_master, {}),
+    (pins.test_quantizer_is_lossless_on_its_grid, {}),
+    (pins.test_quantizer_error_bound_and_order, {}),
+    (pins.test_quantizer_constant_block_and_nan, {}),
+    (pins.test_int4_packing, {}),
+    (pins.test_quantized_reduce_scatter_equals_plain_on_grid_gradients, dict(bits=8)),
 ]
 
 
@@ -65,6 +70,9 @@ orig_msb = Z.model_state_bytes
 orig_clip = Z.clip_factor
 orig_norm_shards = Z._norm_from_shards
 orig_skip = Z._skip
+orig_quant = Z.quantize_blocks
+orig_dequant = Z.dequantize_blocks
+orig_pack4 = Z.pack_int4
 
 
 def adam_swapped_beta(p, m, v, g, sc):
@@ -157,6 +165,34 @@ def skip_keeps_scale(state):
     return state.copy()
 
 
+def quant_qmax_off_by_one(x, bits, block=Z.Q_BLOCK):
+    x = np.asarray(x, np.float32)
+    codes, scale, lo = orig_quant(x, bits, block)
+    scale = scale * np.float32(((1 << bits) - 1) / (1 << bits))
+    k = np.arange(x.size) // block
+    q = np.where(scale[k] != 0, np.rint((x - lo[k]) / np.where(scale[k] != 0, scale[k], 1)), 0)
+    return np.clip(q, 0, (1 << bits) - 1).astype(np.uint8), scale, lo
+
+
+def quant_floor(x, bits, block=Z.Q_BLOCK):
+    x = np.asarray(x, np.float32)
+    codes, scale, lo = orig_quant(x, bits, block)
+    k = np.arange(x.size) // block
+    q = np.where(scale[k] != 0, np.floor((x - lo[k]) / np.where(scale[k] != 0, scale[k], 1) - 0.25), 0)
+    return np.clip(q, 0, (1 << bits) - 1).astype(np.uint8), scale, lo
+
+
+def dequant_forgets_lo(codes, scale, lo, block=Z.Q_BLOCK):
+    return orig_dequant(codes, scale, np.zeros_like(lo), block)
+
+
+def pack4_swapped_nibbles(codes):
+    c = np.asarray(codes, np.uint8)
+    if c.size % 2:
+        c = np.concatenate([c, np.zeros(1, np.uint8)])
+    return (c[1::2] & 0x0F) | ((c[0::2] & 0x0F) << 4)
+
+
 MUTANTS = [
     ("adam_update", adam_swapped_beta),
     ("adam_update", adam_no_decay),
@@ -174,6 +210,10 @@ MUTANTS = [
     ("clip_factor", clip_wrong_comparison),
     ("_norm_from_shards", norm_wrong_shard_index),
     ("_skip", skip_keeps_scale),
+    ("quantize_blocks", quant_qmax_off_by_one),
+    ("quantize_blocks", quant_floor),
+    ("dequantize_blocks", dequant_forgets_lo),
+    ("pack_int4", pack4_swapped_nibbles),
 ]
 
 

@@ -414,3 +414,99 @@ def test_clip_scales_gradient_to_max_norm():
     # max_norm above the norm: no clipping
     _, res3 = O.step(st, grads[0], O.Hyper(beta1=0.75, eps=1e-8, max_norm=norm * 2))
     assert res3.clip is None
+
+
+# ---------------------------------------------------------------- ZeRO++ quantizer
+def test_quantizer_is_lossless_on_its_grid():
+    # values lo + k*s with k in [0, 255] (k = 0 and 255 present, s dyadic):
+    # scale = 255 s / 255 = s exactly and every code is k exactly
+    rng = np.random.default_rng(21)
+    s, lo = 2.0 ** -6, -1.5
+    k = rng.integers(0, 256, 1000)
+    k[:2] = [0, 255]
+    x = (lo + k * s).astype(np.float32)
+    codes, scale, l0 = O.quantize_blocks(x, 8, block=1000)
+    assert scale[0] == np.float32(s) and l0[0] == np.float32(lo)
+    assert np.array_equal(codes, k.astype(np.uint8))
+    assert np.array_equal(O.dequantize_blocks(codes, scale, l0, block=1000), x)
+    # 4-bit: 16 levels
+    k4 = rng.integers(0, 16, 300)
+    k4[:2] = [0, 15]
+    x4 = (0.25 + k4 * 2.0 ** -3).astype(np.float32)
+    c4, s4, l4 = O.quantize_blocks(x4, 4, block=300)
+    assert np.array_equal(c4, k4.astype(np.uint8)) and s4[0] == np.float32(0.125)
+
+
+def test_quantizer_error_bound_and_order():
+    rng = np.random.default_rng(22)
+    x = rng.normal(0, 3, 5000).astype(np.float32)
+    for bits in (8, 4):
+        codes, scale, lo = O.quantize_blocks(x, bits)
+        xq = O.dequantize_blocks(codes, scale, lo)
+        k = np.arange(x.size) // O.Q_BLOCK
+        ulp = np.spacing(np.abs(x).max()).astype(np.float64)
+        assert np.all(np.abs(xq.astype(np.float64) - x) <= scale[k] / 2 + 4 * ulp)
+        for b in range(scale.size):
+            blk = slice(b * O.Q_BLOCK, (b + 1) * O.Q_BLOCK)
+            xb, cb = x[blk], codes[blk]
+            assert cb[np.argmin(xb)] == 0 and cb[np.argmax(xb)] == (1 << bits) - 1
+            order = np.argsort(xb, kind="stable")
+            assert np.all(np.diff(cb[order].astype(int)) >= 0)      # codes are monotone
+    assert (O.quantize_blocks(x, 8)[0].size, O.quantize_blocks(x, 8)[1].size) == (5000, 20)
+
+
+def test_quantizer_constant_block_and_nan():
+    c, s, l = O.quantize_blocks(np.full(10, 0.375, np.float32), 8)
+    assert s[0] == 0 and not np.any(c) and np.all(O.dequantize_blocks(c, s, l) == 0.375)
+    x = np.ones(300, np.float32)
+    x[5] = np.nan
+    c, s, l = O.quantize_blocks(x, 8)
+    assert np.all(np.isnan(O.dequantize_blocks(c, s, l)[:256]))   # the NaN poisons its block
+    assert np.all(O.dequantize_blocks(c, s, l)[256:] == 1.0)
+
+
+def test_int4_packing():
+    assert list(O.pack_int4(np.array([1, 2, 15, 0], np.uint8))) == [0x21, 0x0F]
+    c = np.random.default_rng(3).integers(0, 16, 301).astype(np.uint8)
+    assert np.array_equal(O.unpack_int4(O.pack_int4(c), 301), c)
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_quantized_reduce_scatter_equals_plain_on_grid_gradients(bits):
+    # gradients whose every quantization block spans at most 2^bits levels of a
+    # dyadic grid are exchanged losslessly: the ZeRO++ step equals ZeRO-3's
+    rng = np.random.default_rng(23)
+    n, psi = 3, 700
+    part = O.partition(psi, n, 8)
+    buckets = [(0, 256), (256, 520), (520, part.psi_pad)]
+    master = rng.normal(0, 0.02, psi).astype(np.float32)
+    levels = (1 << bits) - 1
+    g = np.zeros((n, part.psi_pad), np.float32)
+    for r in range(n):
+        for (a, b) in buckets:
+            for k0 in range(a, b, O.Q_BLOCK):
+                k1 = min(b, k0 + O.Q_BLOCK)
+                q = rng.integers(0, levels + 1, k1 - k0)
+                q[:2] = [0, levels]
+                g[r, k0:k1] = (q - levels // 2) * 2.0 ** -10
+    g[:, psi:] = 0
+    gb = O.rne16(g, O.BF16)
+    assert np.array_equal(O.widen16(gb, O.BF16), g)
+    h = O.Hyper(weight_decay=0.1)
+    st = O.init_state(3, O.BF16, part, master)
+    bg = [gb[:, a:b] for (a, b) in buckets]
+    want, r1 = O.step_stage3(st, bg, buckets, h)
+    got, r2 = O.step_stage3_quantized(st, bg, buckets, h, bits)
+    assert np.array_equal(want.master, got.master) and np.array_equal(want.params, got.params)
+    assert r1.norm == r2.norm
+
+
+def test_quantized_gather_reproduces_grid_weights():
+    # a shard whose blocks hold at most 256 grid levels is gathered exactly
+    rng = np.random.default_rng(24)
+    q = rng.integers(0, 256, 600)
+    for k0 in range(0, 600, O.Q_BLOCK):
+        q[k0:k0 + 2] = [0, 255]                  # every block spans the full 256 levels
+    w = O.rne16(((q - 128) * 2.0 ** -9).astype(np.float32), O.BF16)
+    outs, view = O.quantized_gather(w, 0, 600, O.BF16, 4)
+    assert len(outs) == 4 and np.array_equal(view, w)
