@@ -53,7 +53,7 @@ def measured_peaks():
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for f in ("zero_kernels.cu", "zero_internal.h"):
+    for f in ("zero_kernels.cu", "zero_internal.h", "zero_device.cuh"):
         with open(os.path.join(ROOT, "zero_partitioned_mixed_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -511,29 +511,32 @@ def bench_stage3(w, buckets, steps, warmup, torch, S, Z, flush_l2=False):
     grows = [gbuf[r] for r in range(N)]
     orows = [outs[r] for r in range(N)]
 
-    def one_step(timer):
+    def one_step(tg, tr, tf):
         for (a, b) in buckets:
             if flush is not None:
                 flush.zero_()
-            with timer:
+            with tg:
                 buf.gather(a, b, orows)
         for (a, b) in reversed(buckets):
             if flush is not None:
                 flush.zero_()
-            with timer:
+            with tg:
                 buf.gather(a, b, orows)
+            with tr:
                 buf.reduce_scatter(a, b, grows, hyp)
-        with timer:
+        with tf:
             buf.step(hyp)
 
     for _ in range(warmup):
-        one_step(CallTimer(torch))
+        one_step(CallTimer(torch), CallTimer(torch), CallTimer(torch))
     torch.cuda.synchronize()
-    timer = CallTimer(torch)
+    tg, tr, tf = CallTimer(torch), CallTimer(torch), CallTimer(torch)
     before = _bytes_total(buf)
     for _ in range(steps):
-        one_step(timer)
-    ms = timer.total_ms() / steps
+        one_step(tg, tr, tf)
+    bench_stage3.parts = {"gather_ms": tg.total_ms() / steps, "reduce_scatter_ms": tr.total_ms() / steps,
+                          "finish_ms": tf.total_ms() / steps}
+    ms = sum(bench_stage3.parts.values())
     per_step = _bytes_delta(buf, before) / steps
     st = buf.status()
     buf.close()
@@ -585,6 +588,72 @@ def bench_stage2_buckets(w, bucket, steps, warmup, torch, S, Z):
     return ms, per_step, st, len(buckets)
 
 
+def bench_stage3_zeropp(w, buckets, steps, warmup, torch, S, Z, bits):
+    """ZeRO-3 with the ZeRO++ exchanges: INT8 block-quantized parameter gathers
+    (forward and backward) and a reduce-scatter of the ranks' INT8/INT4
+    block-quantized gradients, then the step.  The ranks' gradient codes are
+    produced once before timing (the producer-side quantization belongs to
+    backward); its own time is measured separately on one bucket."""
+    from zero_partitioned_mixed_gb300.buffers import RankBuffers
+    buf = RankBuffers(w.psi, w.n_ranks, 3, w.dtype, double_buffer=True)
+    P, N = buf.psi_pad, w.n_ranks
+    td = S.torch_dtype(w.dtype)
+    zdt = Z.ZERO_BF16 if w.dtype == "bf16" else Z.ZERO_FP16
+    mv, mm, vv = buf.state(0)
+    S.draw_master(w, mv, w.psi)
+    S.draw_moments(w, mm, vv, w.psi)
+    buf.params[:P].copy_(mv.to(td))
+    lmax = max(b - a for a, b in buckets)
+    lpad = (lmax + 7) // 8 * 8
+    nb = (lmax + 255) // 256
+    gbuf = torch.empty((N, lpad), dtype=td, device="cuda")
+    for r in range(N):
+        S.draw_grads(w, gbuf[r], lmax, 1, r, w.loss_scale)
+    cbytes = (lpad if bits == 8 else lpad // 2 + 16)
+    gcodes = torch.empty((N, (cbytes + 15) // 16 * 16), dtype=torch.uint8, device="cuda")
+    gscales = torch.empty((N, 2 * nb + 2), dtype=torch.float32, device="cuda")
+    qt = CallTimer(torch)
+    for r in range(N):
+        with qt:
+            Z.zero_quantize_blocks(zdt, bits, gbuf[r], lmax, gcodes[r], gscales[r])
+    quant_ms = qt.total_ms() / N
+    ocodes = torch.empty((N, (lpad + 15) // 16 * 16), dtype=torch.uint8, device="cuda")
+    oscales = torch.empty((N, 2 * nb + 2), dtype=torch.float32, device="cuda")
+    buf.set_scaler(w.loss_scale, 0, 0)
+    hyp = Z.hyper(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay, w.max_norm, Z.ZERO_MODE_AUTO)
+    cr, sr = [gcodes[r] for r in range(N)], [gscales[r] for r in range(N)]
+    ocr, osr = [ocodes[r] for r in range(N)], [oscales[r] for r in range(N)]
+
+    def one_step(tg, tr, tf):
+        for (a, b) in buckets:
+            with tg:
+                Z.zero_gather_bucket_q8(buf.h, a, b, buf.params, ocr, osr)
+        for (a, b) in reversed(buckets):
+            with tg:
+                Z.zero_gather_bucket_q8(buf.h, a, b, buf.params, ocr, osr)
+            with tr:
+                Z.zero_reduce_scatter_bucket_q(buf.h, a, b, bits, cr, sr, buf.master, buf.m, buf.v,
+                                               buf.params, hyp)
+        with tf:
+            buf.step(hyp)
+
+    for _ in range(warmup):
+        one_step(CallTimer(torch), CallTimer(torch), CallTimer(torch))
+    tg, tr, tf = CallTimer(torch), CallTimer(torch), CallTimer(torch)
+    before = _bytes_total(buf)
+    for _ in range(steps):
+        one_step(tg, tr, tf)
+    parts = {"gather_ms": tg.total_ms() / steps, "reduce_scatter_ms": tr.total_ms() / steps,
+             "finish_ms": tf.total_ms() / steps}
+    ms = sum(parts.values())
+    per_step = _bytes_delta(buf, before) / steps
+    st = buf.status()
+    buf.close()
+    del gbuf, gcodes, gscales, ocodes, oscales
+    torch.cuda.empty_cache()
+    return ms, per_step, st, quant_ms, lmax, parts
+
+
 def run_other(args, ws, rank, local):
     import dataclasses
 
@@ -615,6 +684,29 @@ def run_other(args, ws, rank, local):
         lines.append(_line(w.name, w.psi / (ms * 1e-3), ms, args.steps, args.warmup, bps, w.dtype,
                            {"stage": 2, "buckets": nb, "mode": "speculative, fused per bucket, one "
                             "constant-size gradient buffer per rank", "l2": "inputs larger than L2"}))
+    elif args.workload == "llama7b-zeropp":
+        w = S.LLAMA7B
+        buckets = S.layer_buckets(S.llama7b_shapes(), w.psi)
+        for bits in (8, 4):
+            ms, bps, st, qms, lmax, parts = bench_stage3_zeropp(w, buckets, args.steps, args.warmup, torch, S, Z,
+                                                                bits)
+            lines.append(_line(f"{w.name}_zeropp_int8gather_int{bits}rs", w.psi / (ms * 1e-3), ms, args.steps,
+                               args.warmup, bps, w.dtype,
+                               {"stage": 3, "buckets": len(buckets), "gather": "int8 blocks of 256 (qwZ)",
+                                "reduce_scatter": f"int{bits} blocks of 256 (qgZ)",
+                                "producer_quantize_ms_per_rank_per_layer": qms, "layer_elems": lmax,
+                                "l2": "inputs larger than L2", **parts}))
+    elif args.workload in ("flat-zero3", "flat-zeropp"):
+        psi = args.psi or (1 << 25)
+        w = S.Workload(f"flat_psi{psi}_n8_stage3_bf16", psi, 8, 3, "bf16", 1, grad_sigma=1e-3)
+        buckets = S.flat_buckets(psi, 8, max(64, psi // 4))
+        if args.workload == "flat-zero3":
+            ms, bps, st = bench_stage3(w, buckets, args.steps, args.warmup, torch, S, Z)
+            parts = bench_stage3.parts
+        else:
+            ms, bps, st, _, _, parts = bench_stage3_zeropp(w, buckets, args.steps, args.warmup, torch, S, Z, 8)
+        lines.append(_line(w.name + ("_zeropp" if args.workload == "flat-zeropp" else ""), psi / (ms * 1e-3), ms,
+                           args.steps, args.warmup, bps, "bf16", {"stage": 3, "buckets": len(buckets), **parts}))
     elif args.workload == "gpt2":
         w = S.GPT2
         ms, bps, st = bench_dense(w, 2, args.steps, args.warmup, torch, S, Z)
@@ -626,7 +718,7 @@ def run_other(args, ws, rank, local):
         ms, bps, st = bench_stage3(w, buckets, args.steps, args.warmup, torch, S, Z)
         lines.append(_line(w.name, w.psi / (ms * 1e-3), ms, args.steps, args.warmup, bps, w.dtype,
                            {"stage": 3, "buckets": len(buckets), "mode": "speculative, fused per bucket",
-                            "l2": "inputs larger than L2"}))
+                            "l2": "inputs larger than L2", **bench_stage3.parts}))
     elif args.workload == "sweep":
         for psi, n in S.sweep_points():
             for stage in (1, 2, 3):
@@ -655,7 +747,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=4)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["flat1.5b", "toy", "gpt2", "llama7b", "sweep", "zero2-buckets"], default="flat1.5b")
+    ap.add_argument("--workload", choices=["flat1.5b", "toy", "gpt2", "llama7b", "sweep", "zero2-buckets", "llama7b-zeropp",
+                                      "flat-zero3", "flat-zeropp"], default="flat1.5b")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--psi", type=int, default=None, help="override psi of the flat workload (profiling)")

@@ -236,6 +236,49 @@ ZERO_API int zero_reduce_scatter_bucket_replicas(zero_handle_t h, uint64_t a, ui
                                         void* const* params, const zero_hyper_t* hyper, void* stream);
 
 /*
+ * ZeRO++ block-quantized exchanges.  ("CMU 11-868 L18" notes, other memory
+ * optimizations: ZeRO++ block-quantizes parameters from 16 bits to INT8 with
+ * zero-point quantization for the forward gather, and quantizes the
+ * backward reduce-scatter to INT8 or INT4.)
+ * Format: blocks of ZERO_Q_BLOCK elements counted from the start of the
+ * buffer (or bucket); per block lo = min and hi = max (a NaN makes both NaN),
+ * scale = (hi - lo) / (2^bits - 1) and inv = (2^bits - 1) / (hi - lo) in
+ * fp32, code = rint((x - lo) * inv) clamped to [0, 2^bits - 1] (0 when
+ * scale == 0; 0 for a NaN); dequantized
+ * x' = lo + code * scale (fp32 multiply, then add).  Codes: one byte per
+ * element (bits = 8) or two per byte with the even element in the low nibble
+ * (bits = 4); `scales` holds one {scale, lo} float pair per block.  Code
+ * buffers and 16-bit buffers must be 16-byte aligned, scales 8-byte aligned.
+ */
+#define ZERO_Q_BLOCK 256
+
+/* Quantize count 16-bit values (a rank's bucket gradient before the
+ * reduce-scatter, qgZ).  Needs no handle: errors via zero_last_error(NULL). */
+ZERO_API int zero_quantize_blocks(int dtype, int bits, const void* src16, uint64_t count, void* codes,
+                         float* scales, void* stream);
+
+/* Dequantize count values to 16 bits (RNE): what a rank computes with after
+ * a quantized gather.  Needs no handle. */
+ZERO_API int zero_dequantize_blocks(int dtype, int bits, const void* codes, const float* scales, uint64_t count,
+                           void* out16, void* stream);
+
+/* a9 with qwZ: the owners' 16-bit values of bucket [a, b) are quantized to
+ * INT8 once and every rank r receives the codes (codes_out[r], b - a bytes)
+ * and scales (scales_out[r], 2*ceil((b-a)/256) floats).  Stage 3 only.
+ * Errors: EINVAL, ECUDA. */
+ZERO_API int zero_gather_bucket_q8(zero_handle_t h, uint64_t a, uint64_t b, const void* shard16,
+                          void* const* codes_out, float* const* scales_out, void* stream);
+
+/* a10 with qgZ: zero_reduce_scatter_bucket whose inputs are the N ranks'
+ * quantized bucket gradients (codes[r], scales[r], as zero_quantize_blocks
+ * writes them for the bucket's b - a elements).  The owner sums the
+ * dequantized values in rank order; everything after is as for
+ * zero_reduce_scatter_bucket, and zero_step finishes the step.  Stage 3. */
+ZERO_API int zero_reduce_scatter_bucket_q(zero_handle_t h, uint64_t a, uint64_t b, int bits,
+                                 const void* const* codes, const float* const* scales, float* master,
+                                 float* m, float* v, void* shard16, const zero_hyper_t* hyper, void* stream);
+
+/*
  * zero_get_status -- a11: copy the device status of the last step to the
  * host struct *out (host pointer).  Synchronises the given stream.
  * Errors: EINVAL, ECUDA.

@@ -605,10 +605,11 @@ def quantize_blocks(x: np.ndarray, bits: int, block: int = Q_BLOCK):
     the forward gather, and the backward reduce-scatter is quantized to INT8
     or INT4.  Reading taken: blocks of `block` consecutive elements from the
     start of the buffer (the last one may be short); per block lo = min,
-    hi = max, scale = (hi - lo) / (2^bits - 1) in fp32; code
-    q = rint((x - lo) / scale) clamped to [0, 2^bits - 1], or 0 when scale
-    is 0.  min/max propagate NaN (a NaN element makes its whole block NaN
-    after dequantization, so overflow detection still sees it).  Returns
+    hi = max, scale = (hi - lo) / (2^bits - 1) and inv = (2^bits - 1) / (hi - lo)
+    in fp32; code q = rint((x - lo) * inv) clamped to [0, 2^bits - 1], or 0
+    when scale is 0 (one division per block, a multiply per element).  min/max propagate NaN (a NaN element makes its whole block NaN
+    after dequantization, so overflow detection still sees it); a code that
+    comes out NaN is stored as 0.  Returns
     (codes uint8, one per element; scale fp32; lo fp32).
     """
     if bits not in (4, 8):
@@ -622,11 +623,17 @@ def quantize_blocks(x: np.ndarray, bits: int, block: int = Q_BLOCK):
     lo = np.zeros(nb, np.float32)
     for k in range(nb):
         blk = x[k * block:(k + 1) * block]
-        l, hgh = np.float32(blk.min()), np.float32(blk.max())
-        s = np.float32(hgh - l) / qmax
+        # min/max with NaN propagation; a zero bound is taken as +0
+        l = np.float32(blk.min()) + np.float32(0.0)
+        hgh = np.float32(blk.max()) + np.float32(0.0)
+        rng = np.float32(hgh - l)
+        s = rng / qmax
         scale[k], lo[k] = s, l
         if s != 0:
-            q = np.rint((blk - l) / s)
+            with np.errstate(invalid="ignore", divide="ignore", over="ignore"):
+                inv = qmax / rng
+                q = np.rint((blk - l) * inv)
+            q = np.where(np.isnan(q), 0, q)          # a NaN's code is 0 (its block is NaN anyway)
             codes[k * block:(k + 1) * block] = np.clip(q, 0, qmax).astype(np.uint8)
     return codes, scale, lo
 
@@ -635,7 +642,8 @@ def dequantize_blocks(codes: np.ndarray, scale: np.ndarray, lo: np.ndarray, bloc
     """x' = lo + q * scale per block, in fp32 (a multiply, then an add)."""
     codes = np.asarray(codes)
     k = np.arange(codes.size) // block
-    return (lo[k] + codes.astype(np.float32) * scale[k]).astype(np.float32)
+    with np.errstate(invalid="ignore", over="ignore"):
+        return (lo[k] + codes.astype(np.float32) * scale[k]).astype(np.float32)
 
 
 def pack_int4(codes: np.ndarray) -> np.ndarray:

@@ -1,0 +1,148 @@
+"""ZeRO++ quantized exchanges on the GPU vs the oracle: block quantizer and
+dequantizer (INT8 / INT4, both 16-bit formats, ragged sizes), the INT8
+quantized ZeRO-3 gather, and ZeRO-3 steps whose reduce-scatter consumes the
+ranks' quantized gradients (speculative and two-pass, overflow)."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from _parity import bits16, bits32
+from zero_partitioned_mixed_gb300 import _binding as B
+from zero_partitioned_mixed_gb300 import synth as S
+from zero_partitioned_mixed_gb300.buffers import RankBuffers
+
+pytestmark = pytest.mark.gpu
+ZDT = {"fp16": B.ZERO_FP16, "bf16": B.ZERO_BF16}
+
+
+def _nb(count):
+    return (count + O.Q_BLOCK - 1) // O.Q_BLOCK
+
+
+def _codes_buf(count, bits):
+    nbytes = count if bits == 8 else (count + 1) // 2
+    return torch.zeros(max(16, (nbytes + 15) // 16 * 16), dtype=torch.uint8, device="cuda")
+
+
+def _quantize_gpu(x16, dtype, bits):
+    n = x16.numel()
+    codes = _codes_buf(n, bits)
+    scales = torch.zeros(max(2, 2 * _nb(n)), dtype=torch.float32, device="cuda")
+    B.zero_quantize_blocks(ZDT[dtype], bits, x16, n, codes, scales)
+    return codes, scales
+
+
+def _oracle_codes(x_bits, dtype, bits):
+    codes, scale, lo = O.quantize_blocks(O.widen16(x_bits, dtype), bits)
+    packed = codes if bits == 8 else O.pack_int4(codes)
+    return packed, scale, lo
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("bits", [8, 4])
+@pytest.mark.parametrize("count", [1, 7, 255, 256, 257, 4096, 100_003])
+def test_quantize_and_dequantize_match_oracle(dtype, bits, count):
+    g = torch.Generator(device="cuda")
+    g.manual_seed(count * 7 + bits)
+    x = torch.empty(max(8, (count + 7) // 8 * 8), dtype=S.torch_dtype(dtype), device="cuda")
+    x[:count] = (torch.randn(count, generator=g, device="cuda") * 3).to(x.dtype)
+    x[count:] = 0
+    if count > 300:
+        x[256:512] = x[300]                     # a constant block: scale 0
+    codes, scales = _quantize_gpu(x[:count], dtype, bits)
+    xb = bits16(x[:count])
+    packed, scale, lo = _oracle_codes(xb, dtype, bits)
+    got = codes.cpu().numpy()[:packed.size]
+    assert np.array_equal(got, packed)
+    sc = scales.cpu().numpy()[:2 * _nb(count)]
+    assert np.array_equal(sc[0::2].view(np.uint32), scale.view(np.uint32))
+    assert np.array_equal(sc[1::2].view(np.uint32), lo.view(np.uint32))
+    out = torch.zeros_like(x)
+    B.zero_dequantize_blocks(ZDT[dtype], bits, codes, scales, count, out)
+    want = O.rne16(O.dequantize_blocks(O.quantize_blocks(O.widen16(xb, dtype), bits)[0], scale, lo), dtype)
+    assert np.array_equal(bits16(out[:count]), want)
+
+
+@pytest.mark.parametrize("a,b", [(0, 70_000), (1024, 1032), (13, 5_013), (256, 257)])
+def test_quantized_gather_matches_oracle(a, b):
+    psi, n, dt = 80_000, 4, "bf16"
+    buf = RankBuffers(psi, n, 3, dt)
+    P = buf.psi_pad
+    buf.params[:P].copy_((torch.randn(P, device="cuda") * 0.02).to(torch.bfloat16))
+    L = b - a
+    codes = [_codes_buf(L, 8) for _ in range(n)]
+    scales = [torch.zeros(2 * _nb(L), dtype=torch.float32, device="cuda") for _ in range(n)]
+    B.zero_gather_bucket_q8(buf.h, a, b, buf.params, codes, scales)
+    outs, view = O.quantized_gather(bits16(buf.params[:P]), a, b, dt, n)
+    for r in range(n):
+        c, s, l = outs[r]
+        assert np.array_equal(codes[r].cpu().numpy()[:L], c)
+        sc = scales[r].cpu().numpy()
+        assert np.array_equal(sc[0::2], s) and np.array_equal(sc[1::2], l)
+        deq = torch.zeros(max(8, (L + 7) // 8 * 8), dtype=torch.bfloat16, device="cuda")
+        B.zero_dequantize_blocks(B.ZERO_BF16, 8, codes[r], scales[r], L, deq)
+        assert np.array_equal(bits16(deq[:L]), view)
+    assert buf.bytes_moved()["hbm_write_bytes"] == n * (L + 8 * _nb(L))
+    buf.close()
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+@pytest.mark.parametrize("double_buffer", [True, False])
+def test_quantized_reduce_scatter_step_matches_oracle(bits, double_buffer):
+    psi, n, dt = 150_001, 4, "bf16"
+    part = O.partition(psi, n, 8)
+    P = part.psi_pad
+    buckets = [(0, 40_000), (40_000, 40_013), (40_013, 99_999), (99_999, P)]
+    buf = RankBuffers(psi, n, 3, dt, double_buffer=double_buffer)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(bits)
+    master = torch.randn(psi, generator=g, device="cuda") * 0.02
+    st = O.init_state(3, dt, part, master.cpu().numpy())
+    mv, _, _ = buf.state(0)
+    mv.copy_(torch.from_numpy(st.master))
+    buf.params[:P].copy_(torch.from_numpy(st.params.view(np.int16)).view(torch.bfloat16))
+    hb, ho = B.hyper(weight_decay=0.05), O.Hyper(weight_decay=0.05)
+    for step in range(3):
+        grads = torch.zeros((n, buf.stride), dtype=torch.bfloat16, device="cuda")
+        grads[:, :psi] = (torch.randn((n, psi), generator=g, device="cuda") * 1e-2).to(torch.bfloat16)
+        if step == 1:
+            grads[2, 77_777] = float("inf")
+        gb = bits16(grads)
+        for (a, b) in reversed(buckets):
+            L = b - a
+            codes, scales = [], []
+            for r in range(n):
+                src = torch.zeros(max(8, (L + 7) // 8 * 8), dtype=torch.bfloat16, device="cuda")
+                src[:L].copy_(grads[r, a:b])
+                c, s = _quantize_gpu(src[:L], dt, bits)
+                codes.append(c)
+                scales.append(s)
+            B.zero_reduce_scatter_bucket_q(buf.h, a, b, bits, codes, scales, buf.master, buf.m, buf.v,
+                                           buf.params, hb)
+        buf.step(hb)
+        st, res = O.step_stage3_quantized(st, [gb[:, a:b] for (a, b) in buckets], buckets, ho, bits)
+        s = buf.status()
+        assert bool(s["overflow"]) == res.overflow == (step == 1)
+        assert s["steps_applied"] == st.t
+        if res.applied:
+            assert abs(s["grad_norm"] - res.norm) <= 1e-5 * res.norm
+        gm, gmm, gv = buf.state(s["state_slot"])
+        assert np.array_equal(bits32(gm), st.master.view(np.uint32))
+        assert np.array_equal(bits32(gmm), st.m.view(np.uint32))
+        assert np.array_equal(bits32(gv), st.v.view(np.uint32))
+        assert np.array_equal(bits16(buf.params[:P]), st.params)
+    buf.close()
+
+
+def test_quantized_calls_reject_bad_arguments():
+    x = torch.zeros(64, dtype=torch.float16, device="cuda")
+    with pytest.raises(B.ZeroError):
+        B.zero_quantize_blocks(B.ZERO_FP16, 3, x, 64, x, x)
+    with pytest.raises(B.ZeroError):
+        B.zero_quantize_blocks(B.ZERO_FP16, 8, x.view(-1)[1:], 8, x, x)
+    buf = RankBuffers(1024, 2, 2, "fp16")
+    with pytest.raises(B.ZeroError):
+        B.zero_gather_bucket_q8(buf.h, 0, 8, buf.params, [x, x], [x, x])
+    buf.close()

@@ -20,8 +20,10 @@ EXPORTS = (
     "zero_init_partition", "zero_partition_info", "zero_set_scaler", "zero_step",
     "zero_gather_bucket", "zero_reduce_scatter_bucket", "zero_get_status",
     "zero_bytes_moved", "zero_last_error", "zero_destroy", "zero_step_noalloc",
-    "zero_reduce_scatter_bucket_replicas",
+    "zero_reduce_scatter_bucket_replicas", "zero_quantize_blocks", "zero_dequantize_blocks",
+    "zero_gather_bucket_q8", "zero_reduce_scatter_bucket_q",
 )
+ZERO_Q_BLOCK = 256
 
 
 class ZeroError(RuntimeError):
@@ -81,6 +83,11 @@ def load_library():
     lib.zero_reduce_scatter_bucket.argtypes = [P, U64, U64, C.POINTER(P), P, P, P, P, C.POINTER(Hyper), P]
     lib.zero_reduce_scatter_bucket_replicas.argtypes = [P, U64, U64, C.POINTER(P), P, P, P, C.POINTER(P),
                                                          C.POINTER(Hyper), P]
+    lib.zero_quantize_blocks.argtypes = [I32, I32, P, U64, P, P, P]
+    lib.zero_dequantize_blocks.argtypes = [I32, I32, P, P, U64, P, P]
+    lib.zero_gather_bucket_q8.argtypes = [P, U64, U64, P, C.POINTER(P), C.POINTER(P), P]
+    lib.zero_reduce_scatter_bucket_q.argtypes = [P, U64, U64, I32, C.POINTER(P), C.POINTER(P), P, P, P, P,
+                                                 C.POINTER(Hyper), P]
     lib.zero_get_status.argtypes = [P, P, C.POINTER(Result)]
     lib.zero_bytes_moved.argtypes = [P, C.POINTER(Bytes)]
     lib.zero_last_error.argtypes = [P]
@@ -194,6 +201,28 @@ def zero_reduce_scatter_bucket_replicas(h, a: int, b: int, grads, master, m, v, 
                                                             _ptr(v), _ptr_array(params), C.byref(hyp),
                                                             _stream(stream))
     _check(rc, h)
+
+
+def zero_quantize_blocks(dtype: int, bits: int, src16, count: int, codes, scales, stream=None):
+    _check(load_library().zero_quantize_blocks(dtype, bits, _ptr(src16), count, _ptr(codes), _ptr(scales),
+                                               _stream(stream)), None)
+
+
+def zero_dequantize_blocks(dtype: int, bits: int, codes, scales, count: int, out16, stream=None):
+    _check(load_library().zero_dequantize_blocks(dtype, bits, _ptr(codes), _ptr(scales), count, _ptr(out16),
+                                                 _stream(stream)), None)
+
+
+def zero_gather_bucket_q8(h, a: int, b: int, shard16, codes_out, scales_out, stream=None):
+    _check(load_library().zero_gather_bucket_q8(h, a, b, _ptr(shard16), _ptr_array(codes_out),
+                                                _ptr_array(scales_out), _stream(stream)), h)
+
+
+def zero_reduce_scatter_bucket_q(h, a: int, b: int, bits: int, codes, scales, master, m, v, shard16, hyp: Hyper,
+                                 stream=None):
+    _check(load_library().zero_reduce_scatter_bucket_q(h, a, b, bits, _ptr_array(codes), _ptr_array(scales),
+                                                       _ptr(master), _ptr(m), _ptr(v), _ptr(shard16), C.byref(hyp),
+                                                       _stream(stream)), h)
 
 
 def zero_get_status(h, stream=None) -> dict:

@@ -166,7 +166,8 @@ bool same_hyper(const zero_hyper_t& x, const zero_hyper_t& y) {
 // bucket (stage 3 always; stage 2 when the caller reduces during backward).
 // outs: the 16-bit shard (stage 3) or the N replicas (stage 2).
 int rs_bucket(zero_handle* h, uint64_t a0, uint64_t b0, const void* const* grads, float* master, float* m,
-              float* v, void* const* outs, const zero_hyper_t* hyper, void* stream) {
+              float* v, void* const* outs, const zero_hyper_t* hyper, void* stream, int qbits = 0,
+              const float* const* qscales = nullptr) {
     int rc = check_hyper(h, hyper);
     if (rc) return rc;
     if (a0 > b0 || b0 > h->psi_pad) return fail(h, ZERO_EINVAL, "bucket must satisfy 0 <= a <= b <= psi_pad");
@@ -196,9 +197,15 @@ int rs_bucket(zero_handle* h, uint64_t a0, uint64_t b0, const void* const* grads
     if (!grads) return fail(h, ZERO_EINVAL, "grads is NULL");
     zg::Args a = base_args(h, hyper);
     for (int r = 0; r < h->n; ++r) {
-        if ((rc = check_ptr(h, grads[r], "grads[r]"))) return rc;
+        if ((rc = check_ptr(h, grads[r], qbits ? "codes[r]" : "grads[r]"))) return rc;
         a.grads[r] = grads[r];
+        if (qbits) {
+            if (!qscales || !qscales[r] || (reinterpret_cast<uintptr_t>(qscales[r]) & 7u))
+                return fail(h, ZERO_EINVAL, "scales[r] is NULL or not 8-byte aligned");
+            a.qsrc[r] = qscales[r];
+        }
     }
+    a.qbits = qbits;
     const bool spec = mode == ZERO_MODE_SPECULATIVE;
     const int n_out = h->stage == 3 ? 1 : h->n;
     if (spec) {
@@ -221,18 +228,28 @@ int rs_bucket(zero_handle* h, uint64_t a0, uint64_t b0, const void* const* grads
     a.count = L;
     a.bucket_index = h->rs_calls;
     const bool vec8 = (a0 % 8) == 0 && (L % 8) == 0;
-    const zg::Kind kind = !spec ? zg::Kind::kRsWs : (h->stage == 3 ? zg::Kind::kRsSpec : zg::Kind::kRsSpecReplicas);
-    if ((rc = launch(h, kind, vec8, a, static_cast<cudaStream_t>(stream), "reduce-scatter"))) return rc;
+    if (qbits) {
+        const cudaError_t e = zg::launch_q(spec ? zg::QKind::kRsQSpec : zg::QKind::kRsQWs, h->dtype, qbits,
+                                           pick_vec(vec8, a), a, static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return cuda_fail(h, e, "quantized reduce-scatter");
+    } else {
+        const zg::Kind kind =
+            !spec ? zg::Kind::kRsWs : (h->stage == 3 ? zg::Kind::kRsSpec : zg::Kind::kRsSpecReplicas);
+        if ((rc = launch(h, kind, vec8, a, static_cast<cudaStream_t>(stream), "reduce-scatter"))) return rc;
+    }
     if (h->rs_calls == 0) {
         h->rs_mode = mode;
         h->rs_hyper = *hyper;
     }
     h->rs_calls += 1;
     h->covered.emplace_back(a0, b0);
-    if (spec) count(h, 2 * N * L + 12 * L, 12 * L + 2 * static_cast<uint64_t>(n_out) * L);
-    else count(h, 2 * N * L, 4 * L);
+    const uint64_t in_bytes = qbits ? N * (L * qbits / 8 + 8 * ((L + zg::kQBlock - 1) / zg::kQBlock)) : 2 * N * L;
+    if (spec) count(h, in_bytes + 12 * L, 12 * L + 2 * static_cast<uint64_t>(n_out) * L);
+    else count(h, in_bytes, 4 * L);
     return ZERO_OK;
 }
+
+bool aligned8(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 7u) == 0; }
 
 }  // namespace
 
@@ -488,6 +505,89 @@ int zero_reduce_scatter_bucket_replicas(zero_handle_t h, uint64_t a0, uint64_t b
     if (!h) return fail(nullptr, ZERO_EINVAL, "handle is NULL");
     if (h->stage != 2) return fail(h, ZERO_EINVAL, "zero_reduce_scatter_bucket_replicas is for stage 2");
     return rs_bucket(h, a0, b0, grads, master, m, v, params, hyper, stream);
+}
+
+int zero_quantize_blocks(int dtype, int bits, const void* src16, uint64_t count, void* codes, float* scales,
+                         void* stream) {
+    if (dtype != ZERO_FP16 && dtype != ZERO_BF16) return fail(nullptr, ZERO_EINVAL, "dtype must be fp16 or bf16");
+    if (bits != 8 && bits != 4) return fail(nullptr, ZERO_EINVAL, "bits must be 8 or 4");
+    if (count == 0) return ZERO_OK;
+    if (!src16 || !aligned16(src16)) return fail(nullptr, ZERO_EINVAL, "src16 is NULL or not 16-byte aligned");
+    if (!codes || !aligned16(codes)) return fail(nullptr, ZERO_EINVAL, "codes is NULL or not 16-byte aligned");
+    if (!scales || !aligned8(scales)) return fail(nullptr, ZERO_EINVAL, "scales is NULL or not 8-byte aligned");
+    zg::Args a;
+    std::memset(&a, 0, sizeof(a));
+    a.grads[0] = src16;
+    a.params[0] = codes;
+    a.qdst[0] = scales;
+    a.count = count;
+    a.qbits = bits;
+    a.qvec = 1;
+    const cudaError_t e = zg::launch_q(zg::QKind::kQuantize, dtype, bits, zg::Vec::k1, a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(nullptr, e, "quantize");
+    return ZERO_OK;
+}
+
+int zero_dequantize_blocks(int dtype, int bits, const void* codes, const float* scales, uint64_t count, void* out16,
+                           void* stream) {
+    if (dtype != ZERO_FP16 && dtype != ZERO_BF16) return fail(nullptr, ZERO_EINVAL, "dtype must be fp16 or bf16");
+    if (bits != 8 && bits != 4) return fail(nullptr, ZERO_EINVAL, "bits must be 8 or 4");
+    if (count == 0) return ZERO_OK;
+    if (!codes || !aligned16(codes)) return fail(nullptr, ZERO_EINVAL, "codes is NULL or not 16-byte aligned");
+    if (!scales || !aligned8(scales)) return fail(nullptr, ZERO_EINVAL, "scales is NULL or not 8-byte aligned");
+    if (!out16 || !aligned16(out16)) return fail(nullptr, ZERO_EINVAL, "out16 is NULL or not 16-byte aligned");
+    zg::Args a;
+    std::memset(&a, 0, sizeof(a));
+    a.grads[0] = codes;
+    a.qsrc[0] = scales;
+    a.params[0] = out16;
+    a.count = count;
+    a.qbits = bits;
+    const cudaError_t e = zg::launch_q(zg::QKind::kDequantize, dtype, bits, zg::Vec::k1, a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(nullptr, e, "dequantize");
+    return ZERO_OK;
+}
+
+int zero_gather_bucket_q8(zero_handle_t h, uint64_t a0, uint64_t b0, const void* shard16, void* const* codes_out,
+                          float* const* scales_out, void* stream) {
+    if (!h) return fail(nullptr, ZERO_EINVAL, "handle is NULL");
+    if (h->stage != 3) return fail(h, ZERO_EINVAL, "zero_gather_bucket_q8 is for stage 3");
+    if (a0 > b0 || b0 > h->psi_pad) return fail(h, ZERO_EINVAL, "bucket must satisfy 0 <= a <= b <= psi_pad");
+    const uint64_t L = b0 - a0, N = static_cast<uint64_t>(h->n);
+    if (L == 0) {
+        count(h, 0, 0);
+        return ZERO_OK;
+    }
+    int rc = check_ptr(h, shard16, "shard16");
+    if (rc) return rc;
+    if (!codes_out || !scales_out) return fail(h, ZERO_EINVAL, "codes_out / scales_out is NULL");
+    zg::Args a = base_args(h, nullptr);
+    a.grads[0] = shard16;
+    for (int r = 0; r < h->n; ++r) {
+        if ((rc = check_ptr(h, codes_out[r], "codes_out[r]"))) return rc;
+        if (!scales_out[r] || !aligned8(scales_out[r])) return fail(h, ZERO_EINVAL, "scales_out[r] is NULL or not 8-byte aligned");
+        a.params[r] = codes_out[r];
+        a.qdst[r] = scales_out[r];
+    }
+    a.base = a0;
+    a.count = L;
+    a.qbits = 8;
+    a.qvec = (a0 % 8) == 0 ? 1 : 0;
+    const cudaError_t e = zg::launch_q(zg::QKind::kGatherQ8, h->dtype, 8, zg::Vec::k1, a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(h, e, "quantized gather");
+    const uint64_t nb = (L + zg::kQBlock - 1) / zg::kQBlock;
+    count(h, 2 * L, N * (L + 8 * nb));
+    return ZERO_OK;
+}
+
+int zero_reduce_scatter_bucket_q(zero_handle_t h, uint64_t a0, uint64_t b0, int bits, const void* const* codes,
+                                 const float* const* scales, float* master, float* m, float* v, void* shard16,
+                                 const zero_hyper_t* hyper, void* stream) {
+    if (!h) return fail(nullptr, ZERO_EINVAL, "handle is NULL");
+    if (h->stage != 3) return fail(h, ZERO_EINVAL, "zero_reduce_scatter_bucket_q is for stage 3");
+    if (bits != 8 && bits != 4) return fail(h, ZERO_EINVAL, "bits must be 8 or 4");
+    void* outs[1] = {shard16};
+    return rs_bucket(h, a0, b0, codes, master, m, v, outs, hyper, stream, bits, scales);
 }
 
 int zero_get_status(zero_handle_t h, void* stream, zero_result_t* out) {

@@ -72,7 +72,12 @@ struct Args {
     HyperDev hyper;
     Workspace ws;
     int bucket_index;
-    int use_div;         // 1: N*scale is not a power of two -> IEEE divide
+    int use_div;         // unused: the kernels decide divide vs multiply on the device
+    // ZeRO++ block-quantized exchange (zero_quant.cu)
+    const float* qsrc[kMaxRanks];  // per-rank {scale, lo} pairs of quantized inputs
+    float* qdst[kMaxRanks];        // per-rank {scale, lo} pairs of quantized outputs
+    int qbits;                     // 8 or 4
+    int qvec;                      // 1: 16-bit source 16-byte aligned at every block start
 };
 
 enum class Kind : int {
@@ -100,6 +105,19 @@ enum class Vec : int { k8s32, k8s16, k1 };
 cudaError_t launch(Kind kind, int dtype, Vec vec, const Args& a, cudaStream_t s, int* grid_out);
 cudaError_t launch_finalize3(bool spec, const Args& a, cudaStream_t s);
 cudaError_t launch_set_scaler(DevStatus* st, float loss_scale, int64_t t, int32_t slot, cudaStream_t s);
+
+constexpr int kQBlock = 256;   // ZeRO++ quantization block (elements)
+
+enum class QKind : int {
+    kQuantize,     // one 16-bit buffer -> codes + {scale, lo}
+    kDequantize,   // codes + {scale, lo} -> one 16-bit buffer
+    kGatherQ8,     // ZeRO-3 gather: shard bucket -> N copies of int8 codes + scales
+    kRsQSpec,      // ZeRO-3 reduce-scatter of N quantized gradients + fused speculative AdamW
+    kRsQWs,        // ZeRO-3 reduce-scatter of N quantized gradients into the workspace
+};
+
+// Launcher of the ZeRO++ kernels (zero_quant.cu).
+cudaError_t launch_q(QKind kind, int dtype, int bits, Vec vec, const Args& a, cudaStream_t s);
 
 // Message returned by zero_last_error(NULL) for calls that take no handle.
 void set_global_error(const char* msg);

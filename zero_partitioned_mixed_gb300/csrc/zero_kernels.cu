@@ -23,316 +23,10 @@
 // the flattened gradient-norm buffer; "CMU 11-868 L18" ZeRO-1/2/3 call
 // sequences; "zero-stages-simulation" README partition and schedule.
 
-#include <cuda_bf16.h>
-#include <cuda_fp16.h>
-
-#include "zero_internal.h"
+#include "zero_device.cuh"
 
 namespace zg {
 namespace {
-
-// ------------------------------------------------------------------ 16-bit
-template <int DT>
-__device__ __forceinline__ float widen(uint32_t bits16);
-template <>
-__device__ __forceinline__ float widen<kFp16>(uint32_t b) {
-    return __half2float(__ushort_as_half(static_cast<unsigned short>(b)));
-}
-template <>
-__device__ __forceinline__ float widen<kBf16>(uint32_t b) {
-    return __uint_as_float(b << 16);
-}
-
-template <int DT>
-__device__ __forceinline__ uint32_t narrow(float x);
-template <>
-__device__ __forceinline__ uint32_t narrow<kFp16>(float x) {
-    return __half_as_ushort(__float2half_rn(x));
-}
-template <>
-__device__ __forceinline__ uint32_t narrow<kBf16>(float x) {
-    return __bfloat16_as_ushort(__float2bfloat16_rn(x));
-}
-
-// Vector I/O policies.  An IO type moves IO::W consecutive elements per
-// thread: 16-bit values (gradients, replicas) and fp32 values (master, m,
-// v, g_hat).
-//   Io8s32: 8 elements; 16-bit as one 128-bit access, fp32 as one 256-bit
-//           access (ld/st.global.v8.f32, sm_100 and later; 32-byte aligned);
-//   Io8s16: 8 elements; fp32 as two 128-bit accesses (16-byte aligned);
-//   Io1:    one element (any size, any offset).
-// All accesses carry the streaming hint (.cs): nothing is re-read within a step.
-struct Io8s16 {
-    static constexpr int W = 8;
-    __device__ static __forceinline__ void ld16(const void* p, uint64_t i, uint32_t (&out)[8]) {
-        const uint4 x = __ldcs(reinterpret_cast<const uint4*>(p) + (i >> 3));
-        out[0] = x.x & 0xFFFFu; out[1] = x.x >> 16;
-        out[2] = x.y & 0xFFFFu; out[3] = x.y >> 16;
-        out[4] = x.z & 0xFFFFu; out[5] = x.z >> 16;
-        out[6] = x.w & 0xFFFFu; out[7] = x.w >> 16;
-    }
-    __device__ static __forceinline__ void st16(void* p, uint64_t i, const uint32_t (&q)[8]) {
-        uint4 x;
-        x.x = q[0] | (q[1] << 16); x.y = q[2] | (q[3] << 16);
-        x.z = q[4] | (q[5] << 16); x.w = q[6] | (q[7] << 16);
-        __stcs(reinterpret_cast<uint4*>(p) + (i >> 3), x);
-    }
-    __device__ static __forceinline__ void ldf(const float* p, uint64_t i, float (&out)[8]) {
-        const float4 a = __ldcs(reinterpret_cast<const float4*>(p + i));
-        const float4 b = __ldcs(reinterpret_cast<const float4*>(p + i) + 1);
-        out[0] = a.x; out[1] = a.y; out[2] = a.z; out[3] = a.w;
-        out[4] = b.x; out[5] = b.y; out[6] = b.z; out[7] = b.w;
-    }
-    __device__ static __forceinline__ void stf(float* p, uint64_t i, const float (&x)[8]) {
-        __stcs(reinterpret_cast<float4*>(p + i), make_float4(x[0], x[1], x[2], x[3]));
-        __stcs(reinterpret_cast<float4*>(p + i) + 1, make_float4(x[4], x[5], x[6], x[7]));
-    }
-};
-
-struct Io8s32 : Io8s16 {
-    // one 256-bit access per thread: a warp covers 1 KiB contiguous in one instruction
-    __device__ static __forceinline__ void ldf(const float* p, uint64_t i, float (&o)[8]) {
-        asm("ld.global.cs.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-            : "=f"(o[0]), "=f"(o[1]), "=f"(o[2]), "=f"(o[3]), "=f"(o[4]), "=f"(o[5]), "=f"(o[6]), "=f"(o[7])
-            : "l"(p + i));
-    }
-    __device__ static __forceinline__ void stf(float* p, uint64_t i, const float (&x)[8]) {
-        asm volatile("st.global.cs.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
-                     :: "l"(p + i), "f"(x[0]), "f"(x[1]), "f"(x[2]), "f"(x[3]), "f"(x[4]), "f"(x[5]),
-                        "f"(x[6]), "f"(x[7])
-                     : "memory");
-    }
-};
-
-struct Io1 {
-    static constexpr int W = 1;
-    __device__ static __forceinline__ void ld16(const void* p, uint64_t i, uint32_t (&out)[1]) {
-        out[0] = __ldcs(reinterpret_cast<const unsigned short*>(p) + i);
-    }
-    __device__ static __forceinline__ void st16(void* p, uint64_t i, const uint32_t (&q)[1]) {
-        __stcs(reinterpret_cast<unsigned short*>(p) + i, static_cast<unsigned short>(q[0]));
-    }
-    __device__ static __forceinline__ void ldf(const float* p, uint64_t i, float (&out)[1]) {
-        out[0] = __ldcs(p + i);
-    }
-    __device__ static __forceinline__ void stf(float* p, uint64_t i, const float (&x)[1]) {
-        __stcs(p + i, x[0]);
-    }
-};
-
-// ------------------------------------------------------------------ scalars
-// Adam coefficients of step t, formed in double and rounded once to fp32.
-__device__ StepScalars make_scalars(const HyperDev& h, int64_t t) {
-    const double lr = h.lr, b1 = h.beta1, b2 = h.beta2, wd = h.weight_decay;
-    const double bc1 = __dsub_rn(1.0, pow(b1, static_cast<double>(t)));
-    const double bc2 = __dsub_rn(1.0, pow(b2, static_cast<double>(t)));
-    StepScalars s;
-    s.b1 = h.beta1;
-    s.b2 = h.beta2;
-    s.a1 = __double2float_rn(__dsub_rn(1.0, b1));
-    s.a2 = __double2float_rn(__dsub_rn(1.0, b2));
-    s.eps = h.eps;
-    s.dfac = __double2float_rn(__dsub_rn(1.0, __dmul_rn(lr, wd)));
-    s.step_size = __double2float_rn(__ddiv_rn(lr, bc1));
-    s.bc2s = __double2float_rn(__dsqrt_rn(bc2));
-    return s;
-}
-
-// One AdamW update, each operation rounded once, in the oracle's order.
-__device__ __forceinline__ void adam1(float g, float& p, float& m, float& v, const StepScalars& c) {
-    p = __fmul_rn(p, c.dfac);
-    m = __fadd_rn(__fmul_rn(c.b1, m), __fmul_rn(c.a1, g));
-    v = __fadd_rn(__fmul_rn(c.b2, v), __fmul_rn(c.a2, __fmul_rn(g, g)));
-    const float den = __fadd_rn(__fdiv_rn(__fsqrt_rn(v), c.bc2s), c.eps);
-    p = __fsub_rn(p, __fmul_rn(c.step_size, __fdiv_rn(m, den)));
-}
-
-__device__ __forceinline__ bool nonfinite(float x) {
-    return (__float_as_uint(x) & 0x7F800000u) == 0x7F800000u;
-}
-
-// Per-block view of the device status, read once by thread 0.
-struct Pro {
-    StepScalars sc;
-    float den, inv, clip_f;
-    int use_div, live, use_clip, overflow;
-};
-
-// Prologue of kernels that reduce gradients: unscale denominator N*scale
-// (fp32 product, as the oracle forms it) and, for the one-pass kernels,
-// the Adam coefficients of step t+1.
-__device__ __forceinline__ void prologue_reduce(const Args& a, Pro& pro, bool with_scalars) {
-    if (threadIdx.x == 0) {
-        const DevStatus* st = a.ws.status;
-        const float den = __fmul_rn(static_cast<float>(a.n_ranks), st->loss_scale);
-        const uint32_t bits = __float_as_uint(den);
-        const uint32_t ex = (bits >> 23) & 0xFFu;
-        // a power of two whose reciprocal is a normal number: s*inv == s/den exactly
-        const bool pow2 = (bits & 0x7FFFFFu) == 0u && ex >= 1u && ex <= 253u;
-        pro.den = den;
-        pro.use_div = pow2 ? 0 : 1;
-        pro.inv = pow2 ? __fdiv_rn(1.0f, den) : 0.0f;
-        pro.live = st->live_slot;
-        pro.clip_f = st->clip_f;
-        pro.use_clip = st->use_clip;
-        pro.overflow = st->overflow;
-        if (with_scalars) pro.sc = make_scalars(a.hyper, st->t + 1);
-        else pro.sc = st->sc;
-    }
-    __syncthreads();
-}
-
-// Sum of the N ranks' values of W elements at local index j, then unscale.
-template <int DT, class IO>
-__device__ __forceinline__ void reduce_group(const Args& a, uint64_t j, const Pro& pro, float (&g)[IO::W]) {
-    constexpr int W = IO::W;
-    float s[W];
-#pragma unroll
-    for (int k = 0; k < W; ++k) s[k] = 0.0f;
-    const int n = a.n_ranks;
-    int r = 0;
-    for (; r + 8 <= n; r += 8) {
-        uint32_t raw[8][W];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) IO::ld16(a.grads[r + q], j, raw[q]);
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-#pragma unroll
-            for (int k = 0; k < W; ++k) s[k] = __fadd_rn(s[k], widen<DT>(raw[q][k]));
-    }
-    for (; r < n; ++r) {
-        uint32_t raw[W];
-        IO::ld16(a.grads[r], j, raw);
-#pragma unroll
-        for (int k = 0; k < W; ++k) s[k] = __fadd_rn(s[k], widen<DT>(raw[k]));
-    }
-#pragma unroll
-    for (int k = 0; k < W; ++k) g[k] = pro.use_div ? __fdiv_rn(s[k], pro.den) : __fmul_rn(s[k], pro.inv);
-}
-
-// Squares of the real elements into the thread's fp64 accumulator: an
-// exact product (FMA error term) and a compensated fp32 sum per group, then
-// one fp64 add, so the result carries ~1e-14 relative error.
-template <int W>
-__device__ __forceinline__ void norm_group(const float (&g)[W], int valid, double& acc, int& bad) {
-    float hi = 0.0f, lo = 0.0f;
-#pragma unroll
-    for (int k = 0; k < W; ++k) {
-        if (k < valid) {
-            const float x = g[k];
-            bad |= nonfinite(x) ? 1 : 0;
-            const float p = __fmul_rn(x, x);
-            const float e = __fmaf_rn(x, x, -p);
-            const float s = __fadd_rn(hi, p);
-            const float bp = __fsub_rn(s, hi);
-            const float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bp)), __fsub_rn(p, bp));
-            hi = s;
-            lo = __fadd_rn(lo, __fadd_rn(err, e));
-        }
-    }
-    acc = __dadd_rn(acc, __dadd_rn(static_cast<double>(hi), static_cast<double>(lo)));
-}
-
-__device__ __forceinline__ int valid_count(uint64_t gi, int W, uint64_t psi) {
-    if (gi + W <= psi) return W;
-    if (gi >= psi) return 0;
-    return static_cast<int>(psi - gi);
-}
-
-// Deterministic block sum (fixed shuffle tree, then warp sums in order).
-__device__ double block_sum(double x) {
-    __shared__ double sm[kThreads / 32];
-    __syncthreads();
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) x = __dadd_rn(x, __shfl_down_sync(0xFFFFFFFFu, x, off));
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if (lane == 0) sm[warp] = x;
-    __syncthreads();
-    double t = 0.0;
-    if (threadIdx.x == 0) {
-        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t = __dadd_rn(t, sm[w]);
-    }
-    return t;  // valid in thread 0
-}
-
-// Publish the block's partial; true in every thread of the last block.
-__device__ bool publish(const Args& a, double blk, int flag, double* slot_norm, int32_t* slot_flag) {
-    __shared__ int s_last;
-    if (threadIdx.x == 0) {
-        slot_norm[blockIdx.x] = blk;
-        slot_flag[blockIdx.x] = flag;
-        __threadfence();
-        const unsigned prev = atomicAdd(&a.ws.status->ticket, 1u);
-        s_last = (prev == gridDim.x - 1) ? 1 : 0;
-    }
-    __syncthreads();
-    return s_last != 0;
-}
-
-// In the last block: fixed-order sum of all blocks' partials.
-__device__ void gather_partials(const double* slot_norm, const int32_t* slot_flag, int count,
-                                double& q, int& flag) {
-    __threadfence();
-    double s = 0.0;
-    int f = 0;
-    for (int b = threadIdx.x; b < count; b += blockDim.x) {
-        s = __dadd_rn(s, *reinterpret_cast<const volatile double*>(slot_norm + b));
-        f |= *reinterpret_cast<const volatile int32_t*>(slot_flag + b);
-    }
-    q = block_sum(s);
-    flag = __syncthreads_or(f);
-}
-
-// Overflow: skip.  The scale halves (floor 1.0); t and the state stay.
-__device__ void status_skip(DevStatus* st, double q) {
-    st->overflow = 1;
-    st->applied = 0;
-    st->norm = __dsqrt_rn(q);
-    st->clip_coef = 1.0;
-    st->clip_f = 1.0f;
-    st->use_clip = 0;
-    st->loss_scale = fmaxf(__fmul_rn(st->loss_scale, 0.5f), 1.0f);
-    st->skipped += 1;
-}
-
-// Speculative pass done without overflow: the shadow slot becomes live.
-__device__ void status_commit_spec(DevStatus* st, double q) {
-    st->overflow = 0;
-    st->applied = 1;
-    st->norm = __dsqrt_rn(q);
-    st->clip_coef = 1.0;
-    st->clip_f = 1.0f;
-    st->use_clip = 0;
-    st->live_slot ^= 1;
-    st->t += 1;
-}
-
-// Two-pass decision before the apply pass: clip factor and step t+1 scalars.
-__device__ void status_decide_two_pass(DevStatus* st, double q, const HyperDev& h) {
-    const double norm = __dsqrt_rn(q);
-    st->overflow = 0;
-    st->applied = 1;
-    st->norm = norm;
-    st->use_clip = 0;
-    st->clip_f = 1.0f;
-    if (h.max_norm > 0.0f) {
-        const double c = __ddiv_rn(static_cast<double>(h.max_norm), __dadd_rn(norm, 1e-6));
-        if (c < 1.0) {
-            st->use_clip = 1;
-            st->clip_f = __double2float_rn(c);
-        }
-    }
-    st->clip_coef = static_cast<double>(st->clip_f);
-    st->t += 1;
-    st->sc = make_scalars(h, st->t);
-}
-
-__device__ __forceinline__ uint64_t grid_threads() {
-    return static_cast<uint64_t>(gridDim.x) * blockDim.x;
-}
-__device__ __forceinline__ uint64_t thread_id() {
-    return static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-}
 
 // ------------------------------------------------------------------ kernels
 // Stages 1/2, one pass: reduce-scatter + unscale + flag + norm partial +
@@ -648,30 +342,6 @@ __global__ void k_set_scaler(DevStatus* st, float loss_scale, int64_t t, int32_t
 }
 
 // ------------------------------------------------------------------ launch
-template <typename KernelT>
-cudaError_t run(KernelT kernel, const Args& a, uint64_t nvec, cudaStream_t s, int* grid_out) {
-    static int sms = 0;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (sms == 0) {
-        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
-    }
-    int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0);
-    if (e != cudaSuccess) return e;
-    if (per_sm < 1) per_sm = 1;
-    uint64_t want = (nvec + kThreads - 1) / kThreads;
-    uint64_t cap = static_cast<uint64_t>(sms) * static_cast<uint64_t>(per_sm);
-    if (cap > static_cast<uint64_t>(kMaxBlocks)) cap = kMaxBlocks;
-    uint64_t grid = want < cap ? want : cap;
-    if (grid < 1) grid = 1;
-    if (grid_out) *grid_out = static_cast<int>(grid);
-    kernel<<<static_cast<unsigned>(grid), kThreads, 0, s>>>(a);
-    return cudaGetLastError();
-}
-
 template <int DT, class IO>
 cudaError_t launch_dw(Kind kind, const Args& a, cudaStream_t s, int* grid_out) {
     const uint64_t nvec = a.count / IO::W;

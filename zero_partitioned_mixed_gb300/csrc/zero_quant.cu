@@ -1,0 +1,420 @@
+// ZeRO++ block-quantized exchanges for sm_103a.
+//
+// "CMU 11-868 L18" notes, other memory optimizations (ZeRO++): parameters
+// are block-quantized from 16 bits to INT8 with zero-point quantization for
+// the forward gather (qwZ), and the backward reduce-scatter is quantized to
+// INT8 or INT4 (qgZ).  Format (the same as the CPU oracle's): blocks of 256
+// elements from the start of the buffer or bucket; per block lo = min,
+// hi = max (NaN propagates), scale = (hi - lo) / (2^bits - 1) and
+// inv = (2^bits - 1) / (hi - lo), code = rint((x - lo) * inv) clamped to
+// [0, 2^bits - 1] (0 when scale is 0, 0 for a NaN); dequantized
+// x' = lo + code * scale.
+//
+// Two exact bit-level shortcuts keep the per-element cost to a few adds:
+// for 0 <= u < 2^22, u + 2^23 (rounded to nearest even) holds rint(u) in its
+// low mantissa bits; and the float with bits 0x4B000000 | q, minus 2^23, is
+// exactly q for any q < 2^23.  Neither changes a result.  Codes: one byte each (INT8), or two
+// per byte (INT4, even element in the low nibble).  Scales: {scale, lo}
+// float pairs, one per block.
+//
+// One warp owns one 256-element block at a time (8 elements per lane), two
+// blocks per iteration so that their loads are in flight together: the
+// block's min and max are one warp reduction each (redux.sync); codes leave as 8-byte (INT8) or
+// 4-byte (INT4) stores per lane.  All kernels are HBM streams.
+
+#include "zero_device.cuh"
+
+namespace zg {
+namespace {
+
+// min/max that return NaN when either input is NaN (one instruction each),
+// and their warp-wide forms.
+__device__ __forceinline__ float qmin(float a, float b) {
+    float d;
+    asm("min.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+    return d;
+}
+__device__ __forceinline__ float qmax(float a, float b) {
+    float d;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+    return d;
+}
+__device__ __forceinline__ float warp_qmin(float a) {
+    float d;
+    asm volatile("redux.sync.min.NaN.f32 %0, %1, 0xffffffff;" : "=f"(d) : "f"(a));
+    return d;
+}
+__device__ __forceinline__ float warp_qmax(float a) {
+    float d;
+    asm volatile("redux.sync.max.NaN.f32 %0, %1, 0xffffffff;" : "=f"(d) : "f"(a));
+    return d;
+}
+
+constexpr float kTwo23 = 8388608.0f;
+
+// rint(clamp(u, 0, top)) as an integer; a NaN u gives 0 (fmaxf returns the
+// other operand).
+__device__ __forceinline__ uint32_t code_of(float x, float lo, float inv, float top) {
+    const float u = fminf(fmaxf(__fmul_rn(__fsub_rn(x, lo), inv), 0.0f), top);
+    return __float_as_uint(__fadd_rn(u, kTwo23)) & 0x1FFu;
+}
+
+// float(q) for q < 2^23, exactly.
+__device__ __forceinline__ float as_float(uint32_t q) {
+    return __fsub_rn(__uint_as_float(0x4B000000u | q), kTwo23);
+}
+
+__device__ __forceinline__ float dequant(uint32_t q, float scale, float lo) {
+    return __fadd_rn(lo, __fmul_rn(as_float(q), scale));
+}
+
+// Lane's 8 values of a block of a 16-bit buffer (elements >= count are absent).
+template <int DT>
+__device__ __forceinline__ int load_lane8(const void* src, uint64_t e0, uint64_t count, bool vec, float (&x)[8]) {
+    const int nv = e0 >= count ? 0 : static_cast<int>(count - e0 < 8 ? count - e0 : 8);
+    if (vec && nv == 8) {
+        uint32_t raw[8];
+        Io8s16::ld16(src, e0, raw);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) x[k] = widen<DT>(raw[k]);
+    } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            x[k] = 0.0f;
+            if (k < nv) x[k] = widen<DT>(reinterpret_cast<const unsigned short*>(src)[e0 + k]);
+        }
+    }
+    return nv;
+}
+
+// Block min/max over the warp; every lane gets {scale, inv, lo}.
+template <int BITS>
+__device__ __forceinline__ void block_scale(const float (&x)[8], int nv, float& scale, float& inv, float& lo) {
+    float mn = __int_as_float(0x7F800000), mx = -__int_as_float(0x7F800000);
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        if (k < nv) {
+            mn = qmin(mn, x[k]);
+            mx = qmax(mx, x[k]);
+        }
+    // warp-wide, then +0.0 makes a zero bound +0 whatever the order of ties
+    mn = __fadd_rn(warp_qmin(mn), 0.0f);
+    mx = __fadd_rn(warp_qmax(mx), 0.0f);
+    lo = mn;
+    const float range = __fsub_rn(mx, mn);
+    const float top = static_cast<float>((1 << BITS) - 1);
+    scale = __fdiv_rn(range, top);
+    inv = __fdiv_rn(top, range);
+}
+
+// Store a lane's 8 codes at element e0 of a code buffer.
+template <int BITS>
+__device__ __forceinline__ void store_codes(void* codes, uint64_t e0, int nv, const uint32_t (&q)[8]) {
+    if (BITS == 8) {
+        unsigned char* c = static_cast<unsigned char*>(codes) + e0;
+        if (nv == 8) {
+            uint2 w;
+            w.x = q[0] | (q[1] << 8) | (q[2] << 16) | (q[3] << 24);
+            w.y = q[4] | (q[5] << 8) | (q[6] << 16) | (q[7] << 24);
+            __stcs(reinterpret_cast<uint2*>(c), w);
+        } else {
+            for (int k = 0; k < nv; ++k) c[k] = static_cast<unsigned char>(q[k]);
+        }
+    } else {
+        unsigned char* c = static_cast<unsigned char*>(codes) + (e0 >> 1);
+        if (nv == 8) {
+            const uint32_t w = q[0] | (q[1] << 4) | (q[2] << 8) | (q[3] << 12) | (q[4] << 16) | (q[5] << 20) |
+                               (q[6] << 24) | (q[7] << 28);
+            __stcs(reinterpret_cast<unsigned int*>(c), w);
+        } else {
+            for (int k = 0; k < nv; k += 2) {
+                const uint32_t hi = (k + 1 < nv) ? q[k + 1] : 0u;
+                c[k >> 1] = static_cast<unsigned char>(q[k] | (hi << 4));
+            }
+        }
+    }
+}
+
+// A lane's 8 codes at element e0 (e0 % 8 == 0).
+template <int BITS>
+__device__ __forceinline__ void load_codes8(const void* codes, uint64_t e0, uint32_t (&q)[8]) {
+    if (BITS == 8) {
+        const uint2 w = __ldcs(reinterpret_cast<const uint2*>(static_cast<const unsigned char*>(codes) + e0));
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            q[k] = (w.x >> (8 * k)) & 0xFFu;
+            q[4 + k] = (w.y >> (8 * k)) & 0xFFu;
+        }
+    } else {
+        const uint32_t w = __ldcs(reinterpret_cast<const unsigned int*>(static_cast<const unsigned char*>(codes) + (e0 >> 1)));
+#pragma unroll
+        for (int k = 0; k < 8; ++k) q[k] = (w >> (4 * k)) & 0xFu;
+    }
+}
+
+// A lane's 8 codes at element e0 (e0 % 8 == 0) as exact floats: the byte
+// (or nibble) is placed under the exponent of 2^23 and 2^23 subtracted.
+template <int BITS>
+__device__ __forceinline__ void load_codes8_f(const void* codes, uint64_t e0, float (&f)[8]) {
+    if (BITS == 8) {
+        const uint2 w = __ldcs(reinterpret_cast<const uint2*>(static_cast<const unsigned char*>(codes) + e0));
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            f[k] = __fsub_rn(__uint_as_float(__byte_perm(w.x, 0x4B000000u, 0x7540u | k)), kTwo23);
+            f[4 + k] = __fsub_rn(__uint_as_float(__byte_perm(w.y, 0x4B000000u, 0x7540u | k)), kTwo23);
+        }
+    } else {
+        const uint32_t w = __ldcs(reinterpret_cast<const unsigned int*>(static_cast<const unsigned char*>(codes) + (e0 >> 1)));
+#pragma unroll
+        for (int k = 0; k < 8; ++k) f[k] = __fsub_rn(__uint_as_float(((w >> (4 * k)) & 0xFu) | 0x4B000000u), kTwo23);
+    }
+}
+
+template <int BITS>
+__device__ __forceinline__ uint32_t load_code1(const void* codes, uint64_t e) {
+    if (BITS == 8) return static_cast<const unsigned char*>(codes)[e];
+    const uint32_t b = static_cast<const unsigned char*>(codes)[e >> 1];
+    return (e & 1) ? (b >> 4) : (b & 0xFu);
+}
+
+__device__ __forceinline__ uint64_t warp_id() { return (static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; }
+__device__ __forceinline__ uint64_t warp_count() { return (static_cast<uint64_t>(gridDim.x) * blockDim.x) >> 5; }
+
+// ------------------------------------------------------------------ kernels
+constexpr int kQUnroll = 2;   // blocks per warp iteration: their loads are all in flight together
+
+// Quantize kQUnroll consecutive blocks starting at block blk0 of src (count
+// elements) and hand each block's codes and {scale, lo} to `emit`.
+template <int DT, int BITS, class Emit>
+__device__ __forceinline__ void quantize_blocks_u(const unsigned short* src, uint64_t count, uint64_t blk0,
+                                                  uint64_t nb, bool vec, int lane, Emit&& emit) {
+    const float top = static_cast<float>((1 << BITS) - 1);
+    float x[kQUnroll][8];
+    int nv[kQUnroll];
+#pragma unroll
+    for (int u = 0; u < kQUnroll; ++u) {
+        const uint64_t e0 = (blk0 + u) * kQBlock + static_cast<uint64_t>(lane) * 8;
+        nv[u] = (blk0 + u < nb) ? load_lane8<DT>(src, e0, count, vec, x[u]) : 0;
+    }
+#pragma unroll
+    for (int u = 0; u < kQUnroll; ++u) {
+        if (blk0 + u >= nb) break;
+        float scale, inv, lo;
+        block_scale<BITS>(x[u], nv[u], scale, inv, lo);
+        uint32_t q[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) q[k] = (k < nv[u] && scale != 0.0f) ? code_of(x[u][k], lo, inv, top) : 0u;
+        emit(blk0 + u, (blk0 + u) * kQBlock + static_cast<uint64_t>(lane) * 8, nv[u], q, scale, lo);
+    }
+}
+
+// One 16-bit buffer (grads[0] + base, count elements) -> codes (params[0])
+// and {scale, lo} pairs (qdst[0]).
+template <int DT, int BITS>
+__global__ void __launch_bounds__(kThreads) k_quantize(const __grid_constant__ Args a) {
+    const int lane = threadIdx.x & 31;
+    const uint64_t nb = (a.count + kQBlock - 1) / kQBlock;
+    const unsigned short* src = static_cast<const unsigned short*>(a.grads[0]) + a.base;
+    for (uint64_t blk0 = warp_id() * kQUnroll; blk0 < nb; blk0 += warp_count() * kQUnroll) {
+        quantize_blocks_u<DT, BITS>(src, a.count, blk0, nb, a.qvec != 0, lane,
+                                    [&](uint64_t blk, uint64_t e0, int nv, const uint32_t (&q)[8], float scale,
+                                        float lo) {
+                                        if (nv > 0) store_codes<BITS>(a.params[0], e0, nv, q);
+                                        if (lane == 0) {
+                                            a.qdst[0][2 * blk] = scale;
+                                            a.qdst[0][2 * blk + 1] = lo;
+                                        }
+                                    });
+    }
+}
+
+// ZeRO-3 quantized gather (qwZ): bucket [base, base+count) of the 16-bit
+// shard (grads[0]) -> for every rank r: codes (params[r]) and scales (qdst[r]).
+template <int DT>
+__global__ void __launch_bounds__(kThreads) k_gather_q8(const __grid_constant__ Args a) {
+    const int lane = threadIdx.x & 31;
+    const uint64_t nb = (a.count + kQBlock - 1) / kQBlock;
+    const unsigned short* src = static_cast<const unsigned short*>(a.grads[0]) + a.base;
+    for (uint64_t blk0 = warp_id() * kQUnroll; blk0 < nb; blk0 += warp_count() * kQUnroll) {
+        quantize_blocks_u<DT, 8>(src, a.count, blk0, nb, a.qvec != 0, lane,
+                                 [&](uint64_t blk, uint64_t e0, int nv, const uint32_t (&q)[8], float scale,
+                                     float lo) {
+                                     for (int r = 0; r < a.n_ranks; ++r) {
+                                         if (nv > 0) store_codes<8>(a.params[r], e0, nv, q);
+                                         if (lane == 0) {
+                                             a.qdst[r][2 * blk] = scale;
+                                             a.qdst[r][2 * blk + 1] = lo;
+                                         }
+                                     }
+                                 });
+    }
+}
+
+// codes (grads[0]) + scales (qsrc[0]) -> 16-bit buffer (params[0]), count elements.
+template <int DT, int BITS>
+__global__ void __launch_bounds__(kThreads) k_dequantize(const __grid_constant__ Args a) {
+    const uint64_t nv8 = (a.count + 7) / 8;
+    for (uint64_t t = thread_id(); t < nv8; t += grid_threads()) {
+        const uint64_t e0 = t * 8;
+        const uint64_t blk = e0 / kQBlock;
+        const float scale = a.qsrc[0][2 * blk], lo = a.qsrc[0][2 * blk + 1];
+        const int nv = static_cast<int>(a.count - e0 < 8 ? a.count - e0 : 8);
+        uint32_t out[8];
+        if (nv == 8) {
+            uint32_t q[8];
+            load_codes8<BITS>(a.grads[0], e0, q);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) out[k] = narrow<DT>(dequant(q[k], scale, lo));
+            Io8s16::st16(a.params[0], e0, out);
+        } else {
+            for (int k = 0; k < nv; ++k)
+                reinterpret_cast<unsigned short*>(a.params[0])[e0 + k] =
+                    static_cast<unsigned short>(narrow<DT>(dequant(load_code1<BITS>(a.grads[0], e0 + k), scale, lo)));
+        }
+    }
+}
+
+// Sum over ranks (order 0..N-1, from +0) of the dequantized gradients of W
+// elements at bucket-local index j, then unscale.  Ranks go in chunks of 8
+// whose code and scale loads are all issued before any arithmetic.
+template <int BITS, int W>
+__device__ __forceinline__ void reduce_group_q(const Args& a, uint64_t j, const Pro& pro, float (&g)[W]) {
+    float s[W];
+#pragma unroll
+    for (int k = 0; k < W; ++k) s[k] = 0.0f;
+    const uint64_t blk = j / kQBlock;
+    const int n = a.n_ranks;
+    int r = 0;
+    for (; r + 8 <= n; r += 8) {
+        float q[8][W];
+        float2 sl[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            sl[t] = *reinterpret_cast<const float2*>(a.qsrc[r + t] + 2 * blk);
+            if (W == 8) {
+                float tmp[8];
+                load_codes8_f<BITS>(a.grads[r + t], j, tmp);
+#pragma unroll
+                for (int k = 0; k < W; ++k) q[t][k] = tmp[k];
+            } else {
+#pragma unroll
+                for (int k = 0; k < W; ++k) q[t][k] = as_float(load_code1<BITS>(a.grads[r + t], j + k));
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < 8; ++t)
+#pragma unroll
+            for (int k = 0; k < W; ++k) s[k] = __fadd_rn(s[k], __fadd_rn(sl[t].y, __fmul_rn(q[t][k], sl[t].x)));
+    }
+    for (; r < n; ++r) {
+        const float2 sl = *reinterpret_cast<const float2*>(a.qsrc[r] + 2 * blk);
+        uint32_t q[W];
+        if (W == 8) {
+            uint32_t tmp[8];
+            load_codes8<BITS>(a.grads[r], j, tmp);
+#pragma unroll
+            for (int k = 0; k < W; ++k) q[k] = tmp[k];
+        } else {
+#pragma unroll
+            for (int k = 0; k < W; ++k) q[k] = load_code1<BITS>(a.grads[r], j + k);
+        }
+#pragma unroll
+        for (int k = 0; k < W; ++k) s[k] = __fadd_rn(s[k], dequant(q[k], sl.x, sl.y));
+    }
+#pragma unroll
+    for (int k = 0; k < W; ++k) g[k] = pro.use_div ? __fdiv_rn(s[k], pro.den) : __fmul_rn(s[k], pro.inv);
+}
+
+// ZeRO-3 reduce-scatter of bucket [base, base+count) from the N ranks'
+// quantized gradients (qgZ): as k_rs, with the ranks' values dequantized.
+template <int DT, class IO, int BITS, bool SPEC>
+__global__ void __launch_bounds__(kThreads) k_rs_q(const __grid_constant__ Args a) {
+    constexpr int W = IO::W;
+    __shared__ Pro pro;
+    prologue_reduce(a, pro, SPEC);
+    const uint64_t src = static_cast<uint64_t>(pro.live) * a.slot_stride;
+    const uint64_t dst = static_cast<uint64_t>(pro.live ^ 1) * a.slot_stride;
+    const uint64_t nvec = a.count / W;
+    double acc = 0.0;
+    int bad = 0;
+    for (uint64_t vi = thread_id(); vi < nvec; vi += grid_threads()) {
+        const uint64_t j = vi * W;
+        const uint64_t gi = a.base + j;
+        float g[W];
+        reduce_group_q<BITS, W>(a, j, pro, g);
+        const int valid = valid_count(gi, W, a.psi);
+        norm_group<W>(g, valid, acc, bad);
+        if (SPEC) {
+            float p[W], m[W], v[W];
+            IO::ldf(a.master + src, gi, p);
+            IO::ldf(a.m + src, gi, m);
+            IO::ldf(a.v + src, gi, v);
+            uint32_t q[W];
+#pragma unroll
+            for (int k = 0; k < W; ++k) {
+                if (k < valid) {
+                    adam1(g[k], p[k], m[k], v[k], pro.sc);
+                } else {
+                    p[k] = 0.0f; m[k] = 0.0f; v[k] = 0.0f;
+                }
+                q[k] = narrow<DT>(p[k]);
+            }
+            IO::stf(a.master + dst, gi, p);
+            IO::stf(a.m + dst, gi, m);
+            IO::stf(a.v + dst, gi, v);
+            IO::st16(a.params[0], gi, q);
+        } else {
+#pragma unroll
+            for (int k = 0; k < W; ++k)
+                if (k >= valid) g[k] = 0.0f;
+            IO::stf(a.ws.ghat, gi, g);
+        }
+    }
+    const double blk = block_sum(acc);
+    const int flag = __syncthreads_or(bad);
+    if (publish(a, blk, flag, a.ws.partials, a.ws.flags)) {
+        double qsum;
+        int f;
+        gather_partials(a.ws.partials, a.ws.flags, gridDim.x, qsum, f);
+        if (threadIdx.x == 0) {
+            a.ws.bucket_norm[a.bucket_index] = qsum;
+            a.ws.bucket_flag[a.bucket_index] = f;
+            a.ws.status->ticket = 0u;
+        }
+    }
+}
+
+template <int DT, int BITS>
+cudaError_t launch_db(QKind kind, Vec vec, const Args& a, cudaStream_t s) {
+    const uint64_t nb = (a.count + kQBlock - 1) / kQBlock;
+    switch (kind) {
+        case QKind::kQuantize: return run(k_quantize<DT, BITS>, a, (nb + kQUnroll - 1) / kQUnroll * 32, s, nullptr);
+        case QKind::kGatherQ8: return run(k_gather_q8<DT>, a, (nb + kQUnroll - 1) / kQUnroll * 32, s, nullptr);
+        case QKind::kDequantize: return run(k_dequantize<DT, BITS>, a, (a.count + 7) / 8, s, nullptr);
+        case QKind::kRsQSpec:
+        case QKind::kRsQWs: {
+            const bool spec = kind == QKind::kRsQSpec;
+            switch (vec) {
+                case Vec::k8s32:
+                    return spec ? run(k_rs_q<DT, Io8s32, BITS, true>, a, a.count / 8, s, nullptr)
+                                : run(k_rs_q<DT, Io8s32, BITS, false>, a, a.count / 8, s, nullptr);
+                case Vec::k8s16:
+                    return spec ? run(k_rs_q<DT, Io8s16, BITS, true>, a, a.count / 8, s, nullptr)
+                                : run(k_rs_q<DT, Io8s16, BITS, false>, a, a.count / 8, s, nullptr);
+                default:
+                    return spec ? run(k_rs_q<DT, Io1, BITS, true>, a, a.count, s, nullptr)
+                                : run(k_rs_q<DT, Io1, BITS, false>, a, a.count, s, nullptr);
+            }
+        }
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_q(QKind kind, int dtype, int bits, Vec vec, const Args& a, cudaStream_t s) {
+    if (dtype == kFp16) return bits == 8 ? launch_db<kFp16, 8>(kind, vec, a, s) : launch_db<kFp16, 4>(kind, vec, a, s);
+    return bits == 8 ? launch_db<kBf16, 8>(kind, vec, a, s) : launch_db<kBf16, 4>(kind, vec, a, s);
+}
+
+}  // namespace zg
