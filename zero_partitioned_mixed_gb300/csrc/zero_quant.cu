@@ -18,7 +18,7 @@
 // float pairs, one per block.
 //
 // One warp owns one 256-element block at a time (8 elements per lane), two
-// blocks per iteration so that their loads are in flight together: the
+// or four blocks per iteration so that their loads are in flight together: the
 // block's min and max are one warp reduction each (redux.sync); codes leave as 8-byte (INT8) or
 // 4-byte (INT4) stores per lane.  All kernels are HBM streams.
 
@@ -181,11 +181,15 @@ __device__ __forceinline__ uint64_t warp_id() { return (static_cast<uint64_t>(bl
 __device__ __forceinline__ uint64_t warp_count() { return (static_cast<uint64_t>(gridDim.x) * blockDim.x) >> 5; }
 
 // ------------------------------------------------------------------ kernels
-constexpr int kQUnroll = 2;   // blocks per warp iteration: their loads are all in flight together
+// Blocks per warp iteration (their loads are in flight together): two for
+// the gather, whose stores to N ranks dominate; four for the one-output
+// quantize, which is read-bound.
+constexpr int kQUnrollGather = 2;
+constexpr int kQUnrollQuant = 4;
 
-// Quantize kQUnroll consecutive blocks starting at block blk0 of src (count
+// Quantize U consecutive blocks starting at block blk0 of src (count
 // elements) and hand each block's codes and {scale, lo} to `emit`.
-template <int DT, int BITS, class Emit>
+template <int DT, int BITS, int kQUnroll, class Emit>
 __device__ __forceinline__ void quantize_blocks_u(const unsigned short* src, uint64_t count, uint64_t blk0,
                                                   uint64_t nb, bool vec, int lane, Emit&& emit) {
     const float top = static_cast<float>((1 << BITS) - 1);
@@ -215,8 +219,8 @@ __global__ void __launch_bounds__(kThreads) k_quantize(const __grid_constant__ A
     const int lane = threadIdx.x & 31;
     const uint64_t nb = (a.count + kQBlock - 1) / kQBlock;
     const unsigned short* src = static_cast<const unsigned short*>(a.grads[0]) + a.base;
-    for (uint64_t blk0 = warp_id() * kQUnroll; blk0 < nb; blk0 += warp_count() * kQUnroll) {
-        quantize_blocks_u<DT, BITS>(src, a.count, blk0, nb, a.qvec != 0, lane,
+    for (uint64_t blk0 = warp_id() * kQUnrollQuant; blk0 < nb; blk0 += warp_count() * kQUnrollQuant) {
+        quantize_blocks_u<DT, BITS, kQUnrollQuant>(src, a.count, blk0, nb, a.qvec != 0, lane,
                                     [&](uint64_t blk, uint64_t e0, int nv, const uint32_t (&q)[8], float scale,
                                         float lo) {
                                         if (nv > 0) store_codes<BITS>(a.params[0], e0, nv, q);
@@ -235,8 +239,8 @@ __global__ void __launch_bounds__(kThreads) k_gather_q8(const __grid_constant__ 
     const int lane = threadIdx.x & 31;
     const uint64_t nb = (a.count + kQBlock - 1) / kQBlock;
     const unsigned short* src = static_cast<const unsigned short*>(a.grads[0]) + a.base;
-    for (uint64_t blk0 = warp_id() * kQUnroll; blk0 < nb; blk0 += warp_count() * kQUnroll) {
-        quantize_blocks_u<DT, 8>(src, a.count, blk0, nb, a.qvec != 0, lane,
+    for (uint64_t blk0 = warp_id() * kQUnrollGather; blk0 < nb; blk0 += warp_count() * kQUnrollGather) {
+        quantize_blocks_u<DT, 8, kQUnrollGather>(src, a.count, blk0, nb, a.qvec != 0, lane,
                                  [&](uint64_t blk, uint64_t e0, int nv, const uint32_t (&q)[8], float scale,
                                      float lo) {
                                      for (int r = 0; r < a.n_ranks; ++r) {
@@ -388,8 +392,10 @@ template <int DT, int BITS>
 cudaError_t launch_db(QKind kind, Vec vec, const Args& a, cudaStream_t s) {
     const uint64_t nb = (a.count + kQBlock - 1) / kQBlock;
     switch (kind) {
-        case QKind::kQuantize: return run(k_quantize<DT, BITS>, a, (nb + kQUnroll - 1) / kQUnroll * 32, s, nullptr);
-        case QKind::kGatherQ8: return run(k_gather_q8<DT>, a, (nb + kQUnroll - 1) / kQUnroll * 32, s, nullptr);
+        case QKind::kQuantize:
+            return run(k_quantize<DT, BITS>, a, (nb + kQUnrollQuant - 1) / kQUnrollQuant * 32, s, nullptr);
+        case QKind::kGatherQ8:
+            return run(k_gather_q8<DT>, a, (nb + kQUnrollGather - 1) / kQUnrollGather * 32, s, nullptr);
         case QKind::kDequantize: return run(k_dequantize<DT, BITS>, a, (a.count + 7) / 8, s, nullptr);
         case QKind::kRsQSpec:
         case QKind::kRsQWs: {
