@@ -443,8 +443,7 @@ def _bytes_total(buf):
 def bench_dense(w, stage, steps, warmup, torch, S, Z, flush_l2=False, sets_max=5):
     """Stages 0-2: resident gradient sets, one zero_step per bench step."""
     from zero_partitioned_mixed_gb300.buffers import RankBuffers
-    db = stage != 0 and w.max_norm == 0
-    buf = RankBuffers(w.psi, w.n_ranks, stage, w.dtype, double_buffer=db, alloc_grads=False)
+    buf = RankBuffers(w.psi, w.n_ranks, stage, w.dtype, double_buffer=stage != 0, alloc_grads=False)
     P, N = buf.psi_pad, w.n_ranks
     td = S.torch_dtype(w.dtype)
     mv, mm, vv = buf.state(0)
@@ -711,7 +710,8 @@ def run_other(args, ws, rank, local):
         w = S.GPT2
         ms, bps, st = bench_dense(w, 2, args.steps, args.warmup, torch, S, Z)
         lines.append(_line(w.name, w.psi / (ms * 1e-3), ms, args.steps, args.warmup, bps, w.dtype,
-                           {"stage": 2, "mode": "two-pass (clip 1.0)", "l2": "inputs larger than L2"}))
+                           {"stage": 2, "mode": "speculative one pass; a step whose norm exceeds 1.0 is redone",
+                            "l2": "inputs larger than L2"}))
     elif args.workload == "llama7b":
         w = S.LLAMA7B
         buckets = S.layer_buckets(S.llama7b_shapes(), w.psi)

@@ -68,7 +68,8 @@ typedef enum {
     ZERO_MODE_AUTO = 0,            /* SPECULATIVE if possible, else TWO_PASS_WS for N > 4, else REREAD */
     ZERO_MODE_TWO_PASS_WS = 1,     /* pass 1 writes fp32 g_hat to workspace; pass 2 reads it */
     ZERO_MODE_TWO_PASS_REREAD = 2, /* pass 2 reduces the N gradient buffers again */
-    ZERO_MODE_SPECULATIVE = 3      /* one pass writing the shadow state slot; commit or roll back */
+    ZERO_MODE_SPECULATIVE = 3      /* one pass writing the shadow state slot; commit, roll back, or
+                                      (one-shot step whose norm needs clipping) redo from the old slot */
 } zero_mode_t;
 
 /* zero_init_partition flags */
@@ -159,6 +160,12 @@ ZERO_API int zero_set_scaler(zero_handle_t h, float loss_scale, int64_t steps_ap
  *   (two-pass modes) applies Adam and writes the 16-bit shard.
  * On overflow nothing of master/m/v/params changes, the scale halves and t
  * is not advanced.
+ * Speculative mode (ZERO_F_DOUBLE_BUFFER; AUTO picks it for stages 1/2):
+ * one pass updates the shadow slot and the replicas assuming no clipping.
+ * If the norm then calls for clipping, a second pass redoes the update
+ * from the untouched old slot with the clip factor, so only clipped steps
+ * pay for two passes.  Bucketed steps (stage 3, and stage 2 with NULL grads)
+ * cannot re-read their gradients and use the two-pass mode when clipping.
  *   grads   host array of N device pointers, psi_pad 16-bit elements each
  *           (stages 0-2); NULL for stage 3
  *   params  host array of N device pointers to psi_pad 16-bit replicas

@@ -95,11 +95,14 @@ def test_flat_1p5b_stage1_four_steps_with_overflow(pool):
     torch.cuda.empty_cache()
 
 
-def test_gpt2_small_stage2_clip_five_steps(pool):
+@pytest.mark.parametrize("double_buffer", [False, True])
+def test_gpt2_small_stage2_clip_five_steps(pool, double_buffer):
+    # two-pass (clip decided before the update) and speculative (redo only
+    # if the norm exceeds max_norm, which it does not here)
     w = S.GPT2
     hb, ho = _hyper(w)
     n, dt = w.n_ranks, w.dtype
-    buf = RankBuffers(w.psi, n, 2, dt, double_buffer=False, alloc_grads=False)
+    buf = RankBuffers(w.psi, n, 2, dt, double_buffer=double_buffer, alloc_grads=False)
     P = buf.psi_pad
     part = O.partition(w.psi, n, 8)
     mv, mm, vv = buf.state(0)
@@ -126,7 +129,7 @@ def test_gpt2_small_stage2_clip_five_steps(pool):
         assert st["clip_coef"] == (float(clip) if clip is not None else 1.0)
         p, m, v, bad = oracle_sampled_step(p, m, v, gs, n, dt, 1.0, ho, k + 1, clip, valid)
         assert not bad
-        _check_samples(buf, 0, idx_t, p, m, v, dt, n, 2)
+        _check_samples(buf, st["state_slot"], idx_t, p, m, v, dt, n, 2)
     buf.close()
     del grads, sv, buf
     torch.cuda.empty_cache()

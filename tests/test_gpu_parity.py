@@ -142,10 +142,6 @@ def test_errors_are_returned_not_raised_on_device():
     with pytest.raises(B.ZeroError) as e:
         B.zero_step(buf.h, [bad, buf.grads[1]], buf.param_rows(), buf.master, buf.m, buf.v, B.hyper())
     assert e.value.code == 1 and "aligned" in str(e.value)
-    with pytest.raises(B.ZeroError) as e:
-        B.zero_step(buf.h, buf.grad_rows(), buf.param_rows(), buf.master, buf.m, buf.v,
-                    B.hyper(max_norm=1.0, mode=3))
-    assert e.value.code == 1
     with pytest.raises(B.ZeroError):
         B.zero_gather_bucket(buf.h, 0, 8, buf.params, buf.param_rows())   # not stage 3
     buf.close()
@@ -154,6 +150,9 @@ def test_errors_are_returned_not_raised_on_device():
         b3.step(B.hyper())                  # no bucket reduced yet
     assert e.value.code == 5
     g = [torch.zeros(512, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    with pytest.raises(B.ZeroError) as e:
+        b3.reduce_scatter(0, 512, g, B.hyper(max_norm=1.0, mode=3))   # bucketed: no speculative clip
+    assert e.value.code == 1
     b3.reduce_scatter(0, 512, g, B.hyper())
     with pytest.raises(B.ZeroError) as e:
         b3.reduce_scatter(256, 768, g, B.hyper())   # overlaps
@@ -324,3 +323,17 @@ def test_stage2_bucketed_with_clipping_and_errors():
     with pytest.raises(B.ZeroError):
         B.zero_reduce_scatter_bucket_replicas(b1.h, 0, 512, g, b1.master, b1.m, b1.v, b1.param_rows(), B.hyper())
     b1.close()
+
+
+
+@pytest.mark.parametrize("stage", [1, 2])
+@pytest.mark.parametrize("max_norm", [0.05, 1e6])
+def test_speculative_step_with_clipping(stage, max_norm):
+    # one pass assuming no clip; a step whose norm needs clipping is redone
+    # from the old slot (max_norm 0.05: every step clips; 1e6: none does)
+    inject = [(2, 1, 1234, INF)]
+    st = run_case(250_000, 8, stage, "bf16", steps=4, mode=3, double_buffer=True, inject=inject,
+                  hyper_kw=dict(max_norm=max_norm, weight_decay=0.1))
+    st.check()
+    if max_norm > 1:
+        assert st.mismatches == 0

@@ -64,9 +64,13 @@ void count(zero_handle* h, uint64_t r, uint64_t w) {
     h->tot_w += w;
 }
 
-// Resolve AUTO and check that the requested mode fits the handle.
-int resolve_mode(zero_handle* h, const zero_hyper_t* hy, int* mode) {
-    const bool clip = hy->max_norm > 0.0f;
+// Resolve AUTO and check that the requested mode fits the handle.  A
+// one-shot step (stages 1/2 with all gradients at hand) can be speculative
+// even with clipping: when the norm calls for clipping it is redone from the
+// old slot.  Bucketed steps release each bucket's gradients, so clipping
+// there needs the two-pass mode.
+int resolve_mode(zero_handle* h, const zero_hyper_t* hy, int* mode, bool one_shot = false) {
+    const bool clip = hy->max_norm > 0.0f && !one_shot;
     const bool db = double_buffered(h);
     switch (hy->mode) {
         case ZERO_MODE_AUTO:
@@ -77,7 +81,9 @@ int resolve_mode(zero_handle* h, const zero_hyper_t* hy, int* mode) {
         case ZERO_MODE_SPECULATIVE:
             if (h->stage == 0) return fail(h, ZERO_EINVAL, "speculative mode is not available for stage 0");
             if (!db) return fail(h, ZERO_EINVAL, "speculative mode needs ZERO_F_DOUBLE_BUFFER state");
-            if (clip) return fail(h, ZERO_EINVAL, "clipping needs the global norm before the update: use a two-pass mode");
+            if (clip)
+                return fail(h, ZERO_EINVAL,
+                            "clipping a bucketed step needs the global norm before the update: use a two-pass mode");
             *mode = ZERO_MODE_SPECULATIVE;
             return ZERO_OK;
         case ZERO_MODE_TWO_PASS_WS:
@@ -419,7 +425,7 @@ int zero_step(zero_handle_t h, const void* const* grads, void* const* params, fl
     }
 
     int mode = 0;
-    rc = resolve_mode(h, hyper, &mode);
+    rc = resolve_mode(h, hyper, &mode, /*one_shot=*/h->stage != 0);
     if (rc) return rc;
     if (any) {
         if (!grads) return fail(h, ZERO_EINVAL, "grads is NULL");
@@ -439,7 +445,9 @@ int zero_step(zero_handle_t h, const void* const* grads, void* const* params, fl
 
     if (mode == ZERO_MODE_SPECULATIVE) {
         if ((rc = launch(h, zg::Kind::kStepSpec, vec8, a, s, "step"))) return rc;
-        if ((rc = launch(h, zg::Kind::kRollbackReplicas, vec8, a, s, "rollback"))) return rc;
+        if ((rc = launch(h, zg::Kind::kFixupReplicas, vec8, a, s, "fixup"))) return rc;
+        cudaError_t e = zg::launch_commit_redo(h->ws.status, s);
+        if (e != cudaSuccess) return cuda_fail(h, e, "commit");
         count(h, 2 * N * P + 12 * P, 12 * P + 2 * N * P);
         return ZERO_OK;
     }

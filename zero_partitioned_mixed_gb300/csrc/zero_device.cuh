@@ -289,6 +289,29 @@ __device__ void status_commit_spec(DevStatus* st, double q) {
     st->t += 1;
 }
 
+// Speculative one-pass step done without overflow.  With no clipping
+// needed the shadow slot becomes live; when the norm calls for clipping
+// (max_norm > 0 and max_norm / (norm + 1e-6) < 1) the step is marked for a
+// redo from the old slot with the clip factor and step t+1 scalars.
+__device__ void status_decide_spec(DevStatus* st, double q, const HyperDev& h) {
+    const double norm = __dsqrt_rn(q);
+    if (h.max_norm > 0.0f) {
+        const double c = __ddiv_rn(static_cast<double>(h.max_norm), __dadd_rn(norm, 1e-6));
+        if (c < 1.0) {
+            st->overflow = 0;
+            st->applied = 0;
+            st->norm = norm;
+            st->use_clip = 1;
+            st->clip_f = __double2float_rn(c);
+            st->clip_coef = static_cast<double>(st->clip_f);
+            st->redo = 1;
+            st->sc = make_scalars(h, st->t + 1);
+            return;
+        }
+    }
+    status_commit_spec(st, q);
+}
+
 // Two-pass decision before the apply pass: clip factor and step t+1 scalars.
 __device__ void status_decide_two_pass(DevStatus* st, double q, const HyperDev& h) {
     const double norm = __dsqrt_rn(q);

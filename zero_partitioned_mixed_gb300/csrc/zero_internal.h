@@ -40,7 +40,7 @@ struct DevStatus {
     float clip_f;
     int32_t use_clip;
     int32_t error;
-    int32_t pad0;
+    int32_t redo;       // speculative step whose norm needs clipping: redo it from the old slot
     StepScalars sc;     // coefficients of the step being applied (two-pass)
     uint32_t ticket;    // last-block counter; returns to 0 after every launch
     uint32_t pad1;
@@ -90,6 +90,7 @@ enum class Kind : int {
     kApplyStage0,     // stage 0 pass 2: N state replicas
     kRollbackReplicas,
     kRollbackShard,
+    kFixupReplicas,   // after kStepSpec: roll back on overflow, or redo with clipping
     kGather,
     kRsSpec,          // stage 3 bucket reduce-scatter + fused speculative Adam
     kRsWs,            // bucket reduce-scatter into the workspace (stages 2/3)
@@ -105,6 +106,7 @@ enum class Vec : int { k8s32, k8s16, k1 };
 cudaError_t launch(Kind kind, int dtype, Vec vec, const Args& a, cudaStream_t s, int* grid_out);
 cudaError_t launch_finalize3(bool spec, const Args& a, cudaStream_t s);
 cudaError_t launch_set_scaler(DevStatus* st, float loss_scale, int64_t t, int32_t slot, cudaStream_t s);
+cudaError_t launch_commit_redo(DevStatus* st, cudaStream_t s);
 
 constexpr int kQBlock = 256;   // ZeRO++ quantization block (elements)
 

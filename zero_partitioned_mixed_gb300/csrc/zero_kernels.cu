@@ -76,7 +76,7 @@ __global__ void __launch_bounds__(kThreads) k_step_spec(const __grid_constant__ 
         if (threadIdx.x == 0) {
             DevStatus* st = a.ws.status;
             if (f) status_skip(st, qsum);
-            else status_commit_spec(st, qsum);
+            else status_decide_spec(st, qsum, a.hyper);
             st->ticket = 0u;
         }
     }
@@ -229,6 +229,62 @@ __global__ void __launch_bounds__(kThreads) k_rollback(const __grid_constant__ A
     }
 }
 
+// After k_step_spec (stages 1/2): on overflow, rewrite the replicas from the
+// old master; when the step needs clipping, redo it from the old slot --
+// reduce the N gradients again, scale by the clip factor, AdamW into the
+// shadow slot, cast, all-gather -- for k_commit_redo to make live.
+// Otherwise exit at once.
+template <int DT, class IO>
+__global__ void __launch_bounds__(kThreads) k_fixup(const __grid_constant__ Args a) {
+    constexpr int W = IO::W;
+    __shared__ Pro pro;
+    prologue_reduce(a, pro, false);
+    const DevStatus* st = a.ws.status;
+    const int overflow = st->overflow, redo = st->redo;
+    if (!overflow && !redo) return;
+    const uint64_t src = static_cast<uint64_t>(pro.live) * a.slot_stride;
+    const uint64_t dst = static_cast<uint64_t>(pro.live ^ 1) * a.slot_stride;
+    const uint64_t nvec = a.count / W;
+    for (uint64_t vi = thread_id(); vi < nvec; vi += grid_threads()) {
+        const uint64_t gi = vi * W;
+        float p[W];
+        uint32_t q[W];
+        IO::ldf(a.master + src, gi, p);
+        if (overflow) {
+#pragma unroll
+            for (int k = 0; k < W; ++k) q[k] = narrow<DT>(p[k]);
+        } else {
+            float g[W], m[W], v[W];
+            reduce_group<DT, IO>(a, gi, pro, g);
+            IO::ldf(a.m + src, gi, m);
+            IO::ldf(a.v + src, gi, v);
+            const int valid = valid_count(gi, W, a.psi);
+#pragma unroll
+            for (int k = 0; k < W; ++k) {
+                if (k < valid) {
+                    adam1(__fmul_rn(g[k], pro.clip_f), p[k], m[k], v[k], pro.sc);
+                } else {
+                    p[k] = 0.0f; m[k] = 0.0f; v[k] = 0.0f;
+                }
+                q[k] = narrow<DT>(p[k]);
+            }
+            IO::stf(a.master + dst, gi, p);
+            IO::stf(a.m + dst, gi, m);
+            IO::stf(a.v + dst, gi, v);
+        }
+        for (int r = 0; r < a.n_ranks; ++r) IO::st16(a.params[r], gi, q);
+    }
+}
+
+__global__ void k_commit_redo(DevStatus* st) {
+    if (st->redo) {
+        st->redo = 0;
+        st->live_slot ^= 1;
+        st->t += 1;
+        st->applied = 1;
+    }
+}
+
 // ZeRO-3 gather of [base, base+count): out[r][j] = shard[base + j].
 template <class IO>
 __global__ void __launch_bounds__(kThreads) k_gather(const __grid_constant__ Args a) {
@@ -338,6 +394,7 @@ __global__ void k_set_scaler(DevStatus* st, float loss_scale, int64_t t, int32_t
     st->clip_f = 1.0f;
     st->use_clip = 0;
     st->error = 0;
+    st->redo = 0;
     st->ticket = 0u;
 }
 
@@ -355,6 +412,7 @@ cudaError_t launch_dw(Kind kind, const Args& a, cudaStream_t s, int* grid_out) {
         case Kind::kApplyStage0: return run(k_apply_stage0<DT, IO>, a, nvec, s, grid_out);
         case Kind::kRollbackReplicas: return run(k_rollback<DT, IO, false>, a, nvec, s, grid_out);
         case Kind::kRollbackShard: return run(k_rollback<DT, IO, true>, a, nvec, s, grid_out);
+        case Kind::kFixupReplicas: return run(k_fixup<DT, IO>, a, nvec, s, grid_out);
         case Kind::kGather: return run(k_gather<IO>, a, nvec, s, grid_out);
         case Kind::kRsSpec: return run(k_rs<DT, IO, true, false>, a, nvec, s, grid_out);
         case Kind::kRsSpecReplicas: return run(k_rs<DT, IO, true, true>, a, nvec, s, grid_out);
@@ -381,6 +439,11 @@ cudaError_t launch(Kind kind, int dtype, Vec vec, const Args& a, cudaStream_t s,
 cudaError_t launch_finalize3(bool spec, const Args& a, cudaStream_t s) {
     if (spec) k_finalize3<true><<<1, kThreads, 0, s>>>(a);
     else k_finalize3<false><<<1, kThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_commit_redo(DevStatus* st, cudaStream_t s) {
+    k_commit_redo<<<1, 1, 0, s>>>(st);
     return cudaGetLastError();
 }
 
