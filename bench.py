@@ -653,6 +653,48 @@ def bench_stage3_zeropp(w, buckets, steps, warmup, torch, S, Z, bits):
     return ms, per_step, st, quant_ms, lmax, parts
 
 
+def bench_schedule(w, buckets, steps, warmup, torch, S, Z, prefetch, graph):
+    """Whole ZeRO-3 steps through Zero3Schedule (gathers one bucket ahead on a
+    side stream when `prefetch`; the step replayed from a CUDA graph when
+    `graph`), timed with events on the main stream around each step."""
+    from zero_partitioned_mixed_gb300.buffers import RankBuffers
+    from zero_partitioned_mixed_gb300.schedule import Zero3Schedule
+    buf = RankBuffers(w.psi, w.n_ranks, 3, w.dtype, double_buffer=True)
+    P, N = buf.psi_pad, w.n_ranks
+    td = S.torch_dtype(w.dtype)
+    mv, mm, vv = buf.state(0)
+    S.draw_master(w, mv, w.psi)
+    S.draw_moments(w, mm, vv, w.psi)
+    buf.params[:P].copy_(mv.to(td))
+    lmax = max(b - a for a, b in buckets)
+    gbuf = torch.empty((N, (lmax + 7) // 8 * 8), dtype=td, device="cuda")
+    for r in range(N):
+        S.draw_grads(w, gbuf[r], lmax, 1, r, w.loss_scale)
+    rows = [gbuf[r] for r in range(N)]
+    buf.set_scaler(w.loss_scale, 0, 0)
+    hyp = Z.hyper(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay, w.max_norm, Z.ZERO_MODE_AUTO)
+    sched = Zero3Schedule(buf, buckets, prefetch=prefetch)
+    grads = lambda i: rows
+    for _ in range(warmup):
+        sched.step(hyp, grads)
+    g = sched.capture(hyp, grads) if graph else None
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(steps):
+        if g is not None:
+            g.replay()
+        else:
+            sched.step(hyp, grads)
+    t1.record()
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / steps
+    buf.close()
+    del gbuf, sched, g
+    torch.cuda.empty_cache()
+    return ms
+
+
 def run_other(args, ws, rank, local):
     import dataclasses
 
@@ -706,6 +748,24 @@ def run_other(args, ws, rank, local):
             ms, bps, st, _, _, parts = bench_stage3_zeropp(w, buckets, args.steps, args.warmup, torch, S, Z, 8)
         lines.append(_line(w.name + ("_zeropp" if args.workload == "flat-zeropp" else ""), psi / (ms * 1e-3), ms,
                            args.steps, args.warmup, bps, "bf16", {"stage": 3, "buckets": len(buckets), **parts}))
+    elif args.workload == "schedule":
+        # ZeRO-3 step scheduling: sequential vs one-ahead prefetch on a side
+        # stream (Llama-7B), and eager vs CUDA-graph replay (toy buffer, launch-bound)
+        w = S.LLAMA7B
+        buckets = S.layer_buckets(S.llama7b_shapes(), w.psi)
+        for prefetch in (False, True):
+            ms = bench_schedule(w, buckets, args.steps, args.warmup, torch, S, Z, prefetch, False)
+            lines.append(_line(f"{w.name}_{'prefetch' if prefetch else 'sequential'}", w.psi / (ms * 1e-3), ms,
+                               args.steps, args.warmup, (6 * 8 + 30) * w.psi, w.dtype,
+                               {"stage": 3, "buckets": len(buckets), "prefetch": prefetch}))
+        toy = dataclasses.replace(S.TOY, stage=3)
+        tb = S.flat_buckets(637_952, 32, 50_000)
+        for graph in (False, True):
+            ms = bench_schedule(toy, tb, max(args.steps, 20), args.warmup, torch, S, Z, True, graph)
+            lines.append(_line(f"{toy.name}_stage3_{'graph' if graph else 'eager'}", toy.psi / (ms * 1e-3), ms,
+                               max(args.steps, 20), args.warmup, (6 * 32 + 30) * 637_952, toy.dtype,
+                               {"stage": 3, "buckets": len(tb), "cuda_graph": graph,
+                                "l2": "L2-resident, back-to-back replays"}))
     elif args.workload == "gpt2":
         w = S.GPT2
         ms, bps, st = bench_dense(w, 2, args.steps, args.warmup, torch, S, Z)
@@ -748,7 +808,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=4)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=["flat1.5b", "toy", "gpt2", "llama7b", "sweep", "zero2-buckets", "llama7b-zeropp",
-                                      "flat-zero3", "flat-zeropp"], default="flat1.5b")
+                                      "flat-zero3", "flat-zeropp", "schedule"], default="flat1.5b")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--psi", type=int, default=None, help="override psi of the flat workload (profiling)")

@@ -1,0 +1,122 @@
+"""ZeRO-3 step schedule: gathers prefetched on a side stream, CUDA-graph capture.
+
+ZeRO summary Sec. 5 (P_os+g+p): the parameter all-gather is spread across
+forward propagation, each layer's parameters fetched just before use and
+discarded after; backward fetches them again in reverse order and
+reduce-scatters each layer's gradients as they appear; a layer may be
+prefetched while the previous one computes.  The "ZeRO Stage 1/2/3" guide
+names the corresponding knob (prefetch_bucket_size).
+
+Here the gather of bucket b+1 (forward) or b-1 (backward) is issued on a
+side stream one bucket ahead, into the other of two output buffer sets,
+while the main stream runs the caller's work on bucket b (its forward or
+backward compute, then the reduce-scatter).  Events order every reuse of a
+buffer set.  All launches go through the C ABI; nothing here computes.
+
+A step whose buffers and hyper-parameters stay fixed can be captured once
+into a CUDA graph and replayed: the library's calls never synchronise or
+allocate after the first (warm-up) step, and its step count, loss scale
+and state slot live on the device, so each replay is the next step.
+"""
+
+from __future__ import annotations
+
+from typing import Callable, List, Optional, Sequence, Tuple
+
+import torch
+
+from . import _binding as B
+from .buffers import RankBuffers
+
+
+class Zero3Schedule:
+    """One ZeRO-3 step over fixed buckets with one-ahead gather prefetch.
+
+    buf: a stage-3 RankBuffers; buckets: [(a, b)] tiling [0, psi_pad).
+    grad_rows(i) -> list of N device tensors holding rank r's gradient of
+    bucket i (the caller's backward writes them); forward(i, rows) and
+    backward(i, rows) are the caller's per-bucket work on the gathered
+    16-bit parameters (default: none).
+    """
+
+    def __init__(self, buf: RankBuffers, buckets: Sequence[Tuple[int, int]], prefetch: bool = True):
+        if buf.stage != 3:
+            raise ValueError("Zero3Schedule needs a stage-3 RankBuffers")
+        self.buf = buf
+        self.buckets = list(buckets)
+        self.prefetch = prefetch
+        lmax = max(b - a for a, b in self.buckets) if self.buckets else 0
+        lpad = max(8, (lmax + 7) // 8 * 8)
+        td = buf.params.dtype
+        nsets = 2 if prefetch else 1
+        self.outs = [torch.empty((buf.n, lpad), dtype=td, device=buf.params.device) for _ in range(nsets)]
+        self.side = torch.cuda.Stream(device=buf.params.device) if prefetch else None
+        self.graph: Optional[torch.cuda.CUDAGraph] = None
+
+    def _rows(self, k: int) -> List[torch.Tensor]:
+        o = self.outs[k % len(self.outs)]
+        return [o[r] for r in range(self.buf.n)]
+
+    def _pass(self, order: Sequence[int], work: Optional[Callable], rs: Optional[Callable]) -> None:
+        main = torch.cuda.current_stream()
+        buf = self.buf
+        if not self.prefetch:
+            for i in order:
+                a, b = self.buckets[i]
+                buf.gather(a, b, self._rows(0), main)
+                if work is not None:
+                    work(i, self._rows(0))
+                if rs is not None:
+                    rs(i)
+            return
+        n = len(order)
+        ready = [torch.cuda.Event() for _ in range(n)]       # gather k done (side stream)
+        free = [torch.cuda.Event() for _ in range(2)]        # output set released (main stream)
+        for e in free:
+            e.record(main)
+
+        def issue(k):
+            a, b = self.buckets[order[k]]
+            self.side.wait_event(free[k % 2])
+            with torch.cuda.stream(self.side):
+                buf.gather(a, b, self._rows(k), self.side)
+                ready[k].record(self.side)
+
+        if n:
+            issue(0)
+        for k in range(n):
+            if k + 1 < n:
+                issue(k + 1)                                   # prefetch the next bucket
+            main.wait_event(ready[k])
+            if work is not None:
+                work(order[k], self._rows(k))
+            if rs is not None:
+                rs(order[k])
+            free[k % 2].record(main)
+        # every gather was joined into the main stream through ready[k]
+
+    def step(self, hyp, grad_rows: Callable[[int], List[torch.Tensor]],
+             forward: Optional[Callable] = None, backward: Optional[Callable] = None) -> None:
+        """Forward gathers, backward gathers + reduce-scatters, then zero_step."""
+        buf = self.buf
+        nb = len(self.buckets)
+        self._pass(range(nb), forward, None)
+
+        def rs(i):
+            a, b = self.buckets[i]
+            buf.reduce_scatter(a, b, grad_rows(i), hyp)
+
+        self._pass(range(nb - 1, -1, -1), backward, rs)
+        buf.step(hyp)
+
+    def capture(self, hyp, grad_rows, forward=None, backward=None) -> torch.cuda.CUDAGraph:
+        """Capture one step into a CUDA graph (call after one eager warm-up step)."""
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                self.step(hyp, grad_rows, forward, backward)
+        torch.cuda.current_stream().wait_stream(s)
+        self.graph = g
+        return g
