@@ -170,6 +170,69 @@ __device__ __forceinline__ void load_codes8_f(const void* codes, uint64_t e0, fl
     }
 }
 
+// Two fp32 lanes in one 64-bit register for the packed add/sub/mul.rn.f32x2
+// of sm_100 and later: each half is an ordinary fp32 operation rounded once,
+// so results are those of the scalar instructions, at half the issue cost.
+using f2 = unsigned long long;
+__device__ __forceinline__ f2 f2pack(float a, float b) {
+    f2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ f2 f2bits(uint32_t a, uint32_t b) {
+    f2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(a), "r"(b));
+    return r;
+}
+__device__ __forceinline__ void f2unpack(f2 x, float& a, float& b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(x));
+}
+__device__ __forceinline__ f2 f2add(f2 a, f2 b) {
+    f2 r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+// lo + q*scale for a pair, with the multiply packed and the add scalar: a
+// packed multiply feeding a packed add may be fused into one packed FMA
+// (observed: results then differ from two separately rounded operations).
+__device__ __forceinline__ f2 f2dequant(f2 q_biased, f2 two23, f2 sc, float lo) {
+    f2 prod;
+    asm("{\n\t.reg .b64 t;\n\tsub.rn.f32x2 t, %1, %2;\n\tmul.rn.f32x2 %0, t, %3;\n\t}"
+        : "=l"(prod) : "l"(q_biased), "l"(two23), "l"(sc));
+    float p0, p1;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(p0), "=f"(p1) : "l"(prod));
+    return f2pack(__fadd_rn(lo, p0), __fadd_rn(lo, p1));
+}
+
+__device__ __forceinline__ f2 f2sub(f2 a, f2 b) {
+    f2 r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ f2 f2mul(f2 a, f2 b) {
+    f2 r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+// A lane's 8 codes at element e0 as four pairs of 2^23-biased floats
+// (0x4B000000 | code): subtracting 2^23 gives the codes exactly.
+template <int BITS>
+__device__ __forceinline__ void load_codes8_biased(const void* codes, uint64_t e0, f2 (&q)[4]) {
+    if (BITS == 8) {
+        const uint2 w = __ldcs(reinterpret_cast<const uint2*>(static_cast<const unsigned char*>(codes) + e0));
+        q[0] = f2bits(__byte_perm(w.x, 0x4B000000u, 0x7540u), __byte_perm(w.x, 0x4B000000u, 0x7541u));
+        q[1] = f2bits(__byte_perm(w.x, 0x4B000000u, 0x7542u), __byte_perm(w.x, 0x4B000000u, 0x7543u));
+        q[2] = f2bits(__byte_perm(w.y, 0x4B000000u, 0x7540u), __byte_perm(w.y, 0x4B000000u, 0x7541u));
+        q[3] = f2bits(__byte_perm(w.y, 0x4B000000u, 0x7542u), __byte_perm(w.y, 0x4B000000u, 0x7543u));
+    } else {
+        const uint32_t w = __ldcs(reinterpret_cast<const unsigned int*>(static_cast<const unsigned char*>(codes) + (e0 >> 1)));
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            q[k] = f2bits(((w >> (8 * k)) & 0xFu) | 0x4B000000u, ((w >> (8 * k + 4)) & 0xFu) | 0x4B000000u);
+    }
+}
+
 template <int BITS>
 __device__ __forceinline__ uint32_t load_code1(const void* codes, uint64_t e) {
     if (BITS == 8) return static_cast<const unsigned char*>(codes)[e];
@@ -279,54 +342,62 @@ __global__ void __launch_bounds__(kThreads) k_dequantize(const __grid_constant__
 }
 
 // Sum over ranks (order 0..N-1, from +0) of the dequantized gradients of W
-// elements at bucket-local index j, then unscale.  Ranks go in chunks of 8
-// whose code and scale loads are all issued before any arithmetic.
+// elements at bucket-local index j, then unscale: s += lo + q*scale per
+// rank, each operation rounded once.  Ranks go in chunks of 8 whose code and
+// scale loads are all issued before any arithmetic; the 8-wide path works on
+// packed pairs.
 template <int BITS, int W>
 __device__ __forceinline__ void reduce_group_q(const Args& a, uint64_t j, const Pro& pro, float (&g)[W]) {
-    float s[W];
-#pragma unroll
-    for (int k = 0; k < W; ++k) s[k] = 0.0f;
     const uint64_t blk = j / kQBlock;
     const int n = a.n_ranks;
-    int r = 0;
-    for (; r + 8 <= n; r += 8) {
-        float q[8][W];
-        float2 sl[8];
+    if (W == 8) {
+        const f2 two23 = f2pack(kTwo23, kTwo23);
+        f2 s2[4];
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
-            sl[t] = *reinterpret_cast<const float2*>(a.qsrc[r + t] + 2 * blk);
-            if (W == 8) {
-                float tmp[8];
-                load_codes8_f<BITS>(a.grads[r + t], j, tmp);
+        for (int k = 0; k < 4; ++k) s2[k] = f2pack(0.0f, 0.0f);
+        int r = 0;
+        for (; r + 8 <= n; r += 8) {
+            f2 q[8][4];
+            float2 sl[8];
 #pragma unroll
-                for (int k = 0; k < W; ++k) q[t][k] = tmp[k];
-            } else {
+            for (int t = 0; t < 8; ++t) {
+                sl[t] = *reinterpret_cast<const float2*>(a.qsrc[r + t] + 2 * blk);
+                load_codes8_biased<BITS>(a.grads[r + t], j, q[t]);
+            }
 #pragma unroll
-                for (int k = 0; k < W; ++k) q[t][k] = as_float(load_code1<BITS>(a.grads[r + t], j + k));
+            for (int t = 0; t < 8; ++t) {
+                const f2 sc = f2pack(sl[t].x, sl[t].x);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) s2[k] = f2add(s2[k], f2dequant(q[t][k], two23, sc, sl[t].y));
             }
         }
+        for (; r < n; ++r) {
+            const float2 sl = *reinterpret_cast<const float2*>(a.qsrc[r] + 2 * blk);
+            f2 q[4];
+            load_codes8_biased<BITS>(a.grads[r], j, q);
+            const f2 sc = f2pack(sl.x, sl.x);
 #pragma unroll
-        for (int t = 0; t < 8; ++t)
-#pragma unroll
-            for (int k = 0; k < W; ++k) s[k] = __fadd_rn(s[k], __fadd_rn(sl[t].y, __fmul_rn(q[t][k], sl[t].x)));
-    }
-    for (; r < n; ++r) {
-        const float2 sl = *reinterpret_cast<const float2*>(a.qsrc[r] + 2 * blk);
-        uint32_t q[W];
-        if (W == 8) {
-            uint32_t tmp[8];
-            load_codes8<BITS>(a.grads[r], j, tmp);
-#pragma unroll
-            for (int k = 0; k < W; ++k) q[k] = tmp[k];
-        } else {
-#pragma unroll
-            for (int k = 0; k < W; ++k) q[k] = load_code1<BITS>(a.grads[r], j + k);
+            for (int k = 0; k < 4; ++k) s2[k] = f2add(s2[k], f2dequant(q[k], two23, sc, sl.y));
         }
 #pragma unroll
-        for (int k = 0; k < W; ++k) s[k] = __fadd_rn(s[k], dequant(q[k], sl.x, sl.y));
-    }
+        for (int k = 0; k < 4; ++k) {
+            float x0, x1;
+            f2unpack(s2[k], x0, x1);
+            g[2 * k] = pro.use_div ? __fdiv_rn(x0, pro.den) : __fmul_rn(x0, pro.inv);
+            g[2 * k + 1] = pro.use_div ? __fdiv_rn(x1, pro.den) : __fmul_rn(x1, pro.inv);
+        }
+    } else {
+        float s[W];
 #pragma unroll
-    for (int k = 0; k < W; ++k) g[k] = pro.use_div ? __fdiv_rn(s[k], pro.den) : __fmul_rn(s[k], pro.inv);
+        for (int k = 0; k < W; ++k) s[k] = 0.0f;
+        for (int r = 0; r < n; ++r) {
+            const float2 sl = *reinterpret_cast<const float2*>(a.qsrc[r] + 2 * blk);
+#pragma unroll
+            for (int k = 0; k < W; ++k) s[k] = __fadd_rn(s[k], dequant(load_code1<BITS>(a.grads[r], j + k), sl.x, sl.y));
+        }
+#pragma unroll
+        for (int k = 0; k < W; ++k) g[k] = pro.use_div ? __fdiv_rn(s[k], pro.den) : __fmul_rn(s[k], pro.inv);
+    }
 }
 
 // ZeRO-3 reduce-scatter of bucket [base, base+count) from the N ranks'
