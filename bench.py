@@ -236,7 +236,8 @@ def run_ours(args, ws, rank, local):
 
     w, buf, sets = setup_flat15b(Z, S, torch, args.psi)
     N, P = w.n_ranks, buf.psi_pad
-    hyp = Z.hyper(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay, w.max_norm, Z.ZERO_MODE_AUTO)
+    step_mode = Z.ZERO_MODE_SPECULATIVE_STAGED if args.mode == "staged" else Z.ZERO_MODE_AUTO
+    hyp = Z.hyper(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay, w.max_norm, step_mode)
     stream = torch.cuda.current_stream()
     nsets = sets.shape[0]
 
@@ -289,7 +290,8 @@ def run_ours(args, ws, rank, local):
         "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "storage_dtype": w.dtype,
         "data": "synthetic",
-        "config": {"workload": w.name, "psi": w.psi, "n_ranks": N, "stage": w.stage, "mode": "speculative",
+        "config": {"workload": w.name, "psi": w.psi, "n_ranks": N, "stage": w.stage,
+                   "mode": "speculative, staged through shared memory" if args.mode == "staged" else "speculative",
                    "grad_sets": nsets, "overflow_every": f"set {inject_set + 1} of {nsets} (+inf in rank 5)",
                    "l2": f"inputs larger than L2: {alg_bytes / 1e9:.1f} GB per step, no flush needed",
                    "parallelism": "replicas only" if ws > 1 else "1 GPU"},
@@ -809,6 +811,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=["flat1.5b", "toy", "gpt2", "llama7b", "sweep", "zero2-buckets", "llama7b-zeropp",
                                       "flat-zero3", "flat-zeropp", "schedule"], default="flat1.5b")
+    ap.add_argument("--mode", choices=["auto", "staged"], default="auto",
+                    help="flat workload: the step kernel (staged = inputs through shared memory by bulk copies)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--psi", type=int, default=None, help="override psi of the flat workload (profiling)")

@@ -68,8 +68,13 @@ typedef enum {
     ZERO_MODE_AUTO = 0,            /* SPECULATIVE if possible, else TWO_PASS_WS for N > 4, else REREAD */
     ZERO_MODE_TWO_PASS_WS = 1,     /* pass 1 writes fp32 g_hat to workspace; pass 2 reads it */
     ZERO_MODE_TWO_PASS_REREAD = 2, /* pass 2 reduces the N gradient buffers again */
-    ZERO_MODE_SPECULATIVE = 3      /* one pass writing the shadow state slot; commit, roll back, or
+    ZERO_MODE_SPECULATIVE = 3,     /* one pass writing the shadow state slot; commit, roll back, or
                                       (one-shot step whose norm needs clipping) redo from the old slot */
+    ZERO_MODE_SPECULATIVE_STAGED = 4 /* SPECULATIVE, inputs staged through shared memory by bulk
+                                        async copies (stages 1/2 one-shot step; N <= 19, i.e. two
+                                        stages of N*4 KiB + 24 KiB fit in 200 KiB of shared
+                                        memory; psi_pad a multiple of 8; fp32 state 32-byte
+                                        aligned; otherwise ZERO_EINVAL) */
 } zero_mode_t;
 
 /* zero_init_partition flags */

@@ -28,8 +28,8 @@ def pool():
     p.close()
 
 
-def _hyper(w):
-    return (B.hyper(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay, w.max_norm, B.ZERO_MODE_AUTO),
+def _hyper(w, mode=B.ZERO_MODE_AUTO):
+    return (B.hyper(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay, w.max_norm, mode),
             O.Hyper(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay, w.max_norm))
 
 
@@ -49,9 +49,11 @@ def _check_samples(buf, slot, idx_t, p, m, v, dtype, n, stage):
             assert int(ulp16(q[r], want_q).max()) <= ULP16 and np.array_equal(q[r], want_q)
 
 
-def test_flat_1p5b_stage1_four_steps_with_overflow(pool):
+@pytest.mark.parametrize("mode", [B.ZERO_MODE_AUTO, B.ZERO_MODE_SPECULATIVE_STAGED])
+def test_flat_1p5b_stage1_four_steps_with_overflow(pool, mode):
+    # the bench's workload in both of its launch configurations
     w = S.FLAT15B
-    hb, ho = _hyper(w)
+    hb, ho = _hyper(w, mode)
     n, dt = w.n_ranks, w.dtype
     buf = RankBuffers(w.psi, n, w.stage, dt, double_buffer=True, alloc_grads=False)
     P = buf.psi_pad

@@ -113,3 +113,28 @@ def test_no_writes_outside_buffers_stage3_and_zeropp(db):
     torch.cuda.synchronize()
     G.check()
     B.zero_destroy(h)
+
+
+@pytest.mark.parametrize("psi,n", [(100_003, 8), (5, 2), (64, 1), (300_000, 19)])
+def test_no_writes_outside_buffers_staged_step(psi, n):
+    G = Guarded()
+    h = B.zero_init_partition(psi, n, 1, B.ZERO_FP16, 8, B.ZERO_F_DOUBLE_BUFFER)
+    P = B.zero_partition_info(h)[0]
+    grads = [G.tensor(P, torch.float16) for _ in range(n)]
+    params = [G.tensor(P, torch.float16) for _ in range(n)]
+    master, m, v = (G.tensor(2 * P, torch.float32) for _ in range(3))
+    torch.manual_seed(psi)
+    for g in grads:
+        g[:psi].copy_(torch.randn(psi, device="cuda").mul_(1e-2))
+    master[:psi].normal_(0, 0.02)
+    for r in range(n):
+        params[r].copy_(master[:P].to(torch.float16))
+    mode = B.ZERO_MODE_SPECULATIVE_STAGED
+    for k, hyp in enumerate([B.hyper(mode=mode), B.hyper(mode=mode, max_norm=1e-3),
+                             B.hyper(mode=mode, max_norm=1e-3)]):
+        if k == 2:
+            grads[n - 1][min(3, psi - 1)] = float("inf")
+        B.zero_step(h, grads, params, master, m, v, hyp)
+    torch.cuda.synchronize()
+    G.check()
+    B.zero_destroy(h)

@@ -10,7 +10,7 @@ raises :class:`ZeroError` with the command that builds it.
 
 from ._binding import (  # noqa: F401
     ZERO_BF16, ZERO_F_DOUBLE_BUFFER, ZERO_FP16, ZERO_MAX_RANKS,
-    ZERO_MODE_AUTO, ZERO_MODE_SPECULATIVE, ZERO_MODE_TWO_PASS_REREAD,
+    ZERO_MODE_AUTO, ZERO_MODE_SPECULATIVE, ZERO_MODE_SPECULATIVE_STAGED, ZERO_MODE_TWO_PASS_REREAD,
     ZERO_MODE_TWO_PASS_WS, ZeroError, exported_symbols, hyper, library_path,
     load_library, zero_bytes_moved, zero_destroy, zero_gather_bucket,
     zero_get_status, zero_init_partition, zero_last_error, zero_partition_info,

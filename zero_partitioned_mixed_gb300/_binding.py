@@ -10,6 +10,7 @@ from .build import LIB_PATH
 
 ZERO_FP16, ZERO_BF16 = 0, 1
 ZERO_MODE_AUTO, ZERO_MODE_TWO_PASS_WS, ZERO_MODE_TWO_PASS_REREAD, ZERO_MODE_SPECULATIVE = 0, 1, 2, 3
+ZERO_MODE_SPECULATIVE_STAGED = 4
 ZERO_F_DOUBLE_BUFFER = 1
 ZERO_MAX_RANKS = 64
 

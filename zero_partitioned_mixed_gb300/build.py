@@ -25,7 +25,7 @@ BUILD_DIR = os.path.join(PKG, "_build")
 LIB_NAME = "libzero_gb300.so"
 LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
 
-SOURCES = ["zero_kernels.cu", "zero_quant.cu", "zero_api.cpp", "zero_noalloc.cu"]
+SOURCES = ["zero_kernels.cu", "zero_quant.cu", "zero_tma.cu", "zero_api.cpp", "zero_noalloc.cu"]
 HEADERS = [os.path.join(INCLUDE, "zero_gb300.h"), os.path.join(CSRC, "zero_internal.h"),
            os.path.join(CSRC, "zero_device.cuh")]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"

@@ -86,6 +86,14 @@ int resolve_mode(zero_handle* h, const zero_hyper_t* hy, int* mode, bool one_sho
                             "clipping a bucketed step needs the global norm before the update: use a two-pass mode");
             *mode = ZERO_MODE_SPECULATIVE;
             return ZERO_OK;
+        case ZERO_MODE_SPECULATIVE_STAGED:
+            if (!one_shot || h->stage == 0 || h->stage == 3)
+                return fail(h, ZERO_EINVAL, "staged speculative mode is for the one-shot stage 1/2 step");
+            if (!db) return fail(h, ZERO_EINVAL, "speculative mode needs ZERO_F_DOUBLE_BUFFER state");
+            if (zg::tma_stages(h->n) < 2) return fail(h, ZERO_EINVAL, "staged mode supports up to 19 ranks");
+            if (h->psi_pad % 8) return fail(h, ZERO_EINVAL, "staged mode needs psi_pad to be a multiple of 8");
+            *mode = ZERO_MODE_SPECULATIVE_STAGED;
+            return ZERO_OK;
         case ZERO_MODE_TWO_PASS_WS:
             *mode = ZERO_MODE_TWO_PASS_WS;
             return ZERO_OK;
@@ -443,8 +451,15 @@ int zero_step(zero_handle_t h, const void* const* grads, void* const* params, fl
     a.m = m;
     a.v = v;
 
-    if (mode == ZERO_MODE_SPECULATIVE) {
-        if ((rc = launch(h, zg::Kind::kStepSpec, vec8, a, s, "step"))) return rc;
+    if (mode == ZERO_MODE_SPECULATIVE || mode == ZERO_MODE_SPECULATIVE_STAGED) {
+        if (mode == ZERO_MODE_SPECULATIVE_STAGED) {
+            if (any && pick_vec(vec8, a) != zg::Vec::k8s32)
+                return fail(h, ZERO_EINVAL, "staged mode needs 32-byte aligned master/m/v");
+            cudaError_t e = zg::launch_step_tma(h->dtype, a, s);
+            if (e != cudaSuccess) return cuda_fail(h, e, "staged step");
+        } else if ((rc = launch(h, zg::Kind::kStepSpec, vec8, a, s, "step"))) {
+            return rc;
+        }
         if ((rc = launch(h, zg::Kind::kFixupReplicas, vec8, a, s, "fixup"))) return rc;
         cudaError_t e = zg::launch_commit_redo(h->ws.status, s);
         if (e != cudaSuccess) return cuda_fail(h, e, "commit");

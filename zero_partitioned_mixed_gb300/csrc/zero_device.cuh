@@ -221,9 +221,10 @@ __device__ __forceinline__ int valid_count(uint64_t gi, int W, uint64_t psi) {
     return static_cast<int>(psi - gi);
 }
 
-// Deterministic block sum (fixed shuffle tree, then warp sums in order).
+// Deterministic block sum (fixed shuffle tree, then warp sums in order);
+// any block size up to 1024 threads.
 __device__ double block_sum(double x) {
-    __shared__ double sm[kThreads / 32];
+    __shared__ double sm[32];
     __syncthreads();
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) x = __dadd_rn(x, __shfl_down_sync(0xFFFFFFFFu, x, off));

@@ -108,6 +108,11 @@ cudaError_t launch_finalize3(bool spec, const Args& a, cudaStream_t s);
 cudaError_t launch_set_scaler(DevStatus* st, float loss_scale, int64_t t, int32_t slot, cudaStream_t s);
 cudaError_t launch_commit_redo(DevStatus* st, cudaStream_t s);
 
+// The stage 1/2 speculative step with bulk-copy staging (zero_tma.cu), and
+// its pipeline depth for N ranks (0: not available for that N).
+cudaError_t launch_step_tma(int dtype, const Args& a, cudaStream_t s);
+int tma_stages(int n_ranks);
+
 constexpr int kQBlock = 256;   // ZeRO++ quantization block (elements)
 
 enum class QKind : int {
