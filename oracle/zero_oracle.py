@@ -71,6 +71,8 @@ __all__ = [
     "all_reduce_mean", "reduce_scatter_mean", "all_gather",
     "Q_BLOCK", "quantize_blocks", "dequantize_blocks", "pack_int4", "unpack_int4",
     "quantized_gather", "step_stage3_quantized",
+    "persistent_layout", "comm_elems_persistent", "model_state_bytes_persistent",
+    "step_stage3_persistent",
 ]
 
 
@@ -567,6 +569,86 @@ def step_stage3(state: State, bucket_grads: Sequence[np.ndarray],
     out.params[:psi] = rne16(out.master[:psi], state.dtype)
     res.norm, res.clip = norm, c
     return out, res
+
+
+# ---------------------------------------------------------------------------
+# ZeRO-3 with param_persistence_threshold
+# ---------------------------------------------------------------------------
+def persistent_layout(sizes: Sequence[int], threshold: int) -> Tuple[List[int], int, int]:
+    """Tensor order of the flat buffer when small tensors stay replicated.
+
+    "ZeRO Stage 1/2/3" guide, ZeRO-3 config: parameters with fewer elements
+    than param_persistence_threshold stay replicated (the comparison is
+    strict: a tensor of exactly the threshold is partitioned).  Reading:
+    the partitioned tensors come first and the persistent ones after them,
+    each group in model order, so the persistent tensors form one region
+    [p0, psi) of the flat buffer.
+
+    Returns (order, p0, psi): order[k] is the model index of the k-th tensor
+    in the flat buffer.
+    """
+    order = []
+    for i, n in enumerate(sizes):
+        if not n < threshold:
+            order.append(i)
+    p0 = 0
+    for i in order:
+        p0 += int(sizes[i])
+    for i, n in enumerate(sizes):
+        if n < threshold:
+            order.append(i)
+    return order, p0, int(sum(int(n) for n in sizes))
+
+
+def comm_elems_persistent(psi: int, psi_pers: int) -> int:
+    """Elements a rank communicates per ZeRO-3 step with a persistent region.
+
+    ZeRO summary Sec. 7 counts P_os+g+p as a forward gather (Psi), a
+    backward gather (Psi) and a gradient reduce-scatter (Psi).  Persistent
+    parameters are not gathered in forward or backward; their replicas are
+    refreshed by one all-gather of psi_pers after the update, which is how
+    the stage 1/2 parameters are refreshed.
+    """
+    return 2 * (psi - psi_pers) + psi + psi_pers
+
+
+def model_state_bytes_persistent(psi: int, psi_pers: int, n_ranks: int, k: int = 12) -> int:
+    """Per-rank model-state bytes of ZeRO-3 with a persistent region.
+
+    ZeRO summary Sec. 5: P_os+g+p holds (4 + K) Psi / N.  Each rank also
+    holds the full 16-bit copy of the persistent parameters (2 psi_pers);
+    their owner shards stay, as the source of the refresh.  Exact when psi
+    is a multiple of n_ranks (pass psi_pad).
+    """
+    return ((4 + k) * psi) // n_ranks + 2 * psi_pers
+
+
+def step_stage3_persistent(state: State, bucket_grads: Sequence[np.ndarray],
+                           buckets: Sequence[Tuple[int, int]], h: Hyper,
+                           p0: int) -> Tuple[State, StepResult, List[np.ndarray]]:
+    """ZeRO-3 step whose region [p0, psi_pad) stays replicated.
+
+    Same update as step_stage3 (persistence moves no value, only where the
+    16-bit copies live): buckets ending at or before p0 are gathered in
+    forward and in backward; buckets starting at or after p0 are only
+    reduce-scattered.  After the update every rank's persistent copy is the
+    all-gather of the new shards over [p0, psi_pad); after a skipped step it
+    is the unchanged old one.
+
+    Returns (state, result, replicas) with replicas a list of N uint16
+    arrays of length psi_pad - p0.  result.gathered_fwd / gathered_bwd hold
+    the gathered buckets only.
+    """
+    for (a, b) in buckets:
+        if a < p0 < b:
+            raise ValueError("a bucket straddles the persistent boundary")
+    out, res = step_stage3(state, bucket_grads, buckets, h)
+    keep = [i for i, (a, b) in enumerate(buckets) if b <= p0 and a < p0]
+    res.gathered_fwd = [res.gathered_fwd[i] for i in keep]
+    res.gathered_bwd = [res.gathered_bwd[i] for i in keep]
+    pp = state.part.psi_pad
+    replicas = [out.params[p0:pp].copy() for _ in range(state.part.n_ranks)]
+    return out, res, replicas
 
 
 def step(state: State, grads_bits: np.ndarray, h: Hyper,

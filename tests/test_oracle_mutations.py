@@ -46,6 +46,10 @@ PIN_RUNS = [
     (pins.test_quantizer_constant_block_and_nan, {}),
     (pins.test_int4_packing, {}),
     (pins.test_quantized_reduce_scatter_equals_plain_on_grid_gradients, dict(bits=8)),
+    (pins.test_persistent_layout_against_a_sort_key, {}),
+    (pins.test_persistent_threshold_is_strict_and_degenerate_cases, {}),
+    (pins.test_persistent_comm_and_memory_endpoints, {}),
+    (pins.test_persistence_moves_no_value, dict(dt="fp16")),
 ]
 
 
@@ -193,6 +197,36 @@ def pack4_swapped_nibbles(codes):
     return (c[1::2] & 0x0F) | ((c[0::2] & 0x0F) << 4)
 
 
+def persist_threshold_inclusive(sizes, threshold):
+    # "<=" instead of "<": a tensor of exactly the threshold becomes persistent
+    big = [i for i, n in enumerate(sizes) if n > threshold]
+    small = [i for i, n in enumerate(sizes) if n <= threshold]
+    return big + small, sum(sizes[i] for i in big), sum(sizes)
+
+
+def persist_small_first(sizes, threshold):
+    # the region placed at the front instead of the end
+    big = [i for i, n in enumerate(sizes) if not n < threshold]
+    small = [i for i, n in enumerate(sizes) if n < threshold]
+    return small + big, sum(sizes[i] for i in small), sum(sizes)
+
+
+def persist_comm_no_refresh(psi, psi_pers):
+    return 2 * (psi - psi_pers) + psi
+
+
+def persist_msb_no_replicas(psi, psi_pers, n_ranks, k=12):
+    return ((4 + k) * psi) // n_ranks
+
+
+def persist_step_stale_replicas(state, bucket_grads, buckets, h, p0):
+    # the persistent copies left at the values before the update
+    pp = state.part.psi_pad
+    old = [state.params[p0:pp].copy() for _ in range(state.part.n_ranks)]
+    out, res = Z.step_stage3(state, bucket_grads, buckets, h)
+    return out, res, old
+
+
 MUTANTS = [
     ("adam_update", adam_swapped_beta),
     ("adam_update", adam_no_decay),
@@ -214,6 +248,11 @@ MUTANTS = [
     ("quantize_blocks", quant_floor),
     ("dequantize_blocks", dequant_forgets_lo),
     ("pack_int4", pack4_swapped_nibbles),
+    ("persistent_layout", persist_threshold_inclusive),
+    ("persistent_layout", persist_small_first),
+    ("comm_elems_persistent", persist_comm_no_refresh),
+    ("model_state_bytes_persistent", persist_msb_no_replicas),
+    ("step_stage3_persistent", persist_step_stale_replicas),
 ]
 
 

@@ -510,3 +510,91 @@ def test_quantized_gather_reproduces_grid_weights():
     w = O.rne16(((q - 128) * 2.0 ** -9).astype(np.float32), O.BF16)
     outs, view = O.quantized_gather(w, 0, 600, O.BF16, 4)
     assert len(outs) == 4 and np.array_equal(view, w)
+
+
+# ---------------------------------------------------------------- ZeRO-3 param_persistence_threshold
+def test_persistent_layout_against_a_sort_key():
+    # "ZeRO Stage 1/2/3" guide, ZeRO-3 config: params with fewer elements than
+    # the threshold stay replicated.  The layout is the stable partition
+    # "partitioned first, persistent last": the same order as sorting by the
+    # key (is_small, model index), which the oracle does not compute.
+    rng = np.random.default_rng(11)
+    for trial in range(200):
+        k = int(rng.integers(0, 12))
+        sizes = [int(x) for x in rng.integers(1, 40, k)]
+        thr = int(rng.integers(0, 45))
+        order, p0, psi = O.persistent_layout(sizes, thr)
+        want = sorted(range(k), key=lambda i: (sizes[i] < thr, i))
+        assert order == want
+        assert psi == sum(sizes)
+        assert p0 == sum(s for s in sizes if s >= thr)
+        # the region [p0, psi) is exactly the small tensors
+        pos = 0
+        for i in order:
+            assert (pos >= p0) == (sizes[i] < thr)
+            pos += sizes[i]
+
+
+def test_persistent_threshold_is_strict_and_degenerate_cases():
+    sizes = [100, 99, 101, 100]
+    order, p0, psi = O.persistent_layout(sizes, 100)
+    assert order == [0, 2, 3, 1] and p0 == 301 and psi == 400   # exactly 100 stays partitioned
+    assert O.persistent_layout(sizes, 0) == ([0, 1, 2, 3], 400, 400)       # nothing persistent
+    assert O.persistent_layout(sizes, 10 ** 9) == ([0, 1, 2, 3], 0, 400)   # everything persistent
+    assert O.persistent_layout([], 5) == ([], 0, 0)
+
+
+def test_guide_threshold_on_the_model_lists():
+    # threshold 1e5 (the guide's value).  GPT-2 small: every bias and layer
+    # norm is persistent -- per layer 2*768 (ln_1) + 2304 + 768 + 2*768 (ln_2)
+    # + 3072 + 768 = 9984, times 12, plus ln_f 2*768 = 121,344 elements in 98
+    # tensors.  Llama-7B: the 65 RMSNorm weights of 4096 = 266,240.
+    from zero_partitioned_mixed_gb300 import synth as S
+    for shapes, n_pers, psi_pers in ((S.gpt2_small_shapes(), 98, 121_344), (S.llama7b_shapes(), 65, 266_240)):
+        sizes = [S.numel(s) for _, s in shapes]
+        order, p0, psi = O.persistent_layout(sizes, 100_000)
+        assert psi - p0 == psi_pers
+        assert sum(1 for i in order if sizes[i] < 100_000) == n_pers
+
+
+def test_persistent_comm_and_memory_endpoints():
+    # No persistent tensor: ZeRO-3's 3 Psi and (4+K) Psi / N.  Every tensor
+    # persistent: the forward/backward gathers vanish and the refresh is one
+    # all-gather, so the communication is ZeRO-2's 2 Psi, and the memory is
+    # ZeRO-2's plus the 16-bit owner shards kept as the refresh's source.
+    for psi, n in ((637_952, 32), (124_439_808, 8), (6_738_415_616 + 0, 8)):
+        pp = O.partition(psi, n, 8).psi_pad
+        assert O.comm_elems_persistent(pp, 0) == O.comm_elems_paper(pp, 3)
+        assert O.comm_elems_persistent(pp, pp) == O.comm_elems_paper(pp, 2)
+        assert O.comm_elems_persistent(pp, 1000) == 3 * pp - 1000
+        assert O.model_state_bytes_persistent(pp, 0, n) == O.model_state_bytes(pp, n, 3)
+        assert O.model_state_bytes_persistent(pp, pp, n) == O.model_state_bytes(pp, n, 2) + 2 * pp // n
+
+
+@pytest.mark.parametrize("dt", [O.FP16, O.BF16])
+def test_persistence_moves_no_value(dt):
+    # persistence changes where 16-bit copies live, not what the step computes:
+    # three steps equal stage 1's bit for bit; the persistent copies equal the
+    # cast of the new master over [p0, psi_pad); an overflowed step keeps them.
+    n, psi = 4, 1001
+    part, master, m, v, grads = _random_case(5, psi, n, dt)
+    pp = part.psi_pad
+    p0 = 640
+    buckets = [(0, 96), (96, 640), (640, 900), (900, pp)]
+    h = O.Hyper(lr=1e-3, weight_decay=0.1, max_norm=0.05)
+    s3 = O.init_state(3, dt, part, master, m, v)
+    s1 = O.init_state(1, dt, part, master, m, v)
+    for k in range(3):
+        g = grads[k].copy()
+        if k == 1:
+            g[2, 700] = O.rne16(np.array([np.inf], np.float32), dt)[0]
+        s3, res, reps = O.step_stage3_persistent(s3, [g[:, a:b] for (a, b) in buckets], buckets, h, p0)
+        s1, res1 = O.step(s1, g, h)
+        assert res.overflow == res1.overflow == (k == 1)
+        assert np.array_equal(s3.master.view(np.uint32), s1.master.view(np.uint32))
+        assert np.array_equal(s3.params, s1.params[0])
+        assert len(reps) == n and all(np.array_equal(x, O.rne16(s3.master, dt)[p0:pp]) for x in reps)
+        assert len(res.gathered_fwd) == len(res.gathered_bwd) == 2
+        assert np.array_equal(res.gathered_bwd[1][3], res.gathered_fwd[1][0])
+    with pytest.raises(ValueError):
+        O.step_stage3_persistent(s3, [grads[0][:, 0:700], grads[0][:, 700:pp]], [(0, 700), (700, pp)], h, p0)
