@@ -697,6 +697,61 @@ def bench_schedule(w, buckets, steps, warmup, torch, S, Z, prefetch, graph):
     return ms
 
 
+def bench_persist(shapes, name, threshold, steps, warmup, torch, S, Z, graph):
+    """GPT-2-small ZeRO-3 steps with one bucket per tensor through
+    Zero3Schedule (prefetch on), with tensors below `threshold` kept resident
+    (param_persistence_threshold); eager or replayed from a CUDA graph.
+    Returns (ms per step, algorithmic bytes per step from the library's
+    counters, gathered buckets, all buckets, launches per step)."""
+    from zero_partitioned_mixed_gb300.buffers import RankBuffers
+    from zero_partitioned_mixed_gb300.persistence import persistent_layout, tensor_buckets
+    from zero_partitioned_mixed_gb300.schedule import Zero3Schedule
+    lay = persistent_layout(shapes, threshold)
+    w = S.Workload(name, lay.psi, 8, 3, "bf16", 1, grad_sigma=1e-3)
+    buf = RankBuffers(w.psi, w.n_ranks, 3, w.dtype, double_buffer=True)
+    P, N = buf.psi_pad, w.n_ranks
+    buckets = tensor_buckets(lay, P)
+    td = S.torch_dtype(w.dtype)
+    mv, mm, vv = buf.state(0)
+    S.draw_master(w, mv, w.psi)
+    S.draw_moments(w, mm, vv, w.psi)
+    buf.params[:P].copy_(mv.to(td))
+    lmax = max(b - a for a, b in buckets)
+    gbuf = torch.empty((N, (lmax + 7) // 8 * 8), dtype=td, device="cuda")
+    for r in range(N):
+        S.draw_grads(w, gbuf[r], lmax, 1, r, w.loss_scale)
+    rows = [gbuf[r] for r in range(N)]
+    buf.set_scaler(w.loss_scale, 0, 0)
+    hyp = Z.hyper(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay, w.max_norm, Z.ZERO_MODE_AUTO)
+    sched = Zero3Schedule(buf, buckets, prefetch=True, persistent_from=lay.persistent_from(P))
+    grads = lambda i: rows
+    for _ in range(warmup):
+        sched.step(hyp, grads)
+    b0 = _bytes_total(buf)
+    sched.step(hyp, grads)
+    bps = _bytes_total(buf) - b0
+    g = sched.capture(hyp, grads) if graph else None
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(steps):
+        if g is not None:
+            g.replay()
+        else:
+            sched.step(hyp, grads)
+    t1.record()
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / steps
+    ng = len(sched.gathered)
+    # two gathers per gathered bucket, one reduce-scatter per bucket, finalise +
+    # rollback, and the resident refresh
+    launches = 2 * ng + len(buckets) + 2 + (1 if sched.resident is not None else 0)
+    buf.close()
+    del gbuf, sched, g
+    torch.cuda.empty_cache()
+    return ms, bps, ng, len(buckets), launches, lay
+
+
 def run_other(args, ws, rank, local):
     import dataclasses
 
@@ -768,6 +823,23 @@ def run_other(args, ws, rank, local):
                                max(args.steps, 20), args.warmup, (6 * 32 + 30) * 637_952, toy.dtype,
                                {"stage": 3, "buckets": len(tb), "cuda_graph": graph,
                                 "l2": "L2-resident, back-to-back replays"}))
+    elif args.workload == "gpt2-zero3-persist":
+        # ZeRO-3 with one bucket per tensor: every tensor gathered (threshold 0)
+        # against the guide's param_persistence_threshold of 1e5 (biases and
+        # layer norms resident), eager and graph-replayed
+        shapes = S.gpt2_small_shapes()
+        for thr in (0, 100_000):
+            for graph in (False, True):
+                name = f"gpt2_small_zero3_n8_tensor_buckets_persist{thr}"
+                ms, bps, ng, nb, launches, lay = bench_persist(shapes, name, thr, args.steps, args.warmup,
+                                                               torch, S, Z, graph)
+                lines.append(_line(f"{name}_{'graph' if graph else 'eager'}", lay.psi / (ms * 1e-3), ms,
+                                   args.steps, args.warmup, bps, "bf16",
+                                   {"stage": 3, "param_persistence_threshold": thr, "buckets": nb,
+                                    "gathered_buckets": ng, "persistent_tensors": lay.n_persistent,
+                                    "persistent_elems": lay.psi_persistent, "cuda_graph": graph,
+                                    "launches_per_step": launches, "prefetch": True,
+                                    "l2": "inputs larger than L2"}))
     elif args.workload == "gpt2":
         w = S.GPT2
         ms, bps, st = bench_dense(w, 2, args.steps, args.warmup, torch, S, Z)
@@ -810,7 +882,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=4)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=["flat1.5b", "toy", "gpt2", "llama7b", "sweep", "zero2-buckets", "llama7b-zeropp",
-                                      "flat-zero3", "flat-zeropp", "schedule"], default="flat1.5b")
+                                      "flat-zero3", "flat-zeropp", "schedule", "gpt2-zero3-persist"],
+                    default="flat1.5b")
     ap.add_argument("--mode", choices=["auto", "staged"], default="auto",
                     help="flat workload: the step kernel (staged = inputs through shared memory by bulk copies)")
     ap.add_argument("--no-e2e", action="store_true")

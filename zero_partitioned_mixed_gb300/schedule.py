@@ -13,6 +13,13 @@ while the main stream runs the caller's work on bucket b (its forward or
 backward compute, then the reduce-scatter).  Events order every reuse of a
 buffer set.  All launches go through the C ABI; nothing here computes.
 
+With a persistence boundary p0 (param_persistence_threshold; layout in
+persistence.py) the region [p0, psi_pad) keeps N resident 16-bit copies:
+its buckets are not gathered in forward or backward, their gradients are
+reduce-scattered after the backward pass (a persistent tensor's gradient
+is complete only then), and one gather after the update refreshes the
+copies.
+
 A step whose buffers and hyper-parameters stay fixed can be captured once
 into a CUDA graph and replayed: the library's calls never synchronise or
 allocate after the first (warm-up) step, and its step count, loss scale
@@ -39,13 +46,30 @@ class Zero3Schedule:
     16-bit parameters (default: none).
     """
 
-    def __init__(self, buf: RankBuffers, buckets: Sequence[Tuple[int, int]], prefetch: bool = True):
+    def __init__(self, buf: RankBuffers, buckets: Sequence[Tuple[int, int]], prefetch: bool = True,
+                 persistent_from: Optional[int] = None):
         if buf.stage != 3:
             raise ValueError("Zero3Schedule needs a stage-3 RankBuffers")
         self.buf = buf
         self.buckets = list(buckets)
         self.prefetch = prefetch
-        lmax = max(b - a for a, b in self.buckets) if self.buckets else 0
+        P = buf.psi_pad
+        self.p0 = P if persistent_from is None else int(persistent_from)
+        if not 0 <= self.p0 <= P:
+            raise ValueError("persistent_from must lie in [0, psi_pad]")
+        for a, b in self.buckets:
+            if a < self.p0 < b:
+                raise ValueError("a bucket straddles the persistence boundary")
+        self.gathered = [i for i, (a, b) in enumerate(self.buckets) if b <= self.p0 and a < self.p0]
+        gset = set(self.gathered)
+        self.kept = [i for i in range(len(self.buckets)) if i not in gset]
+        self.resident: Optional[torch.Tensor] = None
+        self._fresh = False
+        if self.p0 < P:
+            lp = max(8, (P - self.p0 + 7) // 8 * 8)
+            self.resident = torch.empty((buf.n, lp), dtype=buf.params.dtype, device=buf.params.device)
+        sizes = [self.buckets[i][1] - self.buckets[i][0] for i in self.gathered]
+        lmax = max(sizes) if sizes else 0
         lpad = max(8, (lmax + 7) // 8 * 8)
         td = buf.params.dtype
         nsets = 2 if prefetch else 1
@@ -60,6 +84,7 @@ class Zero3Schedule:
     def _pass(self, order: Sequence[int], work: Optional[Callable], rs: Optional[Callable]) -> None:
         main = torch.cuda.current_stream()
         buf = self.buf
+        order = list(order)
         if not self.prefetch:
             for i in order:
                 a, b = self.buckets[i]
@@ -95,19 +120,36 @@ class Zero3Schedule:
             free[k % 2].record(main)
         # every gather was joined into the main stream through ready[k]
 
+    def resident_rows(self) -> List[torch.Tensor]:
+        """The N resident copies of [p0, psi_pad) (rank r's is row r)."""
+        if self.resident is None:
+            return []
+        return [self.resident[r] for r in range(self.buf.n)]
+
+    def refresh(self) -> None:
+        """Gather [p0, psi_pad) from the owners' shards into the resident copies."""
+        if self.resident is not None:
+            self.buf.gather(self.p0, self.buf.psi_pad, self.resident_rows(), torch.cuda.current_stream())
+            self._fresh = True
+
     def step(self, hyp, grad_rows: Callable[[int], List[torch.Tensor]],
              forward: Optional[Callable] = None, backward: Optional[Callable] = None) -> None:
-        """Forward gathers, backward gathers + reduce-scatters, then zero_step."""
+        """Forward gathers, backward gathers + reduce-scatters, the persistent
+        buckets' reduce-scatters, zero_step, then the resident refresh."""
         buf = self.buf
-        nb = len(self.buckets)
-        self._pass(range(nb), forward, None)
+        if self.resident is not None and not self._fresh:
+            self.refresh()
+        self._pass(self.gathered, forward, None)
 
         def rs(i):
             a, b = self.buckets[i]
             buf.reduce_scatter(a, b, grad_rows(i), hyp)
 
-        self._pass(range(nb - 1, -1, -1), backward, rs)
+        self._pass(self.gathered[::-1], backward, rs)
+        for i in self.kept:
+            rs(i)
         buf.step(hyp)
+        self.refresh()
 
     def capture(self, hyp, grad_rows, forward=None, backward=None) -> torch.cuda.CUDAGraph:
         """Capture one step into a CUDA graph (call after one eager warm-up step)."""
