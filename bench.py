@@ -802,9 +802,13 @@ def run_other(args, ws, rank, local):
             ms, bps, st = bench_stage3(w, buckets, args.steps, args.warmup, torch, S, Z)
             parts = bench_stage3.parts
         else:
-            ms, bps, st, _, _, parts = bench_stage3_zeropp(w, buckets, args.steps, args.warmup, torch, S, Z, 8)
-        lines.append(_line(w.name + ("_zeropp" if args.workload == "flat-zeropp" else ""), psi / (ms * 1e-3), ms,
-                           args.steps, args.warmup, bps, "bf16", {"stage": 3, "buckets": len(buckets), **parts}))
+            ms, bps, st, _, _, parts = bench_stage3_zeropp(w, buckets, args.steps, args.warmup, torch, S, Z,
+                                                           args.rs_bits)
+        extra = {"stage": 3, "buckets": len(buckets), **parts}
+        if args.workload == "flat-zeropp":
+            extra.update({"gather": "int8 blocks of 256", "reduce_scatter": f"int{args.rs_bits} blocks of 256"})
+        lines.append(_line(w.name + (f"_zeropp_int{args.rs_bits}rs" if args.workload == "flat-zeropp" else ""),
+                           psi / (ms * 1e-3), ms, args.steps, args.warmup, bps, "bf16", extra))
     elif args.workload == "schedule":
         # ZeRO-3 step scheduling: sequential vs one-ahead prefetch on a side
         # stream (Llama-7B), and eager vs CUDA-graph replay (toy buffer, launch-bound)
@@ -886,6 +890,8 @@ def main(argv=None):
                     default="flat1.5b")
     ap.add_argument("--mode", choices=["auto", "staged"], default="auto",
                     help="flat workload: the step kernel (staged = inputs through shared memory by bulk copies)")
+    ap.add_argument("--rs-bits", type=int, choices=[8, 4], default=8,
+                    help="flat-zeropp: code width of the quantized gradient reduce-scatter")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--psi", type=int, default=None, help="override psi of the flat workload (profiling)")
