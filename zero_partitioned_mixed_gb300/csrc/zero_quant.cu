@@ -107,16 +107,21 @@ __device__ __forceinline__ void block_scale(const float (&x)[8], int nv, float& 
     inv = __fdiv_rn(top, range);
 }
 
+// Eight byte codes (each < 256) packed little-endian into 8 bytes.
+__device__ __forceinline__ uint2 pack_u8x8(const uint32_t (&q)[8]) {
+    uint2 w;
+    w.x = __byte_perm(__byte_perm(q[0], q[1], 0x0040u), __byte_perm(q[2], q[3], 0x0040u), 0x5410u);
+    w.y = __byte_perm(__byte_perm(q[4], q[5], 0x0040u), __byte_perm(q[6], q[7], 0x0040u), 0x5410u);
+    return w;
+}
+
 // Store a lane's 8 codes at element e0 of a code buffer.
 template <int BITS>
 __device__ __forceinline__ void store_codes(void* codes, uint64_t e0, int nv, const uint32_t (&q)[8]) {
     if (BITS == 8) {
         unsigned char* c = static_cast<unsigned char*>(codes) + e0;
         if (nv == 8) {
-            uint2 w;
-            w.x = q[0] | (q[1] << 8) | (q[2] << 16) | (q[3] << 24);
-            w.y = q[4] | (q[5] << 8) | (q[6] << 16) | (q[7] << 24);
-            __stcs(reinterpret_cast<uint2*>(c), w);
+            __stcs(reinterpret_cast<uint2*>(c), pack_u8x8(q));
         } else {
             for (int k = 0; k < nv; ++k) c[k] = static_cast<unsigned char>(q[k]);
         }
@@ -287,10 +292,8 @@ __global__ void __launch_bounds__(kThreads) k_quantize(const __grid_constant__ A
                                     [&](uint64_t blk, uint64_t e0, int nv, const uint32_t (&q)[8], float scale,
                                         float lo) {
                                         if (nv > 0) store_codes<BITS>(a.params[0], e0, nv, q);
-                                        if (lane == 0) {
-                                            a.qdst[0][2 * blk] = scale;
-                                            a.qdst[0][2 * blk + 1] = lo;
-                                        }
+                                        if (lane == 0)
+                                            *reinterpret_cast<float2*>(a.qdst[0] + 2 * blk) = make_float2(scale, lo);
                                     });
     }
 }
@@ -306,13 +309,17 @@ __global__ void __launch_bounds__(kThreads) k_gather_q8(const __grid_constant__ 
         quantize_blocks_u<DT, 8, kQUnrollGather>(src, a.count, blk0, nb, a.qvec != 0, lane,
                                  [&](uint64_t blk, uint64_t e0, int nv, const uint32_t (&q)[8], float scale,
                                      float lo) {
-                                     for (int r = 0; r < a.n_ranks; ++r) {
-                                         if (nv > 0) store_codes<8>(a.params[r], e0, nv, q);
-                                         if (lane == 0) {
-                                             a.qdst[r][2 * blk] = scale;
-                                             a.qdst[r][2 * blk + 1] = lo;
-                                         }
+                                     // the same 8 bytes to every rank, packed once
+                                     if (nv == 8) {
+                                         const uint2 w = pack_u8x8(q);
+                                         for (int r = 0; r < a.n_ranks; ++r)
+                                             __stcs(reinterpret_cast<uint2*>(static_cast<unsigned char*>(a.params[r]) + e0), w);
+                                     } else if (nv > 0) {
+                                         for (int r = 0; r < a.n_ranks; ++r) store_codes<8>(a.params[r], e0, nv, q);
                                      }
+                                     // lane r writes rank r's {scale, lo}
+                                     for (int r = lane; r < a.n_ranks; r += 32)
+                                         *reinterpret_cast<float2*>(a.qdst[r] + 2 * blk) = make_float2(scale, lo);
                                  });
     }
 }
@@ -403,7 +410,7 @@ __device__ __forceinline__ void reduce_group_q(const Args& a, uint64_t j, const 
 // ZeRO-3 reduce-scatter of bucket [base, base+count) from the N ranks'
 // quantized gradients (qgZ): as k_rs, with the ranks' values dequantized.
 template <int DT, class IO, int BITS, bool SPEC>
-__global__ void __launch_bounds__(kThreads) k_rs_q(const __grid_constant__ Args a) {
+__global__ void __launch_bounds__(kThreads, BITS == 4 ? 4 : 3) k_rs_q(const __grid_constant__ Args a) {
     constexpr int W = IO::W;
     __shared__ Pro pro;
     prologue_reduce(a, pro, SPEC);
