@@ -58,7 +58,7 @@ typedef enum {
     ZERO_EINVAL = 1,    /* bad argument: null/misaligned pointer, range, stage/mode mismatch */
     ZERO_ENOMEM = 2,    /* workspace allocation failed */
     ZERO_ECUDA = 3,     /* a CUDA runtime call or kernel launch failed */
-    ZERO_ETIMEOUT = 4,  /* reserved: no call waits on the device */
+    ZERO_ETIMEOUT = 4,  /* zero_get_status: a bounded wait inside a kernel gave up (staged step) */
     ZERO_ESTATE = 5     /* call sequence wrong (e.g. stage-3 step before every bucket was reduced) */
 } zero_status_t;
 
@@ -74,7 +74,8 @@ typedef enum {
                                         async copies (stages 1/2 one-shot step; N <= 19, i.e. two
                                         stages of N*4 KiB + 24 KiB fit in 200 KiB of shared
                                         memory; psi_pad a multiple of 8; fp32 state 32-byte
-                                        aligned; otherwise ZERO_EINVAL) */
+                                        aligned; grads and master/m/v in device memory,
+                                        not host memory; otherwise ZERO_EINVAL) */
 } zero_mode_t;
 
 /* zero_init_partition flags */
@@ -91,10 +92,12 @@ typedef struct {
 } zero_hyper_t;
 
 typedef struct {
-    int32_t overflow;       /* last step saw a non-finite averaged gradient (step skipped) */
+    int32_t overflow;       /* last step skipped: a non-finite averaged gradient, or (error != 0)
+                               a kernel wait that gave up */
     int32_t applied;        /* last step updated the state */
     int32_t state_slot;     /* live slot (0/1) of double-buffered master/m/v; 0 otherwise */
-    int32_t error;          /* device-side error word, 0 = none */
+    int32_t error;          /* device-side error word, 0 = none; 1 = a bounded wait of the staged
+                               step gave up.  Stays set until zero_set_scaler. */
     double grad_norm;       /* L2 norm of the averaged unscaled gradient of the last step */
     double clip_coef;       /* fp32 factor applied to the gradient (1.0 when not clipping) */
     float loss_scale;       /* current loss scale, after any halving */
@@ -293,9 +296,24 @@ ZERO_API int zero_reduce_scatter_bucket_q(zero_handle_t h, uint64_t a, uint64_t 
 /*
  * zero_get_status -- a11: copy the device status of the last step to the
  * host struct *out (host pointer).  Synchronises the given stream.
- * Errors: EINVAL, ECUDA.
+ * Errors: EINVAL, ECUDA; ETIMEOUT (with *out filled) while the device error
+ * word is set, i.e. after a staged step whose bounded wait gave up.
  */
 ZERO_API int zero_get_status(zero_handle_t h, void* stream, zero_result_t* out);
+
+/*
+ * zero_debug_hold_staged -- test hook for the failure path of
+ * ZERO_MODE_SPECULATIVE_STAGED.  In the next staged zero_step on this handle
+ * (one-shot), CTA 0 stops issuing its bulk copies at its tile `tile` (its
+ * tiles counted from 0), so its compute warps' bounded waits run out (about
+ * 2 s) instead of receiving data.  No access leaves its buffers and every
+ * wait ends.  That step is then skipped (overflow = 1, master/m/v and the
+ * replicas unchanged, loss scale kept), the error word is set and
+ * zero_get_status returns ZERO_ETIMEOUT until zero_set_scaler clears it.
+ * tile < 0 clears a pending hold; a tile past CTA 0's last has no effect.
+ * Errors: EINVAL (NULL handle).
+ */
+ZERO_API int zero_debug_hold_staged(zero_handle_t h, int64_t tile);
 
 /*
  * zero_bytes_moved -- D4/D5 accounting and algorithmic HBM bytes.

@@ -14,6 +14,7 @@ ZERO_MODE_SPECULATIVE_STAGED = 4
 ZERO_F_DOUBLE_BUFFER = 1
 ZERO_MAX_RANKS = 64
 
+ZERO_ETIMEOUT = 4
 STATUS_NAMES = {0: "ZERO_OK", 1: "ZERO_EINVAL", 2: "ZERO_ENOMEM", 3: "ZERO_ECUDA",
                 4: "ZERO_ETIMEOUT", 5: "ZERO_ESTATE"}
 
@@ -22,7 +23,7 @@ EXPORTS = (
     "zero_gather_bucket", "zero_reduce_scatter_bucket", "zero_get_status",
     "zero_bytes_moved", "zero_last_error", "zero_destroy", "zero_step_noalloc",
     "zero_reduce_scatter_bucket_replicas", "zero_quantize_blocks", "zero_dequantize_blocks",
-    "zero_gather_bucket_q8", "zero_reduce_scatter_bucket_q",
+    "zero_gather_bucket_q8", "zero_reduce_scatter_bucket_q", "zero_debug_hold_staged",
 )
 ZERO_Q_BLOCK = 256
 
@@ -90,6 +91,7 @@ def load_library():
     lib.zero_reduce_scatter_bucket_q.argtypes = [P, U64, U64, I32, C.POINTER(P), C.POINTER(P), P, P, P, P,
                                                  C.POINTER(Hyper), P]
     lib.zero_get_status.argtypes = [P, P, C.POINTER(Result)]
+    lib.zero_debug_hold_staged.argtypes = [P, C.c_int64]
     lib.zero_bytes_moved.argtypes = [P, C.POINTER(Bytes)]
     lib.zero_last_error.argtypes = [P]
     lib.zero_last_error.restype = C.c_char_p
@@ -227,9 +229,22 @@ def zero_reduce_scatter_bucket_q(h, a: int, b: int, bits: int, codes, scales, ma
 
 
 def zero_get_status(h, stream=None) -> dict:
+    """The last step's status.  ZERO_ETIMEOUT raises ZeroError carrying the
+    filled status as ``.result``."""
     r = Result()
-    _check(load_library().zero_get_status(h, _stream(stream), C.byref(r)), h)
-    return {f: getattr(r, f) for f, _ in Result._fields_ if f != "reserved"}
+    rc = load_library().zero_get_status(h, _stream(stream), C.byref(r))
+    out = {f: getattr(r, f) for f, _ in Result._fields_ if f != "reserved"}
+    if rc == ZERO_ETIMEOUT:
+        msg = load_library().zero_last_error(h)
+        err = ZeroError(rc, msg.decode() if msg else "")
+        err.result = out
+        raise err
+    _check(rc, h)
+    return out
+
+
+def zero_debug_hold_staged(h, tile: int) -> None:
+    _check(load_library().zero_debug_hold_staged(h, int(tile)), h)
 
 
 def zero_bytes_moved(h) -> dict:

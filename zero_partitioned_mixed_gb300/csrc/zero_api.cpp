@@ -38,6 +38,7 @@ struct zero_handle {
     zero_hyper_t rs_hyper{};
     // accounting
     uint64_t last_r = 0, last_w = 0, tot_r = 0, tot_w = 0;
+    uint64_t hold_tile1 = 0;   // zero_debug_hold_staged, for the next staged step
     std::string err;
 };
 
@@ -455,7 +456,24 @@ int zero_step(zero_handle_t h, const void* const* grads, void* const* params, fl
         if (mode == ZERO_MODE_SPECULATIVE_STAGED) {
             if (any && pick_vec(vec8, a) != zg::Vec::k8s32)
                 return fail(h, ZERO_EINVAL, "staged mode needs 32-byte aligned master/m/v");
-            cudaError_t e = zg::launch_step_tma(h->dtype, a, s);
+            // the bulk copies read the inputs as device global memory only
+            const void* ins[zg::kMaxRanks + 3];
+            int k = 0;
+            for (int r = 0; r < h->n; ++r) ins[k++] = a.grads[r];
+            ins[k++] = a.master;
+            ins[k++] = a.m;
+            ins[k++] = a.v;
+            for (int i = 0; i < k; ++i) {
+                cudaPointerAttributes pa;
+                if (cudaPointerGetAttributes(&pa, ins[i]) != cudaSuccess || pa.type != cudaMemoryTypeDevice) {
+                    cudaGetLastError();
+                    return fail(h, ZERO_EINVAL, "staged mode reads grads and master/m/v from device memory only");
+                }
+            }
+            zg::Args at = a;
+            at.hold_tile1 = h->hold_tile1;
+            h->hold_tile1 = 0;
+            cudaError_t e = zg::launch_step_tma(h->dtype, at, s);
             if (e != cudaSuccess) return cuda_fail(h, e, "staged step");
         } else if ((rc = launch(h, zg::Kind::kStepSpec, vec8, a, s, "step"))) {
             return rc;
@@ -631,6 +649,13 @@ int zero_get_status(zero_handle_t h, void* stream, zero_result_t* out) {
     out->reserved = 0.0f;
     out->steps_applied = st.t;
     out->steps_skipped = st.skipped;
+    if (st.error) return fail(h, ZERO_ETIMEOUT, "a bounded device wait gave up; the step was skipped");
+    return ZERO_OK;
+}
+
+int zero_debug_hold_staged(zero_handle_t h, int64_t tile) {
+    if (!h) return fail(nullptr, ZERO_EINVAL, "handle is NULL");
+    h->hold_tile1 = tile < 0 ? 0 : static_cast<uint64_t>(tile) + 1;
     return ZERO_OK;
 }
 

@@ -78,6 +78,9 @@ struct Args {
     float* qdst[kMaxRanks];        // per-rank {scale, lo} pairs of quantized outputs
     int qbits;                     // 8 or 4
     int qvec;                      // 1: 16-bit source 16-byte aligned at every block start
+    // staged step (zero_tma.cu): 1 + the tile at which CTA 0 stops issuing
+    // its copies, so that its bounded waits run out (0: never)
+    uint64_t hold_tile1;
 };
 
 enum class Kind : int {

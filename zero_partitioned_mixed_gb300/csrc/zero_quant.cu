@@ -209,16 +209,6 @@ __device__ __forceinline__ f2 f2dequant(f2 q_biased, f2 two23, f2 sc, float lo) 
     return f2pack(__fadd_rn(lo, p0), __fadd_rn(lo, p1));
 }
 
-__device__ __forceinline__ f2 f2sub(f2 a, f2 b) {
-    f2 r;
-    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ f2 f2mul(f2 a, f2 b) {
-    f2 r;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
 
 // A lane's 8 codes at element e0 as four pairs of 2^23-biased floats
 // (0x4B000000 | code): subtracting 2^23 gives the codes exactly.

@@ -14,10 +14,11 @@
 //
 // Warp 8 issues the copies; warps 0-7 compute.
 //
-// Every mbarrier wait is bounded (iterations and %globaltimer).  A wait
-// that gives up sets the device error word, marks the step as overflowed
-// (so nothing is committed and the replicas are rolled back by k_fixup),
-// waits -- again bounded -- for the copies it issued, and leaves.
+// Every mbarrier wait is bounded (2^24 polls and 2 s of %globaltimer).  A
+// wait that gives up makes its CTA stop, wait -- again bounded -- for the
+// copies it issued, set the device error word and flag the step as aborted:
+// nothing is committed, the replicas are restored by k_fixup, and the loss
+// scale is kept.
 
 #include "zero_device.cuh"
 
@@ -70,6 +71,39 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
                  : "memory");
 }
 
+// In the last block: the fixed-order sum of the blocks' partials (as
+// gather_partials) and the OR of their flag bits.
+__device__ void gather_flag_bits(const double* slot_norm, const int32_t* slot_flag, int count, double& q,
+                                 int& bits) {
+    __shared__ int s_bits;
+    if (threadIdx.x == 0) s_bits = 0;
+    __threadfence();
+    __syncthreads();
+    double s = 0.0;
+    int f = 0;
+    for (int b = threadIdx.x; b < count; b += blockDim.x) {
+        s = __dadd_rn(s, *reinterpret_cast<const volatile double*>(slot_norm + b));
+        f |= *reinterpret_cast<const volatile int32_t*>(slot_flag + b);
+    }
+    q = block_sum(s);
+    if (f) atomicOr(&s_bits, f);
+    __syncthreads();
+    bits = s_bits;
+}
+
+// A wait gave up: the step is skipped like an overflowed one (state
+// untouched, replicas restored by the fixup kernel, t not advanced) but the
+// loss scale is kept; the device error word stays set.
+__device__ void status_abort(DevStatus* st, double q) {
+    st->overflow = 1;
+    st->applied = 0;
+    st->norm = __dsqrt_rn(q);
+    st->clip_coef = 1.0;
+    st->clip_f = 1.0f;
+    st->use_clip = 0;
+    st->skipped += 1;
+}
+
 struct TmaLayout {
     int stages;
     uint32_t stage_bytes;   // N*4096 + 3*8192
@@ -111,7 +145,7 @@ __global__ void __launch_bounds__(kTmaThreads, 2) k_step_tma(const __grid_consta
     volatile int* vabort = &abort_flag;
 
     double acc = 0.0;
-    int bad = 0;
+    int bad = 0, aborted = 0;
     if (threadIdx.x >= kThreads) {
         // producer warp: lane 0 fills stage k % stages with tile k once the
         // consumers have released its previous fill
@@ -119,6 +153,7 @@ __global__ void __launch_bounds__(kTmaThreads, 2) k_step_tma(const __grid_consta
             uint64_t k = 0;
             for (; k < my_tiles; ++k) {
                 if (*vabort) break;
+                if (blockIdx.x == 0 && k + 1 == a.hold_tile1) break;   // held: the consumers' waits run out
                 const int s = static_cast<int>(k % lay.stages);
                 if (k >= static_cast<uint64_t>(lay.stages) &&
                     !mbar_wait(empty0 + 8 * s, static_cast<uint32_t>((k / lay.stages - 1) & 1))) {
@@ -207,7 +242,7 @@ __global__ void __launch_bounds__(kTmaThreads, 2) k_step_tma(const __grid_consta
             }
             atomicExch(&a.ws.status->error, 1);
         }
-        bad = 1;
+        aborted = 1;
     }
     // elements past the last full tile, element groups of 8 with plain loads
     {
@@ -238,14 +273,16 @@ __global__ void __launch_bounds__(kTmaThreads, 2) k_step_tma(const __grid_consta
         }
     }
     const double blk = block_sum(acc);
-    const int flag = __syncthreads_or(bad);
+    // bit 0: a non-finite gradient; bit 1: this CTA gave up a wait
+    const int flag = (__syncthreads_or(bad) ? 1 : 0) | (__syncthreads_or(aborted) ? 2 : 0);
     if (publish(a, blk, flag, a.ws.partials, a.ws.flags)) {
         double qsum;
         int f;
-        gather_partials(a.ws.partials, a.ws.flags, gridDim.x, qsum, f);
+        gather_flag_bits(a.ws.partials, a.ws.flags, gridDim.x, qsum, f);
         if (threadIdx.x == 0) {
             DevStatus* st = a.ws.status;
-            if (f) status_skip(st, qsum);
+            if (f & 2) status_abort(st, qsum);
+            else if (f) status_skip(st, qsum);
             else status_decide_spec(st, qsum, a.hyper);
             st->ticket = 0u;
         }
