@@ -98,7 +98,9 @@ typedef struct {
     int32_t state_slot;     /* live slot (0/1) of double-buffered master/m/v; 0 otherwise */
     int32_t error;          /* device-side error word, 0 = none; 1 = a bounded wait of the staged
                                step gave up.  Stays set until zero_set_scaler. */
-    double grad_norm;       /* L2 norm of the averaged unscaled gradient of the last step */
+    double grad_norm;       /* L2 norm of the averaged unscaled gradient of the last step; not
+                               meaningful when overflow = 1 (a one-pass step stops at the
+                               first non-finite value it finds) */
     double clip_coef;       /* fp32 factor applied to the gradient (1.0 when not clipping) */
     float loss_scale;       /* current loss scale, after any halving */
     float reserved;

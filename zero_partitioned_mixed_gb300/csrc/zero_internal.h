@@ -43,7 +43,8 @@ struct DevStatus {
     int32_t redo;       // speculative step whose norm needs clipping: redo it from the old slot
     StepScalars sc;     // coefficients of the step being applied (two-pass)
     uint32_t ticket;    // last-block counter; returns to 0 after every launch
-    uint32_t pad1;
+    uint32_t stop;      // one-pass step: a non-finite gradient was seen, the pass may stop
+                        // (the step is skipped); returns to 0 when the pass finalises
 };
 
 struct Workspace {
@@ -72,7 +73,6 @@ struct Args {
     HyperDev hyper;
     Workspace ws;
     int bucket_index;
-    int use_div;         // unused: the kernels decide divide vs multiply on the device
     // ZeRO++ block-quantized exchange (zero_quant.cu)
     const float* qsrc[kMaxRanks];  // per-rank {scale, lo} pairs of quantized inputs
     float* qdst[kMaxRanks];        // per-rank {scale, lo} pairs of quantized outputs

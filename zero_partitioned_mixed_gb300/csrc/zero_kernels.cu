@@ -43,7 +43,15 @@ __global__ void __launch_bounds__(kThreads) k_step_spec(const __grid_constant__ 
     const uint64_t nvec = a.count / W;
     double acc = 0.0;
     int bad = 0;
-    for (uint64_t vi = thread_id(); vi < nvec; vi += grid_threads()) {
+    // Overflow is the existence of one non-finite averaged gradient, and an
+    // overflowed step changes no state (the fixup kernel restores every
+    // replica from the old master).  So the thread that finds one raises
+    // `stop` and every thread leaves the pass at its next iteration; the
+    // flag is read one iteration ahead, off the critical path.
+    volatile uint32_t* stop = &a.ws.status->stop;
+    uint32_t seen = 0;
+    for (uint64_t vi = thread_id(); vi < nvec && !seen; vi += grid_threads()) {
+        const uint32_t seen_next = *stop;
         const uint64_t gi = vi * W;
         float g[W], p[W], m[W], v[W];
         reduce_group<DT, IO>(a, gi, pro, g);
@@ -52,6 +60,11 @@ __global__ void __launch_bounds__(kThreads) k_step_spec(const __grid_constant__ 
         IO::ldf(a.v + src, gi, v);
         const int valid = valid_count(gi, W, a.psi);
         norm_group<W>(g, valid, acc, bad);
+        if (bad) {
+            *stop = 1u;
+            break;
+        }
+        seen = seen_next;
         uint32_t q[W];
 #pragma unroll
         for (int k = 0; k < W; ++k) {
@@ -77,6 +90,7 @@ __global__ void __launch_bounds__(kThreads) k_step_spec(const __grid_constant__ 
             DevStatus* st = a.ws.status;
             if (f) status_skip(st, qsum);
             else status_decide_spec(st, qsum, a.hyper);
+            st->stop = 0u;
             st->ticket = 0u;
         }
     }
@@ -396,6 +410,7 @@ __global__ void k_set_scaler(DevStatus* st, float loss_scale, int64_t t, int32_t
     st->error = 0;
     st->redo = 0;
     st->ticket = 0u;
+    st->stop = 0u;
 }
 
 // ------------------------------------------------------------------ launch
