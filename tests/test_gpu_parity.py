@@ -396,3 +396,58 @@ def test_checkpoint_resume_is_bit_identical(stage, tmp_path):
         assert torch.equal(x.view(torch.int32), y.view(torch.int32))
     assert torch.equal(a.params.view(torch.int16), b.params.view(torch.int16))
     a.close(); b.close()
+
+
+@pytest.mark.parametrize("stage", [1, 2])
+@pytest.mark.parametrize("where", [5, 2_600_000, 7_999_990])
+def test_overflow_stops_the_pass_early(stage, where):
+    # 8M elements over 4 ranks is about 8.6 waves of the persistent grid: an
+    # inf near the start, the middle or the end stops the one-pass step there.
+    # The rollback then restores only what the pass may have written, and
+    # every element of state and replicas must still match the oracle.
+    st = run_case(8_000_011, 4, stage, "fp16", steps=3, mode=3, double_buffer=True, loss_scale=1024.0,
+                  sigma=1e-3, inject=[(1, 2, where, INF)])
+    st.check()
+    assert st.mismatches == 0, st
+
+
+@pytest.mark.parametrize("psi,bucket", [(6_000_001, 1_000_000), (40_000_003, 36_000_000)])
+@pytest.mark.parametrize("stage,mode", [(1, 3), (2, 1), (3, 0)])
+def test_norm_is_bitwise_deterministic(stage, mode, psi, bucket):
+    # CTAs take chunks of work in whatever order they reach the counter, but
+    # norm partials are formed per chunk, then per group of chunks (launches
+    # of more than 4096 chunks: the 40M case), in a fixed order: repeated
+    # runs give the same bits.
+    import struct
+    from zero_partitioned_mixed_gb300 import _binding as B
+    from zero_partitioned_mixed_gb300.buffers import RankBuffers
+    n = 8
+    g = torch.Generator(device="cuda")
+    g.manual_seed(23)
+    width = (psi + 8 * n - 1) // (8 * n) * (8 * n)
+    grads = (torch.randn((n, width), generator=g, device="cuda") * 1e-2).to(torch.bfloat16)
+    master0 = torch.randn(psi, generator=g, device="cuda") * 0.02
+    runs = []
+    for _ in range(3):
+        buf = RankBuffers(psi, n, stage, "bf16", double_buffer=(mode in (0, 3)))
+        P = buf.psi_pad
+        mv, _, _ = buf.state(0)
+        mv[:psi].copy_(master0)
+        if stage == 3:
+            buf.params[:P].copy_(mv.to(torch.bfloat16))
+        else:
+            buf.params[:, :P].copy_(mv.to(torch.bfloat16).unsqueeze(0).expand(n, P))
+        hyp = B.hyper(max_norm=1e6, mode=mode)
+        for _ in range(2):
+            if stage == 3:
+                for a0 in range(0, P, bucket):
+                    b0 = min(P, a0 + bucket)
+                    buf.reduce_scatter(a0, b0, [grads[r, a0:b0] for r in range(n)], hyp)
+                buf.step(hyp)
+            else:
+                buf.step(hyp, [grads[r, :P] for r in range(n)])
+        s = buf.status()
+        m, _, _ = buf.state(s["state_slot"])
+        runs.append((struct.pack("<d", s["grad_norm"]), m.cpu().numpy().tobytes()))
+        buf.close()
+    assert runs[0] == runs[1] == runs[2]

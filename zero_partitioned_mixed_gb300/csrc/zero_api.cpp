@@ -39,6 +39,7 @@ struct zero_handle {
     // accounting
     uint64_t last_r = 0, last_w = 0, tot_r = 0, tot_w = 0;
     uint64_t hold_tile1 = 0;   // zero_debug_hold_staged, for the next staged step
+    uint64_t launch_seq = 0;   // chunked launches: counter slot = launch_seq % kCtrSlots
     std::string err;
 };
 
@@ -152,7 +153,11 @@ zg::Vec pick_vec(bool vec8, const zg::Args& a) {
 }
 
 int launch(zero_handle* h, zg::Kind kind, bool vec8, const zg::Args& a, cudaStream_t s, const char* what) {
-    cudaError_t e = zg::launch(kind, h->dtype, pick_vec(vec8, a), a, s, nullptr);
+    // each launch its own chunk counter: a gather on one stream may overlap
+    // a reduce-scatter on another
+    zg::Args b = a;
+    b.ctr_slot = static_cast<int>(h->launch_seq++ % zg::kCtrSlots);
+    cudaError_t e = zg::launch(kind, h->dtype, pick_vec(vec8, b), b, s, nullptr);
     if (e != cudaSuccess) return cuda_fail(h, e, what);
     return ZERO_OK;
 }
@@ -307,10 +312,18 @@ int zero_init_partition(uint64_t psi, int n_ranks, int stage, int dtype, int ali
         delete h;
         return cuda_fail(nullptr, e, "cudaGetDevice");
     }
-    // one block: status | partials | flags | bucket partials | bucket flags
+    // one block: status | partials | bucket partials | flags | bucket flags |
+    // chunk counters | group tickets | chunk partials | group partials
     const size_t st_bytes = (sizeof(zg::DevStatus) + 255) / 256 * 256;
-    const size_t bytes = st_bytes + zg::kMaxBlocks * (sizeof(double) + sizeof(int32_t)) +
-                         zg::kMaxBuckets * (sizeof(double) + sizeof(int32_t));
+    auto r256 = [](size_t x) { return (x + 255) / 256 * 256; };
+    const size_t fixed = r256(zg::kMaxBlocks * (sizeof(double) + sizeof(int32_t)) +
+                              zg::kMaxBuckets * (sizeof(double) + sizeof(int32_t)));
+    const uint64_t nch = zg::max_chunks(h->psi_pad), ngr = zg::max_groups(h->psi_pad);
+    const size_t ctr_bytes = r256(zg::kCtrSlots * sizeof(zg::ChunkCtr));
+    const size_t tk_bytes = r256(ngr * sizeof(uint32_t));
+    const size_t cp_bytes = r256(nch * sizeof(double));
+    const size_t gp_bytes = r256(ngr * sizeof(double));
+    const size_t bytes = st_bytes + fixed + ctr_bytes + tk_bytes + cp_bytes + gp_bytes;
     e = cudaMalloc(&h->ws_block, bytes);
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -324,6 +337,11 @@ int zero_init_partition(uint64_t psi, int n_ranks, int stage, int dtype, int ali
     h->ws.flags = reinterpret_cast<int32_t*>(h->ws.bucket_norm + zg::kMaxBuckets);
     h->ws.bucket_flag = h->ws.flags + zg::kMaxBlocks;
     h->ws.ghat = nullptr;
+    char* sched = base + st_bytes + fixed;
+    h->ws.ctrs = reinterpret_cast<zg::ChunkCtr*>(sched);
+    h->ws.group_ticket = reinterpret_cast<uint32_t*>(sched + ctr_bytes);
+    h->ws.chunk_part = reinterpret_cast<double*>(sched + ctr_bytes + tk_bytes);
+    h->ws.group_part = reinterpret_cast<double*>(sched + ctr_bytes + tk_bytes + cp_bytes);
     e = cudaMemset(h->ws_block, 0, bytes);
     if (e == cudaSuccess) e = zg::launch_set_scaler(h->ws.status, 1.0f, 0, 0, nullptr);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();

@@ -340,6 +340,138 @@ __device__ __forceinline__ uint64_t thread_id() {
     return static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
 }
 
+// ------------------------------------------------------------ dynamic chunks
+// The CTAs of a persistent grid do not progress at one rate: with a static
+// grid-stride assignment the fast ones finish early and the launch ends in a
+// tail where only the slow ones stream (about 7 % of the step on a GB300).
+// Chunked kernels instead take chunk after chunk from their launch's counter;
+// thread 0 fetches the next index while the block works on the current one.
+// With U = chunk_u(nvec), thread t of whichever CTA takes chunk c handles the
+// vectors c*U*kThreads + u*kThreads + t, u < U.
+class Chunks {
+  public:
+    // A CTA's first chunk is its own index (the grid has no more CTAs than
+    // chunks); each chunk it works on, thread 0 grabs the next from the
+    // counter, which hands out gridDim.x, gridDim.x + 1, ...  So a launch
+    // makes exactly nchunks grabs, and the CTA that makes grab nchunks - 1
+    // (its failing one, like every CTA's last) resets the counter: every
+    // other grab of the launch came before it.
+    __device__ Chunks(ChunkCtr* ctr, unsigned long long* s2, uint64_t nchunks)
+        : ctr_(ctr), s_(s2), n_(nchunks), par_(0), first_(true) {}
+    __device__ uint64_t current() const { return first_ ? static_cast<uint64_t>(blockIdx.x) : s_[par_]; }
+    __device__ int parity() const { return par_; }
+    // thread 0, at the start of each chunk's work (nothing to grab when
+    // every CTA has at most its own chunk)
+    __device__ void prefetch() {
+        if (threadIdx.x == 0) {
+            if (n_ <= gridDim.x) {
+                s_[par_ ^ 1] = ~0ull;
+                return;
+            }
+            const unsigned long long v = atomicAdd(&ctr_->next, 1ull);
+            if (v + 1 == n_) atomicExch(&ctr_->next, 0ull);
+            s_[par_ ^ 1] = static_cast<unsigned long long>(gridDim.x) + v;
+        }
+    }
+    // after the block barrier that closes a chunk
+    __device__ void advance() {
+        par_ ^= 1;
+        first_ = false;
+    }
+
+  private:
+    ChunkCtr* ctr_;
+    unsigned long long* s_;
+    uint64_t n_;
+    int par_;
+    bool first_;
+};
+
+// vector u of this thread in chunk c (chunks of `len` = U * kThreads vectors)
+__device__ __forceinline__ uint64_t chunk_vec(uint64_t c, uint64_t len, int u) {
+    return c * len + static_cast<uint64_t>(u) * kThreads + threadIdx.x;
+}
+
+__device__ __forceinline__ uint64_t group_count(uint64_t nchunks) { return (nchunks + kGroup - 1) / kGroup; }
+
+// Fixed-order warp sum of doubles (lane 0 holds the result).
+__device__ __forceinline__ double warp_dsum(double x) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) x = __dadd_rn(x, __shfl_down_sync(0xFFFFFFFFu, x, off));
+    return x;
+}
+
+// Warp 0, after the barrier that closes chunk c: the chunk's norm partial is
+// the sum, in warp order, of the warps' sums wp[] (each a fixed warp tree over
+// the lanes' accumulators, written before the barrier).  The CTA that
+// completes a group of kGroup chunks sums the group with a fixed tree.  None
+// of this depends on which CTA took which chunk.
+__device__ void commit_chunk(const Workspace& ws, uint64_t c, uint64_t nchunks, const double* wp) {
+    const int lane = threadIdx.x & 31;
+    const uint64_t g = c / kGroup;
+    const uint64_t c0 = g * kGroup;
+    const uint32_t members = static_cast<uint32_t>(nchunks - c0 < kGroup ? nchunks - c0 : kGroup);
+    const bool grouped = nchunks > kDirectChunks;   // else the finaliser sums the chunks
+    int last = 0;
+    if (lane == 0) {
+        double s = 0.0;
+        for (int w = 0; w < kThreads / 32; ++w) s = __dadd_rn(s, wp[w]);
+        ws.chunk_part[c] = s;
+        if (grouped) {
+            __threadfence();
+            last = atomicAdd(&ws.group_ticket[g], 1u) == members - 1 ? 1 : 0;
+        }
+    }
+    last = __shfl_sync(0xFFFFFFFFu, last, 0);
+    if (last) {
+        __threadfence();
+        double x = static_cast<uint32_t>(lane) < members
+                       ? *reinterpret_cast<const volatile double*>(ws.chunk_part + c0 + lane)
+                       : 0.0;
+        x = warp_dsum(x);
+        if (lane == 0) {
+            ws.group_part[g] = x;
+            ws.group_ticket[g] = 0u;
+        }
+    }
+}
+
+// The chunk's closing barrier with its norm partial: each warp's sum goes to
+// s_wp[parity], the barrier ORs `leave_in`, then warp 0 commits the chunk.
+__device__ __forceinline__ int close_chunk(const Workspace& ws, uint64_t c, uint64_t nchunks, double cacc,
+                                           double (*s_wp)[kThreads / 32], int parity, int leave_in) {
+    const double w = warp_dsum(cacc);
+    if ((threadIdx.x & 31) == 0) s_wp[parity][threadIdx.x >> 5] = w;
+    const int leave = __syncthreads_or(leave_in);
+    if (threadIdx.x < 32) commit_chunk(ws, c, nchunks, s_wp[parity]);
+    return leave;
+}
+
+// In the finalising CTA of a chunked launch: fixed-order sum of the group
+// partials (or, up to kDirectChunks chunks, of the chunk partials), and the
+// OR of the CTAs' flags.
+__device__ void gather_groups(const Workspace& ws, uint64_t nchunks, int nblocks, double& q, int& flag) {
+    __threadfence();
+    const bool grouped = nchunks > kDirectChunks;
+    const double* part = grouped ? ws.group_part : ws.chunk_part;
+    const uint64_t n = grouped ? group_count(nchunks) : nchunks;
+    double s = 0.0;
+    int f = 0;
+    for (uint64_t g = threadIdx.x; g < n; g += blockDim.x)
+        s = __dadd_rn(s, *reinterpret_cast<const volatile double*>(part + g));
+    for (int b = threadIdx.x; b < nblocks; b += blockDim.x) f |= *reinterpret_cast<const volatile int32_t*>(ws.flags + b);
+    q = block_sum(s);
+    flag = __syncthreads_or(f);
+}
+
+// A pass cut short leaves groups with missing chunks: the finalising CTA
+// zeroes their tickets.
+__device__ void reset_groups(const Workspace& ws, uint64_t nchunks) {
+    if (nchunks <= kDirectChunks) return;
+    const uint64_t ngroups = group_count(nchunks);
+    for (uint64_t g = threadIdx.x; g < ngroups; g += blockDim.x) ws.group_ticket[g] = 0u;
+}
+
 // Launch on a persistent grid: as many CTAs as fit on the SMs at once (from
 // the occupancy API), or fewer when `units` (vectors) need fewer, capped at
 // the per-block partial slots.
@@ -365,6 +497,12 @@ cudaError_t run(KernelT kernel, const Args& a, uint64_t nvec, cudaStream_t s, in
     if (grid_out) *grid_out = static_cast<int>(grid);
     kernel<<<static_cast<unsigned>(grid), kThreads, 0, s>>>(a);
     return cudaGetLastError();
+}
+
+// Launch a chunked kernel: the persistent grid, but no more CTAs than chunks.
+template <typename KernelT>
+cudaError_t run_chunked(KernelT kernel, const Args& a, uint64_t nvec, cudaStream_t s, int* grid_out) {
+    return run(kernel, a, chunk_total(nvec) * kThreads, s, grid_out);
 }
 
 }  // namespace

@@ -14,6 +14,42 @@ constexpr int kMaxBlocks = 4096;    // per-block norm partials of one launch
 constexpr int kMaxBuckets = 4096;   // reduce-scatter calls of one ZeRO-3 step
 constexpr int kThreads = 256;
 
+// Dynamic chunk scheduling (zero_device.cuh): a launch's CTAs take chunks of
+// kChunkU * kThreads vectors from a counter; norm partials are formed per
+// chunk and summed per group of kGroup chunks, so they do not depend on
+// which CTA took which chunk.
+constexpr int kChunkU = 4;
+constexpr uint64_t kChunkVec = static_cast<uint64_t>(kChunkU) * kThreads;
+constexpr int kGroup = 32;
+constexpr uint64_t kDirectChunks = 4096;   // up to this many chunks, no group stage
+constexpr int kCtrSlots = 64;       // launches of one handle that may be in flight at once
+
+// Vectors per thread in a chunk: kChunkU for large launches, fewer (down to
+// 1) for small ones, so that a launch has about kMinChunks chunks or more --
+// enough for every CTA of the persistent grid.  A function of the launch's
+// size only, so the chunk partials stay deterministic.
+constexpr uint64_t kMinChunks = 2048;
+__host__ __device__ inline int chunk_u(uint64_t nvec) {
+    const uint64_t u = nvec / (static_cast<uint64_t>(kThreads) * kMinChunks);
+    return u >= static_cast<uint64_t>(kChunkU) ? kChunkU : (u < 1 ? 1 : static_cast<int>(u));
+}
+__host__ __device__ inline uint64_t chunk_len(uint64_t nvec) {
+    return static_cast<uint64_t>(chunk_u(nvec)) * kThreads;
+}
+__host__ __device__ inline uint64_t chunk_total(uint64_t nvec) {
+    const uint64_t len = chunk_len(nvec);
+    return (nvec + len - 1) / len;
+}
+
+// Chunks and groups of any launch over at most `elems` elements (worst case:
+// 1-wide vectors; below kChunkU vectors per thread a launch has fewer than
+// 2 * kMinChunks chunks).
+inline uint64_t max_chunks(uint64_t elems) {
+    const uint64_t a = elems / kChunkVec + 1, b = 2 * kMinChunks + 1;
+    return a > b ? a : b;
+}
+inline uint64_t max_groups(uint64_t elems) { return max_chunks(elems) / kGroup + 1; }
+
 enum Dtype : int { kFp16 = 0, kBf16 = 1 };
 
 // Adam coefficients of one step, each rounded once to fp32 from double.
@@ -45,6 +81,15 @@ struct DevStatus {
     uint32_t ticket;    // last-block counter; returns to 0 after every launch
     uint32_t stop;      // one-pass step: a non-finite gradient was seen, the pass may stop
                         // (the step is skipped); returns to 0 when the pass finalises
+    uint64_t hwm1;      // one-pass step: 1 + a bound on the vectors it wrote (every write is
+                        // below it); 0 = unknown (the whole range).  Reset after each step.
+};
+
+// Per-launch chunk counter: grabs made so far; zero between launches (the
+// CTA that makes a launch's last grab resets it).
+struct ChunkCtr {
+    unsigned long long next;
+    unsigned long long pad;
 };
 
 struct Workspace {
@@ -54,6 +99,10 @@ struct Workspace {
     double* bucket_norm;   // [kMaxBuckets]
     int32_t* bucket_flag;  // [kMaxBuckets]
     float* ghat;           // [psi_pad] fp32 averaged gradient, or null
+    ChunkCtr* ctrs;        // [kCtrSlots], zero between launches
+    double* chunk_part;    // [max_chunks(psi_pad)] norm partial of each chunk
+    double* group_part;    // [max_groups(psi_pad)] norm partial of each group of chunks
+    uint32_t* group_ticket;  // [max_groups(psi_pad)], zero between launches
 };
 
 // Everything a launch needs, passed by value as a __grid_constant__ param.
@@ -81,6 +130,7 @@ struct Args {
     // staged step (zero_tma.cu): 1 + the tile at which CTA 0 stops issuing
     // its copies, so that its bounded waits run out (0: never)
     uint64_t hold_tile1;
+    int ctr_slot;          // chunked launches: this launch's counter, ws.ctrs[ctr_slot]
 };
 
 enum class Kind : int {

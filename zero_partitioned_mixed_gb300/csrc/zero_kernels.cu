@@ -10,8 +10,9 @@
 //   all-gather / broadcast -> the thread writes the RNE-cast 16-bit result
 //                      to all N replicas.
 // Every kernel is an HBM-bound stream: 128-bit (16-bit data) and 256-bit
-// (fp32 data) loads and stores of contiguous 8-element groups, grid-stride over a persistent grid sized
-// from the SM count and the kernel's occupancy.  There is no contraction,
+// (fp32 data) loads and stores of contiguous 8-element groups, on a
+// persistent grid sized from the SM count and the kernel's occupancy whose
+// CTAs take chunks of work from a counter (zero_device.cuh).  There is no contraction,
 // so no tensor-core path.
 //
 // Arithmetic follows the method exactly as the CPU oracle states it: fp32
@@ -34,62 +35,84 @@ namespace {
 // last block commits the shadow slot, or records the overflow (the
 // rollback kernel then restores the replicas).
 template <int DT, class IO>
-__global__ void __launch_bounds__(kThreads) k_step_spec(const __grid_constant__ Args a) {
+__global__ void __launch_bounds__(kThreads, 3) k_step_spec(const __grid_constant__ Args a) {
     constexpr int W = IO::W;
     __shared__ Pro pro;
+    __shared__ unsigned long long s_c[2];
+    __shared__ double s_wp[2][kThreads / 32];
     prologue_reduce(a, pro, true);
     const uint64_t src = static_cast<uint64_t>(pro.live) * a.slot_stride;
     const uint64_t dst = static_cast<uint64_t>(pro.live ^ 1) * a.slot_stride;
     const uint64_t nvec = a.count / W;
-    double acc = 0.0;
+    const uint64_t clen = chunk_len(nvec), nchunks = chunk_total(nvec);
+    const int U = chunk_u(nvec);
+    ChunkCtr* ctr = a.ws.ctrs + a.ctr_slot;
     int bad = 0;
     // Overflow is the existence of one non-finite averaged gradient, and an
-    // overflowed step changes no state (the fixup kernel restores every
-    // replica from the old master).  So the thread that finds one raises
-    // `stop` and every thread leaves the pass at its next iteration; the
-    // flag is read one iteration ahead, off the critical path.
+    // overflowed step changes no state (the fixup kernel restores the
+    // replicas from the old master).  So the thread that finds one raises
+    // `stop`, and the CTAs leave at the end of their chunk; the flag is read
+    // one vector ahead, off the critical path.
     volatile uint32_t* stop = &a.ws.status->stop;
     uint32_t seen = 0;
-    for (uint64_t vi = thread_id(); vi < nvec && !seen; vi += grid_threads()) {
-        const uint32_t seen_next = *stop;
-        const uint64_t gi = vi * W;
-        float g[W], p[W], m[W], v[W];
-        reduce_group<DT, IO>(a, gi, pro, g);
-        IO::ldf(a.master + src, gi, p);
-        IO::ldf(a.m + src, gi, m);
-        IO::ldf(a.v + src, gi, v);
-        const int valid = valid_count(gi, W, a.psi);
-        norm_group<W>(g, valid, acc, bad);
-        if (bad) {
-            *stop = 1u;
-            break;
-        }
-        seen = seen_next;
-        uint32_t q[W];
-#pragma unroll
-        for (int k = 0; k < W; ++k) {
-            if (k < valid) {
-                adam1(g[k], p[k], m[k], v[k], pro.sc);
-            } else {
-                p[k] = 0.0f; m[k] = 0.0f; v[k] = 0.0f;
+    uint64_t reach = 0;   // thread 0: 1 + the last chunk this CTA worked on
+    Chunks ch(ctr, s_c, nchunks);
+    for (;;) {
+        const uint64_t c = ch.current();
+        if (c >= nchunks) break;
+        ch.prefetch();
+        reach = c + 1;
+        double cacc = 0.0;
+        for (int u = 0; u < U; ++u) {
+            const uint64_t vi = chunk_vec(c, clen, u);
+            if (vi >= nvec) break;
+            const uint32_t seen_next = *stop;
+            const uint64_t gi = vi * W;
+            float g[W], p[W], m[W], v[W];
+            reduce_group<DT, IO>(a, gi, pro, g);
+            IO::ldf(a.master + src, gi, p);
+            IO::ldf(a.m + src, gi, m);
+            IO::ldf(a.v + src, gi, v);
+            const int valid = valid_count(gi, W, a.psi);
+            norm_group<W>(g, valid, cacc, bad);
+            if (bad) {
+                *stop = 1u;
+                break;
             }
-            q[k] = narrow<DT>(p[k]);
+            seen = seen_next;
+            uint32_t q[W];
+#pragma unroll
+            for (int k = 0; k < W; ++k) {
+                if (k < valid) {
+                    adam1(g[k], p[k], m[k], v[k], pro.sc);
+                } else {
+                    p[k] = 0.0f; m[k] = 0.0f; v[k] = 0.0f;
+                }
+                q[k] = narrow<DT>(p[k]);
+            }
+            IO::stf(a.master + dst, gi, p);
+            IO::stf(a.m + dst, gi, m);
+            IO::stf(a.v + dst, gi, v);
+            for (int r = 0; r < a.n_ranks; ++r) IO::st16(a.params[r], gi, q);
         }
-        IO::stf(a.master + dst, gi, p);
-        IO::stf(a.m + dst, gi, m);
-        IO::stf(a.v + dst, gi, v);
-        for (int r = 0; r < a.n_ranks; ++r) IO::st16(a.params[r], gi, q);
+        const int leave = close_chunk(a.ws, c, nchunks, cacc, s_wp, ch.parity(), static_cast<int>(seen) | bad);
+        ch.advance();
+        if (leave) break;
     }
-    const double blk = block_sum(acc);
+    // a CTA works on its chunks in increasing order: every vector written
+    // lies below the largest reach, which bounds an overflow rollback
+    if (threadIdx.x == 0) atomicMax(reinterpret_cast<unsigned long long*>(&a.ws.status->hwm1), reach * clen + 1ull);
     const int flag = __syncthreads_or(bad);
-    if (publish(a, blk, flag, a.ws.partials, a.ws.flags)) {
-        double qsum;
+    if (publish(a, 0.0, flag, a.ws.partials, a.ws.flags)) {
+        double q;
         int f;
-        gather_partials(a.ws.partials, a.ws.flags, gridDim.x, qsum, f);
+        gather_groups(a.ws, nchunks, gridDim.x, q, f);
+        if (f) reset_groups(a.ws, nchunks);
         if (threadIdx.x == 0) {
             DevStatus* st = a.ws.status;
-            if (f) status_skip(st, qsum);
-            else status_decide_spec(st, qsum, a.hyper);
+            ctr->next = 0ull;   // a pass cut short made fewer than nchunks grabs
+            if (f) status_skip(st, q);
+            else status_decide_spec(st, q, a.hyper);
             st->stop = 0u;
             st->ticket = 0u;
         }
@@ -103,33 +126,48 @@ template <int DT, class IO, bool WS>
 __global__ void __launch_bounds__(kThreads) k_reduce(const __grid_constant__ Args a) {
     constexpr int W = IO::W;
     __shared__ Pro pro;
+    __shared__ unsigned long long s_c[2];
+    __shared__ double s_wp[2][kThreads / 32];
     prologue_reduce(a, pro, false);
     const uint64_t nvec = a.count / W;
-    double acc = 0.0;
+    const uint64_t clen = chunk_len(nvec), nchunks = chunk_total(nvec);
+    const int U = chunk_u(nvec);
+    ChunkCtr* ctr = a.ws.ctrs + a.ctr_slot;
     int bad = 0;
-    for (uint64_t vi = thread_id(); vi < nvec; vi += grid_threads()) {
-        const uint64_t gi = vi * W;
-        float g[W];
-        reduce_group<DT, IO>(a, gi, pro, g);
-        const int valid = valid_count(gi, W, a.psi);
-        norm_group<W>(g, valid, acc, bad);
-        if (WS) {
+    Chunks ch(ctr, s_c, nchunks);
+    for (;;) {
+        const uint64_t c = ch.current();
+        if (c >= nchunks) break;
+        ch.prefetch();
+        double cacc = 0.0;
+        for (int u = 0; u < U; ++u) {
+            const uint64_t vi = chunk_vec(c, clen, u);
+            if (vi >= nvec) break;
+            const uint64_t gi = vi * W;
+            float g[W];
+            reduce_group<DT, IO>(a, gi, pro, g);
+            const int valid = valid_count(gi, W, a.psi);
+            norm_group<W>(g, valid, cacc, bad);
+            if (WS) {
 #pragma unroll
-            for (int k = 0; k < W; ++k)
-                if (k >= valid) g[k] = 0.0f;
-            IO::stf(a.ws.ghat, gi, g);
+                for (int k = 0; k < W; ++k)
+                    if (k >= valid) g[k] = 0.0f;
+                IO::stf(a.ws.ghat, gi, g);
+            }
         }
+        close_chunk(a.ws, c, nchunks, cacc, s_wp, ch.parity(), 0);
+        ch.advance();
     }
-    const double blk = block_sum(acc);
     const int flag = __syncthreads_or(bad);
-    if (publish(a, blk, flag, a.ws.partials, a.ws.flags)) {
-        double qsum;
+    if (publish(a, 0.0, flag, a.ws.partials, a.ws.flags)) {
+        double q;
         int f;
-        gather_partials(a.ws.partials, a.ws.flags, gridDim.x, qsum, f);
+        gather_groups(a.ws, nchunks, gridDim.x, q, f);
         if (threadIdx.x == 0) {
+            ctr->next = 0ull;
             DevStatus* st = a.ws.status;
-            if (f) status_skip(st, qsum);
-            else status_decide_two_pass(st, qsum, a.hyper);
+            if (f) status_skip(st, q);
+            else status_decide_two_pass(st, q, a.hyper);
             st->ticket = 0u;
         }
     }
@@ -143,11 +181,22 @@ template <int DT, class IO, bool SRC_WS, bool TO_SHARD>
 __global__ void __launch_bounds__(kThreads) k_apply(const __grid_constant__ Args a) {
     constexpr int W = IO::W;
     __shared__ Pro pro;
+    __shared__ unsigned long long s_c[2];
     prologue_reduce(a, pro, false);
-    if (pro.overflow) return;
+    if (pro.overflow) return;   // every CTA: the counter stays untouched
     const uint64_t off = static_cast<uint64_t>(pro.live) * a.slot_stride;
     const uint64_t nvec = a.count / W;
-    for (uint64_t vi = thread_id(); vi < nvec; vi += grid_threads()) {
+    const uint64_t clen = chunk_len(nvec), nchunks = chunk_total(nvec);
+    const int U = chunk_u(nvec);
+    ChunkCtr* ctr = a.ws.ctrs + a.ctr_slot;
+    Chunks ch(ctr, s_c, nchunks);
+    for (;;) {
+      const uint64_t c = ch.current();
+      if (c >= nchunks) break;
+      ch.prefetch();
+      for (int u = 0; u < U; ++u) {
+        const uint64_t vi = chunk_vec(c, clen, u);
+        if (vi >= nvec) break;
         const uint64_t gi = vi * W;
         float g[W], p[W], m[W], v[W];
         if (SRC_WS) IO::ldf(a.ws.ghat, gi, g);
@@ -175,19 +224,33 @@ __global__ void __launch_bounds__(kThreads) k_apply(const __grid_constant__ Args
         } else {
             for (int r = 0; r < a.n_ranks; ++r) IO::st16(a.params[r], gi, q);
         }
+      }
+      __syncthreads();
+      ch.advance();
     }
 }
 
 // Stage 0, pass 2: every rank holds the full averaged gradient and its own
 // full replica of master/m/v (rank r at r*psi_pad) and updates all of it.
 template <int DT, class IO>
-__global__ void __launch_bounds__(kThreads) k_apply_stage0(const __grid_constant__ Args a) {
+__global__ void __launch_bounds__(kThreads, 3) k_apply_stage0(const __grid_constant__ Args a) {
     constexpr int W = IO::W;
     __shared__ Pro pro;
+    __shared__ unsigned long long s_c[2];
     prologue_reduce(a, pro, false);
-    if (pro.overflow) return;
+    if (pro.overflow) return;   // every CTA: the counter stays untouched
     const uint64_t nvec = a.count / W;
-    for (uint64_t vi = thread_id(); vi < nvec; vi += grid_threads()) {
+    const uint64_t clen = chunk_len(nvec), nchunks = chunk_total(nvec);
+    const int U = chunk_u(nvec);
+    ChunkCtr* ctr = a.ws.ctrs + a.ctr_slot;
+    Chunks ch(ctr, s_c, nchunks);
+    for (;;) {
+      const uint64_t c = ch.current();
+      if (c >= nchunks) break;
+      ch.prefetch();
+      for (int u = 0; u < U; ++u) {
+        const uint64_t vi = chunk_vec(c, clen, u);
+        if (vi >= nvec) break;
         const uint64_t gi = vi * W;
         float g[W];
         IO::ldf(a.ws.ghat, gi, g);
@@ -216,6 +279,9 @@ __global__ void __launch_bounds__(kThreads) k_apply_stage0(const __grid_constant
             IO::stf(a.v, ri, v);
             IO::st16(a.params[r], gi, q);
         }
+      }
+      __syncthreads();
+      ch.advance();
     }
 }
 
@@ -224,22 +290,36 @@ __global__ void __launch_bounds__(kThreads) k_apply_stage0(const __grid_constant
 template <int DT, class IO, bool TO_SHARD>
 __global__ void __launch_bounds__(kThreads) k_rollback(const __grid_constant__ Args a) {
     constexpr int W = IO::W;
+    __shared__ unsigned long long s_c[2];
     const DevStatus* st = a.ws.status;
-    if (!st->overflow) return;
+    if (!st->overflow) return;   // every CTA: the counter stays untouched
     const uint64_t off = static_cast<uint64_t>(st->live_slot) * a.slot_stride;
     const uint64_t nvec = a.count / W;
-    for (uint64_t vi = thread_id(); vi < nvec; vi += grid_threads()) {
-        const uint64_t gi = a.base + vi * W;
-        float p[W];
-        IO::ldf(a.master + off, gi, p);
-        uint32_t q[W];
+    const uint64_t clen = chunk_len(nvec), nchunks = chunk_total(nvec);
+    const int U = chunk_u(nvec);
+    ChunkCtr* ctr = a.ws.ctrs + a.ctr_slot;
+    Chunks ch(ctr, s_c, nchunks);
+    for (;;) {
+        const uint64_t c = ch.current();
+        if (c >= nchunks) break;
+        ch.prefetch();
+        for (int u = 0; u < U; ++u) {
+            const uint64_t vi = chunk_vec(c, clen, u);
+            if (vi >= nvec) break;
+            const uint64_t gi = a.base + vi * W;
+            float p[W];
+            IO::ldf(a.master + off, gi, p);
+            uint32_t q[W];
 #pragma unroll
-        for (int k = 0; k < W; ++k) q[k] = narrow<DT>(p[k]);
-        if (TO_SHARD) {
-            IO::st16(a.params[0], gi, q);
-        } else {
-            for (int r = 0; r < a.n_ranks; ++r) IO::st16(a.params[r], gi, q);
+            for (int k = 0; k < W; ++k) q[k] = narrow<DT>(p[k]);
+            if (TO_SHARD) {
+                IO::st16(a.params[0], gi, q);
+            } else {
+                for (int r = 0; r < a.n_ranks; ++r) IO::st16(a.params[r], gi, q);
+            }
         }
+        __syncthreads();
+        ch.advance();
     }
 }
 
@@ -252,14 +332,28 @@ template <int DT, class IO>
 __global__ void __launch_bounds__(kThreads) k_fixup(const __grid_constant__ Args a) {
     constexpr int W = IO::W;
     __shared__ Pro pro;
+    __shared__ unsigned long long s_c[2];
     prologue_reduce(a, pro, false);
     const DevStatus* st = a.ws.status;
     const int overflow = st->overflow, redo = st->redo;
-    if (!overflow && !redo) return;
+    if (!overflow && !redo) return;   // every CTA: the counter stays untouched
     const uint64_t src = static_cast<uint64_t>(pro.live) * a.slot_stride;
     const uint64_t dst = static_cast<uint64_t>(pro.live ^ 1) * a.slot_stride;
     const uint64_t nvec = a.count / W;
-    for (uint64_t vi = thread_id(); vi < nvec; vi += grid_threads()) {
+    // a rollback restores only what the stopped pass may have written
+    const uint64_t hw = st->hwm1;
+    const uint64_t lim = (overflow && hw != 0 && hw - 1 < nvec) ? hw - 1 : nvec;
+    const uint64_t clen = chunk_len(lim), nchunks = chunk_total(lim);
+    const int U = chunk_u(lim);
+    ChunkCtr* ctr = a.ws.ctrs + a.ctr_slot;
+    Chunks ch(ctr, s_c, nchunks);
+    for (;;) {
+      const uint64_t c = ch.current();
+      if (c >= nchunks) break;
+      ch.prefetch();
+      for (int u = 0; u < U; ++u) {
+        const uint64_t vi = chunk_vec(c, clen, u);
+        if (vi >= lim) break;
         const uint64_t gi = vi * W;
         float p[W];
         uint32_t q[W];
@@ -287,6 +381,9 @@ __global__ void __launch_bounds__(kThreads) k_fixup(const __grid_constant__ Args
             IO::stf(a.v + dst, gi, v);
         }
         for (int r = 0; r < a.n_ranks; ++r) IO::st16(a.params[r], gi, q);
+      }
+      __syncthreads();
+      ch.advance();
     }
 }
 
@@ -297,18 +394,33 @@ __global__ void k_commit_redo(DevStatus* st) {
         st->t += 1;
         st->applied = 1;
     }
+    st->hwm1 = 0ull;
 }
 
 // ZeRO-3 gather of [base, base+count): out[r][j] = shard[base + j].
 template <class IO>
 __global__ void __launch_bounds__(kThreads) k_gather(const __grid_constant__ Args a) {
     constexpr int W = IO::W;
+    __shared__ unsigned long long s_c[2];
     const uint64_t nvec = a.count / W;
-    for (uint64_t vi = thread_id(); vi < nvec; vi += grid_threads()) {
-        const uint64_t j = vi * W;
-        uint32_t x[W];
-        IO::ld16(a.grads[0], a.base + j, x);
-        for (int r = 0; r < a.n_ranks; ++r) IO::st16(a.params[r], j, x);
+    const uint64_t clen = chunk_len(nvec), nchunks = chunk_total(nvec);
+    const int U = chunk_u(nvec);
+    ChunkCtr* ctr = a.ws.ctrs + a.ctr_slot;
+    Chunks ch(ctr, s_c, nchunks);
+    for (;;) {
+        const uint64_t c = ch.current();
+        if (c >= nchunks) break;
+        ch.prefetch();
+        for (int u = 0; u < U; ++u) {
+            const uint64_t vi = chunk_vec(c, clen, u);
+            if (vi >= nvec) break;
+            const uint64_t j = vi * W;
+            uint32_t x[W];
+            IO::ld16(a.grads[0], a.base + j, x);
+            for (int r = 0; r < a.n_ranks; ++r) IO::st16(a.params[r], j, x);
+        }
+        __syncthreads();
+        ch.advance();
     }
 }
 
@@ -320,16 +432,28 @@ __global__ void __launch_bounds__(kThreads) k_gather(const __grid_constant__ Arg
 // The last block stores the bucket's norm partial and flag for the step's
 // finaliser.
 template <int DT, class IO, bool SPEC, bool TO_REPLICAS>
-__global__ void __launch_bounds__(kThreads) k_rs(const __grid_constant__ Args a) {
+__global__ void __launch_bounds__(kThreads, 3) k_rs(const __grid_constant__ Args a) {
     constexpr int W = IO::W;
     __shared__ Pro pro;
+    __shared__ unsigned long long s_c[2];
+    __shared__ double s_wp[2][kThreads / 32];
     prologue_reduce(a, pro, SPEC);
     const uint64_t src = static_cast<uint64_t>(pro.live) * a.slot_stride;
     const uint64_t dst = static_cast<uint64_t>(pro.live ^ 1) * a.slot_stride;
     const uint64_t nvec = a.count / W;
-    double acc = 0.0;
+    const uint64_t clen = chunk_len(nvec), nchunks = chunk_total(nvec);
+    const int U = chunk_u(nvec);
+    ChunkCtr* ctr = a.ws.ctrs + a.ctr_slot;
     int bad = 0;
-    for (uint64_t vi = thread_id(); vi < nvec; vi += grid_threads()) {
+    Chunks ch(ctr, s_c, nchunks);
+    for (;;) {
+      const uint64_t c = ch.current();
+      if (c >= nchunks) break;
+      ch.prefetch();
+      double acc = 0.0;
+      for (int u = 0; u < U; ++u) {
+        const uint64_t vi = chunk_vec(c, clen, u);
+        if (vi >= nvec) break;
         const uint64_t j = vi * W;
         const uint64_t gi = a.base + j;
         float g[W];
@@ -366,14 +490,17 @@ __global__ void __launch_bounds__(kThreads) k_rs(const __grid_constant__ Args a)
                 if (k >= valid) g[k] = 0.0f;
             IO::stf(a.ws.ghat, gi, g);
         }
+      }
+      close_chunk(a.ws, c, nchunks, acc, s_wp, ch.parity(), 0);
+      ch.advance();
     }
-    const double blk = block_sum(acc);
     const int flag = __syncthreads_or(bad);
-    if (publish(a, blk, flag, a.ws.partials, a.ws.flags)) {
+    if (publish(a, 0.0, flag, a.ws.partials, a.ws.flags)) {
         double qsum;
         int f;
-        gather_partials(a.ws.partials, a.ws.flags, gridDim.x, qsum, f);
+        gather_groups(a.ws, nchunks, gridDim.x, qsum, f);
         if (threadIdx.x == 0) {
+            ctr->next = 0ull;
             a.ws.bucket_norm[a.bucket_index] = qsum;
             a.ws.bucket_flag[a.bucket_index] = f;
             a.ws.status->ticket = 0u;
@@ -411,6 +538,7 @@ __global__ void k_set_scaler(DevStatus* st, float loss_scale, int64_t t, int32_t
     st->redo = 0;
     st->ticket = 0u;
     st->stop = 0u;
+    st->hwm1 = 0ull;
 }
 
 // ------------------------------------------------------------------ launch
@@ -418,20 +546,20 @@ template <int DT, class IO>
 cudaError_t launch_dw(Kind kind, const Args& a, cudaStream_t s, int* grid_out) {
     const uint64_t nvec = a.count / IO::W;
     switch (kind) {
-        case Kind::kStepSpec: return run(k_step_spec<DT, IO>, a, nvec, s, grid_out);
-        case Kind::kReduceWs: return run(k_reduce<DT, IO, true>, a, nvec, s, grid_out);
-        case Kind::kReduceNoWs: return run(k_reduce<DT, IO, false>, a, nvec, s, grid_out);
-        case Kind::kApplyWs: return run(k_apply<DT, IO, true, false>, a, nvec, s, grid_out);
-        case Kind::kApplyReread: return run(k_apply<DT, IO, false, false>, a, nvec, s, grid_out);
-        case Kind::kApplyWsShard: return run(k_apply<DT, IO, true, true>, a, nvec, s, grid_out);
-        case Kind::kApplyStage0: return run(k_apply_stage0<DT, IO>, a, nvec, s, grid_out);
-        case Kind::kRollbackReplicas: return run(k_rollback<DT, IO, false>, a, nvec, s, grid_out);
-        case Kind::kRollbackShard: return run(k_rollback<DT, IO, true>, a, nvec, s, grid_out);
-        case Kind::kFixupReplicas: return run(k_fixup<DT, IO>, a, nvec, s, grid_out);
-        case Kind::kGather: return run(k_gather<IO>, a, nvec, s, grid_out);
-        case Kind::kRsSpec: return run(k_rs<DT, IO, true, false>, a, nvec, s, grid_out);
-        case Kind::kRsSpecReplicas: return run(k_rs<DT, IO, true, true>, a, nvec, s, grid_out);
-        case Kind::kRsWs: return run(k_rs<DT, IO, false, false>, a, nvec, s, grid_out);
+        case Kind::kStepSpec: return run_chunked(k_step_spec<DT, IO>, a, nvec, s, grid_out);
+        case Kind::kReduceWs: return run_chunked(k_reduce<DT, IO, true>, a, nvec, s, grid_out);
+        case Kind::kReduceNoWs: return run_chunked(k_reduce<DT, IO, false>, a, nvec, s, grid_out);
+        case Kind::kApplyWs: return run_chunked(k_apply<DT, IO, true, false>, a, nvec, s, grid_out);
+        case Kind::kApplyReread: return run_chunked(k_apply<DT, IO, false, false>, a, nvec, s, grid_out);
+        case Kind::kApplyWsShard: return run_chunked(k_apply<DT, IO, true, true>, a, nvec, s, grid_out);
+        case Kind::kApplyStage0: return run_chunked(k_apply_stage0<DT, IO>, a, nvec, s, grid_out);
+        case Kind::kRollbackReplicas: return run_chunked(k_rollback<DT, IO, false>, a, nvec, s, grid_out);
+        case Kind::kRollbackShard: return run_chunked(k_rollback<DT, IO, true>, a, nvec, s, grid_out);
+        case Kind::kFixupReplicas: return run_chunked(k_fixup<DT, IO>, a, nvec, s, grid_out);
+        case Kind::kGather: return run_chunked(k_gather<IO>, a, nvec, s, grid_out);
+        case Kind::kRsSpec: return run_chunked(k_rs<DT, IO, true, false>, a, nvec, s, grid_out);
+        case Kind::kRsSpecReplicas: return run_chunked(k_rs<DT, IO, true, true>, a, nvec, s, grid_out);
+        case Kind::kRsWs: return run_chunked(k_rs<DT, IO, false, false>, a, nvec, s, grid_out);
     }
     return cudaErrorInvalidValue;
 }

@@ -33,9 +33,20 @@ constexpr size_t kStatusBytes = 256;
 constexpr size_t kPartialBytes = static_cast<size_t>(zg::kMaxBlocks) * sizeof(double);
 constexpr size_t kFlagBytes = static_cast<size_t>(zg::kMaxBlocks) * sizeof(int32_t);
 constexpr size_t kGhatBytes = static_cast<size_t>(kNoAllocMaxPsiPad) * sizeof(float);
-constexpr size_t kScratchBytes = kStatusBytes + kPartialBytes + kFlagBytes + kGhatBytes;
+constexpr size_t round32(size_t x) { return (x + 31) / 32 * 32; }
+// chunk scheduling: counters and group tickets (zeroed every call), chunk and group partials
+constexpr size_t kCtrBytes = round32(static_cast<size_t>(zg::kCtrSlots) * sizeof(zg::ChunkCtr));
+constexpr size_t kChunks = kNoAllocMaxPsiPad / zg::kChunkVec + 1 > 2 * zg::kMinChunks + 1
+                               ? kNoAllocMaxPsiPad / zg::kChunkVec + 1
+                               : 2 * zg::kMinChunks + 1;
+constexpr size_t kGroups = kChunks / zg::kGroup + 1;
+constexpr size_t kTicketBytes = round32(kGroups * sizeof(uint32_t));
+constexpr size_t kChunkPartBytes = round32(kChunks * sizeof(double));
+constexpr size_t kGroupPartBytes = round32(kGroups * sizeof(double));
+constexpr size_t kScratchBytes = kStatusBytes + kPartialBytes + kFlagBytes + kGhatBytes + kCtrBytes + kTicketBytes +
+                                 kChunkPartBytes + kGroupPartBytes;
 static_assert(sizeof(zg::DevStatus) <= kStatusBytes, "status must fit its slot");
-static_assert(kStatusBytes % 32 == 0 && kPartialBytes % 32 == 0 && kFlagBytes % 32 == 0,
+static_assert(kStatusBytes % 32 == 0 && kPartialBytes % 32 == 0 && kFlagBytes % 32 == 0 && kGhatBytes % 32 == 0,
               "scratch regions stay 32-byte aligned");
 
 // The scratch.  Host code must not pass &g_noalloc_scratch to a kernel: on
@@ -158,6 +169,11 @@ extern "C" int zero_step_noalloc(uint64_t psi, int n_ranks, int stage, int dtype
     a.ws.bucket_norm = nullptr;
     a.ws.bucket_flag = nullptr;
     a.ws.ghat = reinterpret_cast<float*>(base + kStatusBytes + kPartialBytes + kFlagBytes);
+    unsigned char* sched = base + kStatusBytes + kPartialBytes + kFlagBytes + kGhatBytes;
+    a.ws.ctrs = reinterpret_cast<zg::ChunkCtr*>(sched);
+    a.ws.group_ticket = reinterpret_cast<uint32_t*>(sched + kCtrBytes);
+    a.ws.chunk_part = reinterpret_cast<double*>(sched + kCtrBytes + kTicketBytes);
+    a.ws.group_part = reinterpret_cast<double*>(sched + kCtrBytes + kTicketBytes + kChunkPartBytes);
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // 8-wide with 256-bit fp32 accesses when the caller's state is 32-byte
@@ -167,8 +183,12 @@ extern "C" int zero_step_noalloc(uint64_t psi, int n_ranks, int stage, int dtype
     const zg::Vec vec = (P % 8) != 0 ? zg::Vec::k1 : (s32 ? zg::Vec::k8s32 : zg::Vec::k8s16);
     // the status word (and its last-block ticket) must start from zero
     e = cudaMemsetAsync(a.ws.status, 0, kStatusBytes, s);
+    // and the chunk counters and group tickets
+    if (e == cudaSuccess) e = cudaMemsetAsync(sched, 0, kCtrBytes + kTicketBytes, s);
     if (e == cudaSuccess) e = zg::launch_set_scaler(a.ws.status, loss_scale, steps_applied, 0, s);
+    a.ctr_slot = 0;
     if (e == cudaSuccess) e = zg::launch(zg::Kind::kReduceWs, dtype, vec, a, s, nullptr);
+    a.ctr_slot = 1;
     if (e == cudaSuccess) e = zg::launch(zg::Kind::kApplyWs, dtype, vec, a, s, nullptr);
     if (e == cudaSuccess) {
         k_export_result<<<1, 1, 0, s>>>(a.ws.status, result);
