@@ -152,11 +152,13 @@ zg::Vec pick_vec(bool vec8, const zg::Args& a) {
     return s32 ? zg::Vec::k8s32 : zg::Vec::k8s16;
 }
 
+// Each chunked launch its own counter slot: a gather on one stream may
+// overlap a reduce-scatter on another.
+int next_slot(zero_handle* h) { return static_cast<int>(h->launch_seq++ % zg::kCtrSlots); }
+
 int launch(zero_handle* h, zg::Kind kind, bool vec8, const zg::Args& a, cudaStream_t s, const char* what) {
-    // each launch its own chunk counter: a gather on one stream may overlap
-    // a reduce-scatter on another
     zg::Args b = a;
-    b.ctr_slot = static_cast<int>(h->launch_seq++ % zg::kCtrSlots);
+    b.ctr_slot = next_slot(h);
     cudaError_t e = zg::launch(kind, h->dtype, pick_vec(vec8, b), b, s, nullptr);
     if (e != cudaSuccess) return cuda_fail(h, e, what);
     return ZERO_OK;
@@ -632,6 +634,7 @@ int zero_gather_bucket_q8(zero_handle_t h, uint64_t a0, uint64_t b0, const void*
     a.count = L;
     a.qbits = 8;
     a.qvec = (a0 % 8) == 0 ? 1 : 0;
+    a.ctr_slot = next_slot(h);
     const cudaError_t e = zg::launch_q(zg::QKind::kGatherQ8, h->dtype, 8, zg::Vec::k1, a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(h, e, "quantized gather");
     const uint64_t nb = (L + zg::kQBlock - 1) / zg::kQBlock;

@@ -238,6 +238,14 @@ __device__ __forceinline__ uint32_t load_code1(const void* codes, uint64_t e) {
 __device__ __forceinline__ uint64_t warp_id() { return (static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; }
 __device__ __forceinline__ uint64_t warp_count() { return (static_cast<uint64_t>(gridDim.x) * blockDim.x) >> 5; }
 
+// Warp-iterations per chunk for the block-quantizing kernels: 4 when a
+// launch has plenty of work, fewer for small ones (at least kMinChunks
+// chunks when possible).
+__host__ __device__ inline int q_chunk_u(uint64_t iters) {
+    const uint64_t u = iters / kMinChunks;
+    return u >= 4 ? 4 : (u < 1 ? 1 : static_cast<int>(u));
+}
+
 // ------------------------------------------------------------------ kernels
 // Blocks per warp iteration (their loads are in flight together): two for
 // the gather, whose stores to N ranks dominate; four for the one-output
@@ -290,12 +298,29 @@ __global__ void __launch_bounds__(kThreads) k_quantize(const __grid_constant__ A
 
 // ZeRO-3 quantized gather (qwZ): bucket [base, base+count) of the 16-bit
 // shard (grads[0]) -> for every rank r: codes (params[r]) and scales (qdst[r]).
+// Chunked like the other persistent kernels (zero_device.cuh): a chunk is
+// U iterations of the CTA's 8 warps, kQUnrollGather blocks per warp each.
 template <int DT>
 __global__ void __launch_bounds__(kThreads) k_gather_q8(const __grid_constant__ Args a) {
-    const int lane = threadIdx.x & 31;
+    __shared__ unsigned long long s_c[2];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint64_t nb = (a.count + kQBlock - 1) / kQBlock;
     const unsigned short* src = static_cast<const unsigned short*>(a.grads[0]) + a.base;
-    for (uint64_t blk0 = warp_id() * kQUnrollGather; blk0 < nb; blk0 += warp_count() * kQUnrollGather) {
+    // one "vector" = one warp-iteration's blocks; kThreads vectors per U unit
+    // would be too coarse here, so the chunk length counts warp-iterations
+    constexpr uint64_t kPerIter = static_cast<uint64_t>(kThreads / 32) * kQUnrollGather;
+    const uint64_t iters = (nb + kPerIter - 1) / kPerIter;
+    const int U = q_chunk_u(iters);
+    const uint64_t nchunks = (iters + U - 1) / U;
+    ChunkCtr* ctr = a.ws.ctrs + a.ctr_slot;
+    Chunks ch(ctr, s_c, nchunks);
+    for (;;) {
+      const uint64_t c = ch.current();
+      if (c >= nchunks) break;
+      ch.prefetch();
+      for (int u = 0; u < U; ++u) {
+        const uint64_t blk0 = (c * U + u) * kPerIter + static_cast<uint64_t>(warp) * kQUnrollGather;
+        if (blk0 >= nb) break;
         quantize_blocks_u<DT, 8, kQUnrollGather>(src, a.count, blk0, nb, a.qvec != 0, lane,
                                  [&](uint64_t blk, uint64_t e0, int nv, const uint32_t (&q)[8], float scale,
                                      float lo) {
@@ -311,6 +336,9 @@ __global__ void __launch_bounds__(kThreads) k_gather_q8(const __grid_constant__ 
                                      for (int r = lane; r < a.n_ranks; r += 32)
                                          *reinterpret_cast<float2*>(a.qdst[r] + 2 * blk) = make_float2(scale, lo);
                                  });
+      }
+      __syncthreads();
+      ch.advance();
     }
 }
 
@@ -399,6 +427,9 @@ __device__ __forceinline__ void reduce_group_q(const Args& a, uint64_t j, const 
 
 // ZeRO-3 reduce-scatter of bucket [base, base+count) from the N ranks'
 // quantized gradients (qgZ): as k_rs, with the ranks' values dequantized.
+// Static grid-stride: with only 24 resident warps per SM this kernel waits
+// on its loads, and chunked scheduling's block barriers cost more (+6 % for
+// int8) than the balance gains.
 template <int DT, class IO, int BITS, bool SPEC>
 __global__ void __launch_bounds__(kThreads, BITS == 4 ? 4 : 3) k_rs_q(const __grid_constant__ Args a) {
     constexpr int W = IO::W;
@@ -462,8 +493,13 @@ cudaError_t launch_db(QKind kind, Vec vec, const Args& a, cudaStream_t s) {
     switch (kind) {
         case QKind::kQuantize:
             return run(k_quantize<DT, BITS>, a, (nb + kQUnrollQuant - 1) / kQUnrollQuant * 32, s, nullptr);
-        case QKind::kGatherQ8:
-            return run(k_gather_q8<DT>, a, (nb + kQUnrollGather - 1) / kQUnrollGather * 32, s, nullptr);
+        case QKind::kGatherQ8: {
+            // one CTA per chunk at most (run() sizes the grid from threads)
+            const uint64_t per_iter = static_cast<uint64_t>(kThreads / 32) * kQUnrollGather;
+            const uint64_t iters = (nb + per_iter - 1) / per_iter;
+            const uint64_t nch = (iters + q_chunk_u(iters) - 1) / q_chunk_u(iters);
+            return run(k_gather_q8<DT>, a, nch * kThreads, s, nullptr);
+        }
         case QKind::kDequantize: return run(k_dequantize<DT, BITS>, a, (a.count + 7) / 8, s, nullptr);
         case QKind::kRsQSpec:
         case QKind::kRsQWs: {
