@@ -303,7 +303,7 @@ def run_ours(args, ws, rank, local):
                      "kernel": "k_step_spec (fp16, 8-wide)",
                      "algorithmic_bytes_per_launch": alg_bytes,
                      "peak_source": f"{peak_src} hbm_gbs (copy)"},
-        "gpu_launches": 2 * K,
+        "gpu_launches": 3 * K,   # per step: the step kernel, the fixup, the commit
         "status_after": {k: status[k] for k in ("steps_applied", "steps_skipped", "loss_scale")},
     }
     c = clocks.summary()

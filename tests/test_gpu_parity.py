@@ -451,3 +451,15 @@ def test_norm_is_bitwise_deterministic(stage, mode, psi, bucket):
         runs.append((struct.pack("<d", s["grad_norm"]), m.cpu().numpy().tobytes()))
         buf.close()
     assert runs[0] == runs[1] == runs[2]
+
+
+def test_overflow_stop_on_the_grouped_path():
+    # 40M elements over 4 ranks: 5M vectors, 4883 chunks of 1024 -- above
+    # the 4096 chunks summed directly, so norm partials go through group
+    # tickets.  An inf at 30 % stops the pass with groups left incomplete;
+    # the finaliser must reset their tickets (the next steps' norms and every
+    # element of state and replicas must still match the oracle).
+    st = run_case(40_000_003, 4, 1, "bf16", steps=3, mode=3, double_buffer=True, sigma=1e-3,
+                  inject=[(1, 3, 12_000_000, INF)])
+    st.check()
+    assert st.mismatches == 0, st
