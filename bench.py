@@ -442,8 +442,9 @@ def _bytes_total(buf):
     return b["hbm_read_total"] + b["hbm_write_total"]
 
 
-def bench_dense(w, stage, steps, warmup, torch, S, Z, flush_l2=False, sets_max=5):
-    """Stages 0-2: resident gradient sets, one zero_step per bench step."""
+def bench_dense(w, stage, steps, warmup, torch, S, Z, flush_l2=False, sets_max=5, mode=None):
+    """Stages 0-2: resident gradient sets, one zero_step per bench step
+    (mode: a ZERO_MODE_*, default AUTO)."""
     from zero_partitioned_mixed_gb300.buffers import RankBuffers
     buf = RankBuffers(w.psi, w.n_ranks, stage, w.dtype, double_buffer=stage != 0, alloc_grads=False)
     P, N = buf.psi_pad, w.n_ranks
@@ -467,7 +468,8 @@ def bench_dense(w, stage, steps, warmup, torch, S, Z, flush_l2=False, sets_max=5
             S.draw_grads(w, sets[k, r], w.psi, k + 1, r, w.loss_scale, sv)
     del sv
     buf.set_scaler(w.loss_scale, 0, 0)
-    hyp = Z.hyper(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay, w.max_norm, Z.ZERO_MODE_AUTO)
+    hyp = Z.hyper(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay, w.max_norm,
+                  Z.ZERO_MODE_AUTO if mode is None else mode)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda") if flush_l2 else None
     rows = lambda k: [sets[k, r] for r in range(N)]
     for i in range(warmup):
@@ -507,7 +509,8 @@ def bench_stage3(w, buckets, steps, warmup, torch, S, Z, flush_l2=False):
         S.draw_grads(w, gbuf[r], lmax, 1, r, w.loss_scale)
     outs = torch.empty((N, lpad), dtype=td, device="cuda")
     buf.set_scaler(w.loss_scale, 0, 0)
-    hyp = Z.hyper(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay, w.max_norm, Z.ZERO_MODE_AUTO)
+    hyp = Z.hyper(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay, w.max_norm,
+                  Z.ZERO_MODE_AUTO if mode is None else mode)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda") if flush_l2 else None
     grows = [gbuf[r] for r in range(N)]
     orows = [outs[r] for r in range(N)]
@@ -849,6 +852,10 @@ def run_other(args, ws, rank, local):
         ms, bps, st = bench_dense(w, 2, args.steps, args.warmup, torch, S, Z)
         lines.append(_line(w.name, w.psi / (ms * 1e-3), ms, args.steps, args.warmup, bps, w.dtype,
                            {"stage": 2, "mode": "speculative one pass; a step whose norm exceeds 1.0 is redone",
+                            "l2": "inputs larger than L2"}))
+        ms, bps, st = bench_dense(w, 2, args.steps, args.warmup, torch, S, Z, mode=Z.ZERO_MODE_TWO_PASS_WS)
+        lines.append(_line(w.name + "_two_pass", w.psi / (ms * 1e-3), ms, args.steps, args.warmup, bps, w.dtype,
+                           {"stage": 2, "mode": "two-pass: fp32 g_hat to the workspace, clip decided before the update",
                             "l2": "inputs larger than L2"}))
     elif args.workload == "llama7b":
         w = S.LLAMA7B

@@ -24,8 +24,8 @@
  *    on error the call launches nothing and zero_last_error() says why.
  *  - All tensor arguments are caller-owned DEVICE pointers (the caller
  *    allocates them, e.g. with PyTorch) unless a comment says "host".  The
- *    library owns only its small workspace (status word, per-block norm
- *    partials, and for some modes an fp32 gradient buffer of psi_pad floats).
+ *    library owns only its workspace (status word, norm partials, chunk
+ *    counters, and for some modes an fp32 gradient buffer of psi_pad floats).
  *  - Device pointers must be 16-byte aligned.  The 128-bit vector path runs
  *    when psi_pad (or a bucket's bounds) are multiples of 8; otherwise an
  *    element-wise path runs with the same arithmetic.
@@ -338,10 +338,10 @@ ZERO_API int zero_bytes_moved(zero_handle_t h, zero_bytes_t* out);
  * budget fixed before training starts.  zero_init_partition allocates a
  * workspace, so those callers use this call instead.  It takes no handle
  * and calls no cudaMalloc, cudaFree or other allocating routine.
- *   Its scratch -- the status word, the per-block norm partials and the
- *   fp32 averaged gradient -- lives in one static device array of
- *   ZERO_NOALLOC_MAX_PSI_PAD floats plus 48 KiB and 256 bytes (about
- *   16 MiB), which every GPU that loads the library holds until the
+ *   Its scratch -- the status word, the norm partials, the chunk counters
+ *   and the fp32 averaged gradient -- lives in one static device array of
+ *   ZERO_NOALLOC_MAX_PSI_PAD floats plus 84,832 bytes (about 16.1 MiB),
+ *   which every GPU that loads the library holds until the
  *   process exits.  psi_pad above ZERO_NOALLOC_MAX_PSI_PAD is rejected
  *   with ZERO_EINVAL.
  *   The first call on a device looks up that array's device address

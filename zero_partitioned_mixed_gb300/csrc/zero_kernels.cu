@@ -4,9 +4,10 @@
 // collective becomes an HBM stream fused into an update kernel:
 //   reduce-scatter  -> every thread reads the N ranks' 16-bit gradients of
 //                      its 8 elements and sums them in rank order in fp32;
-//   scalar all-reduce of the norm and overflow flag -> per-block partials
-//                      that the last block to finish reduces in a fixed
-//                      order (a ticket counter, no spinning);
+//   scalar all-reduce of the norm and overflow flag -> partials per chunk
+//                      of work (and per group of chunks) that the last
+//                      block to finish sums in a fixed order (a ticket
+//                      counter, no spinning);
 //   all-gather / broadcast -> the thread writes the RNE-cast 16-bit result
 //                      to all N replicas.
 // Every kernel is an HBM-bound stream: 128-bit (16-bit data) and 256-bit

@@ -10,7 +10,7 @@
 // such callers cannot use the handle-based entry points.
 //
 // Instead, every piece of scratch this path needs -- the status word, the
-// per-block norm partials and flags, and the fp32 averaged gradient of up to
+// norm partials and flags, the chunk counters, and the fp32 averaged gradient of up to
 // kNoAllocMaxPsiPad elements -- lives in one file-scope __device__ array.
 // Each GPU that loads the library holds that array until the process exits.
 // The kernels are the library's existing two-pass kernels; only the place
