@@ -510,7 +510,7 @@ def bench_stage3(w, buckets, steps, warmup, torch, S, Z, flush_l2=False):
     outs = torch.empty((N, lpad), dtype=td, device="cuda")
     buf.set_scaler(w.loss_scale, 0, 0)
     hyp = Z.hyper(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay, w.max_norm,
-                  Z.ZERO_MODE_AUTO if mode is None else mode)
+                  Z.ZERO_MODE_AUTO)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda") if flush_l2 else None
     grows = [gbuf[r] for r in range(N)]
     orows = [outs[r] for r in range(N)]
