@@ -129,8 +129,11 @@ def _ptr(x) -> Optional[int]:
 
 
 def _ptr_array(xs: Optional[Sequence]):
+    """A C array of device pointers; an array built earlier passes through."""
     if xs is None:
         return None
+    if isinstance(xs, C.Array):
+        return xs
     arr = (C.c_void_p * max(1, len(xs)))()
     for i, x in enumerate(xs):
         arr[i] = _ptr(x)

@@ -27,7 +27,11 @@ def _round8(x: int) -> int:
 
 
 class RankBuffers:
-    """A handle plus the caller-owned buffers of one partitioned flat model."""
+    """A handle plus the caller-owned buffers of one partitioned flat model.
+
+    grads and params are written in place (the handle keeps their row
+    pointers); rebinding the attributes to other tensors is not supported.
+    """
 
     def __init__(self, psi: int, n_ranks: int, stage: int, dtype: str = "bf16", align: int = 8,
                  double_buffer: bool = True, device="cuda", alloc_grads: bool = True):
@@ -52,6 +56,10 @@ class RankBuffers:
         self.master = torch.zeros(size, dtype=torch.float32, device=device)
         self.m = torch.zeros(size, dtype=torch.float32, device=device)
         self.v = torch.zeros(size, dtype=torch.float32, device=device)
+        # the rows never move: their pointer arrays are built once (at N = 32
+        # building them costs more host time than the step's GPU time)
+        self._grad_ptrs = B._ptr_array(self.grad_rows()) if self.grads is not None else None
+        self._param_ptrs = B._ptr_array(self.param_rows())
 
     # -- views
     def grad_rows(self) -> List[torch.Tensor]:
@@ -77,9 +85,9 @@ class RankBuffers:
 
     def step(self, hyp, grads: Optional[List] = None, stream=None):
         if self.stage == 3:
-            B.zero_step(self.h, None, self.param_rows(), self.master, self.m, self.v, hyp, stream)
+            B.zero_step(self.h, None, self._param_ptrs, self.master, self.m, self.v, hyp, stream)
         else:
-            B.zero_step(self.h, grads if grads is not None else self.grad_rows(), self.param_rows(),
+            B.zero_step(self.h, grads if grads is not None else self._grad_ptrs, self._param_ptrs,
                         self.master, self.m, self.v, hyp, stream)
 
     def gather(self, a: int, b: int, out: List, stream=None):
@@ -89,14 +97,14 @@ class RankBuffers:
         """Reduce-scatter of one bucket: stage 3, or stage 2 reduced during backward."""
         if self.stage == 2:
             B.zero_reduce_scatter_bucket_replicas(self.h, a, b, grads, self.master, self.m, self.v,
-                                                  self.param_rows(), hyp, stream)
+                                                  self._param_ptrs, hyp, stream)
         else:
             B.zero_reduce_scatter_bucket(self.h, a, b, grads, self.master, self.m, self.v, self.params, hyp,
                                          stream)
 
     def finish_bucketed_step(self, hyp, stream=None):
         """zero_step after the step's buckets were reduce-scattered (stages 2 and 3)."""
-        B.zero_step(self.h, None, self.param_rows(), self.master, self.m, self.v, hyp, stream)
+        B.zero_step(self.h, None, self._param_ptrs, self.master, self.m, self.v, hyp, stream)
 
     def status(self, stream=None) -> dict:
         return B.zero_get_status(self.h, stream)
