@@ -512,8 +512,8 @@ def bench_stage3(w, buckets, steps, warmup, torch, S, Z, flush_l2=False):
     hyp = Z.hyper(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay, w.max_norm,
                   Z.ZERO_MODE_AUTO)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda") if flush_l2 else None
-    grows = [gbuf[r] for r in range(N)]
-    orows = [outs[r] for r in range(N)]
+    grows = Z.pointer_array([gbuf[r] for r in range(N)])
+    orows = Z.pointer_array([outs[r] for r in range(N)])
 
     def one_step(tg, tr, tf):
         for (a, b) in buckets:
@@ -675,7 +675,7 @@ def bench_schedule(w, buckets, steps, warmup, torch, S, Z, prefetch, graph):
     gbuf = torch.empty((N, (lmax + 7) // 8 * 8), dtype=td, device="cuda")
     for r in range(N):
         S.draw_grads(w, gbuf[r], lmax, 1, r, w.loss_scale)
-    rows = [gbuf[r] for r in range(N)]
+    rows = Z.pointer_array([gbuf[r] for r in range(N)])
     buf.set_scaler(w.loss_scale, 0, 0)
     hyp = Z.hyper(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay, w.max_norm, Z.ZERO_MODE_AUTO)
     sched = Zero3Schedule(buf, buckets, prefetch=prefetch)
@@ -723,7 +723,7 @@ def bench_persist(shapes, name, threshold, steps, warmup, torch, S, Z, graph):
     gbuf = torch.empty((N, (lmax + 7) // 8 * 8), dtype=td, device="cuda")
     for r in range(N):
         S.draw_grads(w, gbuf[r], lmax, 1, r, w.loss_scale)
-    rows = [gbuf[r] for r in range(N)]
+    rows = Z.pointer_array([gbuf[r] for r in range(N)])
     buf.set_scaler(w.loss_scale, 0, 0)
     hyp = Z.hyper(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay, w.max_norm, Z.ZERO_MODE_AUTO)
     sched = Zero3Schedule(buf, buckets, prefetch=True, persistent_from=lay.persistent_from(P))

@@ -17,5 +17,5 @@ from ._binding import (  # noqa: F401
     zero_reduce_scatter_bucket, zero_reduce_scatter_bucket_replicas, zero_set_scaler, zero_step,
     zero_step_noalloc, zero_quantize_blocks, zero_dequantize_blocks, zero_gather_bucket_q8,
     zero_reduce_scatter_bucket_q, ZERO_Q_BLOCK,
-    result_from_device,
+    result_from_device, pointer_array,
 )

@@ -140,6 +140,14 @@ def _ptr_array(xs: Optional[Sequence]):
     return arr
 
 
+def pointer_array(tensors: Sequence):
+    """The C array of the tensors' device pointers, for calls that are made
+    again and again with the same rows: every call that takes a list of
+    tensors also takes this array, and skips converting the list.  The
+    tensors must stay alive, and in place, while the array is in use."""
+    return _ptr_array(list(tensors))
+
+
 def _stream(stream) -> Optional[int]:
     if stream is None:
         import torch

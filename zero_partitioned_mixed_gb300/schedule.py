@@ -41,7 +41,7 @@ class Zero3Schedule:
 
     buf: a stage-3 RankBuffers; buckets: [(a, b)] tiling [0, psi_pad).
     grad_rows(i) -> list of N device tensors holding rank r's gradient of
-    bucket i (the caller's backward writes them); forward(i, rows) and
+    bucket i (the caller's backward writes them), or their pointer_array; forward(i, rows) and
     backward(i, rows) are the caller's per-bucket work on the gathered
     16-bit parameters (default: none).
     """
@@ -68,12 +68,15 @@ class Zero3Schedule:
         if self.p0 < P:
             lp = max(8, (P - self.p0 + 7) // 8 * 8)
             self.resident = torch.empty((buf.n, lp), dtype=buf.params.dtype, device=buf.params.device)
+            self._resident_ptrs = B.pointer_array([self.resident[r] for r in range(buf.n)])
         sizes = [self.buckets[i][1] - self.buckets[i][0] for i in self.gathered]
         lmax = max(sizes) if sizes else 0
         lpad = max(8, (lmax + 7) // 8 * 8)
         td = buf.params.dtype
         nsets = 2 if prefetch else 1
         self.outs = [torch.empty((buf.n, lpad), dtype=td, device=buf.params.device) for _ in range(nsets)]
+        # the library calls take the rows' pointer arrays, built once
+        self._out_ptrs = [B.pointer_array([o[r] for r in range(buf.n)]) for o in self.outs]
         self.side = torch.cuda.Stream(device=buf.params.device) if prefetch else None
         self.graph: Optional[torch.cuda.CUDAGraph] = None
 
@@ -88,7 +91,7 @@ class Zero3Schedule:
         if not self.prefetch:
             for i in order:
                 a, b = self.buckets[i]
-                buf.gather(a, b, self._rows(0), main)
+                buf.gather(a, b, self._out_ptrs[0], main)
                 if work is not None:
                     work(i, self._rows(0))
                 if rs is not None:
@@ -104,7 +107,7 @@ class Zero3Schedule:
             a, b = self.buckets[order[k]]
             self.side.wait_event(free[k % 2])
             with torch.cuda.stream(self.side):
-                buf.gather(a, b, self._rows(k), self.side)
+                buf.gather(a, b, self._out_ptrs[k % len(self.outs)], self.side)
                 ready[k].record(self.side)
 
         if n:
@@ -129,7 +132,7 @@ class Zero3Schedule:
     def refresh(self) -> None:
         """Gather [p0, psi_pad) from the owners' shards into the resident copies."""
         if self.resident is not None:
-            self.buf.gather(self.p0, self.buf.psi_pad, self.resident_rows(), torch.cuda.current_stream())
+            self.buf.gather(self.p0, self.buf.psi_pad, self._resident_ptrs, torch.cuda.current_stream())
             self._fresh = True
 
     def step(self, hyp, grad_rows: Callable[[int], List[torch.Tensor]],
