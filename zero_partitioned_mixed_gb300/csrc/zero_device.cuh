@@ -8,6 +8,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <mutex>
+
 #include "zero_internal.h"
 
 namespace zg {
@@ -475,22 +477,44 @@ __device__ void reset_groups(const Workspace& ws, uint64_t nchunks) {
 // Launch on a persistent grid: as many CTAs as fit on the SMs at once (from
 // the occupancy API), or fewer when `units` (vectors) need fewer, capped at
 // the per-block partial slots.
+// CTAs of `kernel` resident at once on device `dev` (SMs x CTAs per SM),
+// queried once per kernel and device: the occupancy query costs more host
+// time than a small launch.
 template <typename KernelT>
-cudaError_t run(KernelT kernel, const Args& a, uint64_t nvec, cudaStream_t s, int* grid_out) {
-    static int sms = 0;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+cudaError_t resident_ctas(KernelT kernel, int dev, uint64_t* out) {
+    struct Entry {
+        const void* kernel;
+        int dev;
+        uint64_t ctas;
+    };
+    static Entry cache[512];
+    static int used = 0;
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; ++i)
+        if (cache[i].kernel == reinterpret_cast<const void*>(kernel) && cache[i].dev == dev) {
+            *out = cache[i].ctas;
+            return cudaSuccess;
+        }
+    int sms = 0, per_sm = 0;
+    cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    if (sms == 0) {
-        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
-    }
-    int per_sm = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) per_sm = 1;
+    *out = static_cast<uint64_t>(sms) * static_cast<uint64_t>(per_sm);
+    if (used < 512) cache[used++] = Entry{reinterpret_cast<const void*>(kernel), dev, *out};
+    return cudaSuccess;
+}
+
+template <typename KernelT>
+cudaError_t run(KernelT kernel, const Args& a, uint64_t nvec, cudaStream_t s, int* grid_out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    uint64_t cap = 0;
+    if ((e = resident_ctas(kernel, dev, &cap)) != cudaSuccess) return e;
     uint64_t want = (nvec + kThreads - 1) / kThreads;
-    uint64_t cap = static_cast<uint64_t>(sms) * static_cast<uint64_t>(per_sm);
     if (cap > static_cast<uint64_t>(kMaxBlocks)) cap = kMaxBlocks;
     uint64_t grid = want < cap ? want : cap;
     if (grid < 1) grid = 1;
