@@ -412,7 +412,7 @@ def test_overflow_stops_the_pass_early(stage, where):
 
 
 @pytest.mark.parametrize("psi,bucket", [(6_000_001, 1_000_000), (40_000_003, 36_000_000)])
-@pytest.mark.parametrize("stage,mode", [(1, 3), (2, 1), (3, 0)])
+@pytest.mark.parametrize("stage,mode", [(1, 3), (2, 1), (3, 0), (1, 4)])
 def test_norm_is_bitwise_deterministic(stage, mode, psi, bucket):
     # CTAs take chunks of work in whatever order they reach the counter, but
     # norm partials are formed per chunk, then per group of chunks (launches
@@ -429,7 +429,7 @@ def test_norm_is_bitwise_deterministic(stage, mode, psi, bucket):
     master0 = torch.randn(psi, generator=g, device="cuda") * 0.02
     runs = []
     for _ in range(3):
-        buf = RankBuffers(psi, n, stage, "bf16", double_buffer=(mode in (0, 3)))
+        buf = RankBuffers(psi, n, stage, "bf16", double_buffer=(mode in (0, 3, 4)))
         P = buf.psi_pad
         mv, _, _ = buf.state(0)
         mv[:psi].copy_(master0)
