@@ -80,3 +80,17 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     with pytest.raises(B.ZeroError) as e:
         B.load_library()
     assert "build" in str(e.value)
+
+
+def test_pointer_array_holds_the_rows_and_passes_through():
+    # pointer_array(rows) is what every list-taking call builds internally;
+    # a prebuilt array must reach the C call unchanged
+    import ctypes
+    import torch
+    from zero_partitioned_mixed_gb300 import _binding as B
+    rows = [torch.empty(16) for _ in range(5)]
+    arr = B.pointer_array(rows)
+    assert isinstance(arr, ctypes.Array) and len(arr) == 5
+    assert [arr[i] for i in range(5)] == [t.data_ptr() for t in rows]
+    assert B._ptr_array(arr) is arr
+    assert B._ptr_array(None) is None
