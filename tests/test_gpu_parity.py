@@ -463,3 +463,19 @@ def test_overflow_stop_on_the_grouped_path():
                   inject=[(1, 3, 12_000_000, INF)])
     st.check()
     assert st.mismatches == 0, st
+
+
+@pytest.mark.parametrize("chunks", [456, 457, 915])
+@pytest.mark.parametrize("stage", [1, 3])
+def test_chunk_counts_around_the_grid(stage, chunks):
+    # The step and reduce-scatter kernels run 3 CTAs of 256 threads per SM
+    # (456 on a GB300) and hand out chunks of 256 vectors at these sizes: a
+    # CTA's first chunk is its own index, later ones come from the counter.
+    # Exactly one chunk per CTA, one chunk more, and two rounds plus three.
+    n = 8
+    psi = chunks * 256 * 8 - 5   # the last chunk ragged
+    inject = [(1, 3, psi - 2, INF)]
+    st = run_case(psi, n, stage, "bf16", steps=3, mode=3 if stage == 1 else 0, double_buffer=True,
+                  inject=inject, buckets=[(0, (psi + 63) // 64 * 64)] if stage == 3 else None)
+    st.check()
+    assert st.mismatches == 0, st
