@@ -479,3 +479,31 @@ def test_chunk_counts_around_the_grid(stage, chunks):
                   inject=inject, buckets=[(0, (psi + 63) // 64 * 64)] if stage == 3 else None)
     st.check()
     assert st.mismatches == 0, st
+
+
+@pytest.mark.parametrize("stage", [1, 3])
+def test_missing_rank_is_refused(stage):
+    # a rank whose gradient (or, stage 3, bucket) row is missing: ZERO_EINVAL
+    # before any launch, and the handle stays usable
+    from zero_partitioned_mixed_gb300 import _binding as B
+    n = 4
+    h = B.zero_init_partition(4096, n, stage, B.ZERO_BF16, 8, B.ZERO_F_DOUBLE_BUFFER)
+    try:
+        P = B.zero_partition_info(h)[0]
+        rows = [torch.zeros(P, dtype=torch.bfloat16, device="cuda") for _ in range(n)]
+        rows[2] = None
+        master, m, v = (torch.zeros(2 * P, device="cuda") for _ in range(3))
+        if stage == 3:
+            shard = torch.zeros(P, dtype=torch.bfloat16, device="cuda")
+            with pytest.raises(B.ZeroError, match="ZERO_EINVAL"):
+                B.zero_reduce_scatter_bucket(h, 0, P, rows, master, m, v, shard, B.hyper())
+        else:
+            params = [torch.zeros(P, dtype=torch.bfloat16, device="cuda") for _ in range(n)]
+            with pytest.raises(B.ZeroError, match="ZERO_EINVAL"):
+                B.zero_step(h, rows, params, master, m, v, B.hyper())
+            rows[2] = torch.zeros(P, dtype=torch.bfloat16, device="cuda")
+            B.zero_step(h, rows, params, master, m, v, B.hyper())
+            torch.cuda.synchronize()
+            assert B.zero_get_status(h)["steps_applied"] == 1
+    finally:
+        B.zero_destroy(h)
