@@ -73,15 +73,18 @@ def build_library(force: bool = False, verbose: bool = False) -> str:
     if not force and not _stale():
         return LIB_PATH
     os.makedirs(BUILD_DIR, exist_ok=True)
-    tmp = LIB_PATH + ".tmp"
+    # a name of this process's own: several processes (ranks) may build at
+    # once; each renames its finished library into place atomically
+    tmp = f"{LIB_PATH}.{os.getpid()}.tmp"
     cmd = nvcc_command(out=tmp)
     proc = subprocess.run(cmd, capture_output=True, text=True)
-    log = os.path.join(BUILD_DIR, "build.log")
+    log = os.path.join(BUILD_DIR, f"build.{os.getpid()}.log")
     with open(log, "w") as f:
         f.write(" ".join(cmd) + "\n\n" + proc.stdout + proc.stderr)
     if proc.returncode != 0:
         raise RuntimeError("building libzero_gb300.so failed:\n" + proc.stdout + proc.stderr)
     os.replace(tmp, LIB_PATH)
+    os.replace(log, os.path.join(BUILD_DIR, "build.log"))
     if verbose:
         sys.stdout.write(proc.stdout + proc.stderr)
     return LIB_PATH
