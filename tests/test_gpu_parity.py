@@ -507,3 +507,16 @@ def test_missing_rank_is_refused(stage):
             assert B.zero_get_status(h)["steps_applied"] == 1
     finally:
         B.zero_destroy(h)
+
+
+def test_double_buffer_chosen_from_free_memory():
+    # double_buffer=None: the second state slot is taken when it fits in
+    # free device memory, and not when it cannot (AUTO then runs two-pass)
+    from zero_partitioned_mixed_gb300.buffers import RankBuffers
+    free, _ = torch.cuda.mem_get_info()
+    assert RankBuffers.second_slot_fits(1 << 20, 8, 3)
+    too_big = int(free // 12) + (1 << 20)      # one state slot alone exceeds free memory
+    assert not RankBuffers.second_slot_fits(too_big, 8, 3, alloc_grads=False)
+    buf = RankBuffers(1 << 20, 8, 3, "bf16", double_buffer=None)
+    assert buf.double_buffer
+    buf.close()

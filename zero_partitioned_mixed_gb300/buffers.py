@@ -34,9 +34,11 @@ class RankBuffers:
     """
 
     def __init__(self, psi: int, n_ranks: int, stage: int, dtype: str = "bf16", align: int = 8,
-                 double_buffer: bool = True, device="cuda", alloc_grads: bool = True):
+                 double_buffer: Optional[bool] = True, device="cuda", alloc_grads: bool = True):
         if stage == 0:
             double_buffer = False
+        if double_buffer is None:
+            double_buffer = self.second_slot_fits(psi, n_ranks, stage, align, alloc_grads, device)
         self.psi, self.n, self.stage, self.dtype = psi, n_ranks, stage, dtype
         self.double_buffer = double_buffer
         self.h = B.zero_init_partition(psi, n_ranks, stage, _ZDT[dtype], align,
@@ -60,6 +62,21 @@ class RankBuffers:
         # building them costs more host time than the step's GPU time)
         self._grad_ptrs = B._ptr_array(self.grad_rows()) if self.grads is not None else None
         self._param_ptrs = B._ptr_array(self.param_rows())
+
+    @staticmethod
+    def second_slot_fits(psi: int, n_ranks: int, stage: int, align: int = 8, alloc_grads: bool = True,
+                         device="cuda", margin: float = 0.05) -> bool:
+        """Whether the speculative mode's second master/m/v slot fits in the
+        device's free memory next to everything else these buffers hold
+        (with a 5 % margin); when it does not, single-buffered state makes
+        the library's AUTO mode take the two-pass step instead."""
+        unit = n_ranks * align
+        pp = (psi + unit - 1) // unit * unit
+        stride = max(8, _round8(pp))
+        sixteen = 2 * stride * ((n_ranks if alloc_grads and stage != 3 else 0) + (1 if stage == 3 else n_ranks))
+        state_one = 3 * 4 * pp
+        free, _ = torch.cuda.mem_get_info(torch.device(device))
+        return sixteen + 2 * state_one <= free * (1.0 - margin)
 
     # -- views
     def grad_rows(self) -> List[torch.Tensor]:
