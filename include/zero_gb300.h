@@ -31,6 +31,11 @@
  *    element-wise path runs with the same arithmetic.
  *  - Calls are asynchronous on the given CUDA stream (a cudaStream_t passed
  *    as void*, NULL = legacy default stream).  One host thread per handle.
+ *    The reduce-scatters and steps of one handle share its status word and
+ *    norm partials, so they must run in order (one stream, or ordered by
+ *    events); gathers may overlap them on another stream.  At most 64
+ *    launches of one handle may be in flight at once: each takes the next
+ *    of 64 work counters, round-robin.
  *  - Elements [psi, psi_pad) are padding: gradients there are ignored, and
  *    master/m/v/params there are written as 0.
  *  - The loss scale, the count t of applied Adam steps and the live slot of
