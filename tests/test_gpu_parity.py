@@ -411,12 +411,12 @@ def test_overflow_stops_the_pass_early(stage, where):
     assert st.mismatches == 0, st
 
 
-@pytest.mark.parametrize("psi,bucket", [(6_000_001, 1_000_000), (40_000_003, 36_000_000)])
+@pytest.mark.parametrize("psi,bucket", [(6_000_001, 1_000_000), (140_000_003, 36_000_000)])
 @pytest.mark.parametrize("stage,mode", [(1, 3), (2, 1), (3, 0), (1, 4)])
 def test_norm_is_bitwise_deterministic(stage, mode, psi, bucket):
     # CTAs take chunks of work in whatever order they reach the counter, but
     # norm partials are formed per chunk, then per group of chunks (launches
-    # of more than 4096 chunks: the 40M case), in a fixed order: repeated
+    # of more than 4096 chunks: the 140M case), in a fixed order: repeated
     # runs give the same bits.
     import struct
     from zero_partitioned_mixed_gb300 import _binding as B
@@ -454,13 +454,14 @@ def test_norm_is_bitwise_deterministic(stage, mode, psi, bucket):
 
 
 def test_overflow_stop_on_the_grouped_path():
-    # 40M elements over 4 ranks: 5M vectors, 4883 chunks of 1024 -- above
-    # the 4096 chunks summed directly, so norm partials go through group
-    # tickets.  An inf at 30 % stops the pass with groups left incomplete;
-    # the finaliser must reset their tickets (the next steps' norms and every
-    # element of state and replicas must still match the oracle).
-    st = run_case(40_000_003, 4, 1, "bf16", steps=3, mode=3, double_buffer=True, sigma=1e-3,
-                  inject=[(1, 3, 12_000_000, INF)])
+    # 140M elements over 2 ranks: 17.5M vectors, 4273 chunks of 16 x 256 --
+    # above the 4096 chunks summed directly, so norm partials go through
+    # group tickets.  An inf at 30 % stops the pass with groups left
+    # incomplete; the finaliser must reset their tickets (the next steps'
+    # norms and every element of state and replicas must still match the
+    # oracle).
+    st = run_case(140_000_003, 2, 1, "bf16", steps=3, mode=3, double_buffer=True, sigma=1e-3,
+                  inject=[(1, 1, 42_000_000, INF)])
     st.check()
     assert st.mismatches == 0, st
 

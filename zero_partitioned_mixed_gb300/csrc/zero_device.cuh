@@ -524,9 +524,9 @@ cudaError_t run(KernelT kernel, const Args& a, uint64_t nvec, cudaStream_t s, in
 }
 
 // Launch a chunked kernel: the persistent grid, but no more CTAs than chunks.
-template <typename KernelT>
+template <int UMAX = kChunkU, typename KernelT>
 cudaError_t run_chunked(KernelT kernel, const Args& a, uint64_t nvec, cudaStream_t s, int* grid_out) {
-    return run(kernel, a, chunk_total(nvec) * kThreads, s, grid_out);
+    return run(kernel, a, chunk_total<UMAX>(nvec) * kThreads, s, grid_out);
 }
 
 }  // namespace

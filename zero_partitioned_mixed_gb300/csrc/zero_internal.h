@@ -28,16 +28,21 @@ constexpr int kCtrSlots = 64;       // launches of one handle that may be in fli
 // 1) for small ones, so that a launch has about kMinChunks chunks or more --
 // enough for every CTA of the persistent grid.  A function of the launch's
 // size only, so the chunk partials stay deterministic.
+// UMAX is the kernel's own cap (the stage 1/2 step measured best at 16,
+// the stage-3 kernels at kChunkU); a larger cap only lowers the count.
 constexpr uint64_t kMinChunks = 2048;
+template <int UMAX = kChunkU>
 __host__ __device__ inline int chunk_u(uint64_t nvec) {
     const uint64_t u = nvec / (static_cast<uint64_t>(kThreads) * kMinChunks);
-    return u >= static_cast<uint64_t>(kChunkU) ? kChunkU : (u < 1 ? 1 : static_cast<int>(u));
+    return u >= static_cast<uint64_t>(UMAX) ? UMAX : (u < 1 ? 1 : static_cast<int>(u));
 }
+template <int UMAX = kChunkU>
 __host__ __device__ inline uint64_t chunk_len(uint64_t nvec) {
-    return static_cast<uint64_t>(chunk_u(nvec)) * kThreads;
+    return static_cast<uint64_t>(chunk_u<UMAX>(nvec)) * kThreads;
 }
+template <int UMAX = kChunkU>
 __host__ __device__ inline uint64_t chunk_total(uint64_t nvec) {
-    const uint64_t len = chunk_len(nvec);
+    const uint64_t len = chunk_len<UMAX>(nvec);
     return (nvec + len - 1) / len;
 }
 
