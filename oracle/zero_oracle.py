@@ -24,7 +24,7 @@ Sources (web pages on ZeRO; cited by title and section):
   owner, ZeRO-3 broadcast from owner before forward and again before
   backward.
 
-Readings taken where the pages are silent (each is listed in the design doc):
+Readings taken where the pages are silent:
 
 * Adam: Kingma & Ba with the eps added to the bias-corrected sqrt(v);
   written with t = number of applied steps + 1 and these fp32 operations,
