@@ -414,6 +414,17 @@ def test_overflow_stops_the_pass_early(stage, where):
 @pytest.mark.parametrize("psi,bucket", [(6_000_001, 1_000_000), (140_000_003, 36_000_000)])
 @pytest.mark.parametrize("stage,mode", [(1, 3), (2, 1), (3, 0), (1, 4)])
 def test_norm_is_bitwise_deterministic(stage, mode, psi, bucket):
+    _repeat_bitwise(stage, mode, psi, bucket, 8)
+
+
+@pytest.mark.parametrize("n", [2, 4])
+def test_norm_is_bitwise_deterministic_long_rs_chunks(n):
+    # with N <= 4 the reduce-scatter takes chunks of up to 16 x 256 vectors;
+    # one 140M bucket gives 4273 of them (more than 4096: grouped sums)
+    _repeat_bitwise(3, 0, 140_000_003, 140_000_064, n)
+
+
+def _repeat_bitwise(stage, mode, psi, bucket, n):
     # CTAs take chunks of work in whatever order they reach the counter, but
     # norm partials are formed per chunk, then per group of chunks (launches
     # of more than 4096 chunks: the 140M case), in a fixed order: repeated
@@ -421,7 +432,6 @@ def test_norm_is_bitwise_deterministic(stage, mode, psi, bucket):
     import struct
     from zero_partitioned_mixed_gb300 import _binding as B
     from zero_partitioned_mixed_gb300.buffers import RankBuffers
-    n = 8
     g = torch.Generator(device="cuda")
     g.manual_seed(23)
     width = (psi + 8 * n - 1) // (8 * n) * (8 * n)
@@ -462,6 +472,22 @@ def test_overflow_stop_on_the_grouped_path():
     # oracle).
     st = run_case(140_000_003, 2, 1, "bf16", steps=3, mode=3, double_buffer=True, sigma=1e-3,
                   inject=[(1, 1, 42_000_000, INF)])
+    st.check()
+    assert st.mismatches == 0, st
+
+
+@pytest.mark.parametrize("psi,n,buckets", [
+    # N = 4: the reduce-scatter's chunks grow to 5 x 256 vectors on the 24M
+    # buckets (2344 chunks, summed directly) and the gather runs full
+    # 4-vector batches; an 8-element bucket between them, and the last
+    # bucket ends in the padding
+    (48_000_005, 4, [(0, 24_000_000), (24_000_000, 24_000_008), (24_000_008, 48_000_032)]),
+    # N = 2, one 140M bucket: 16 x 256-vector chunks, 4273 of them -- above
+    # the 4096 summed directly, so the norm goes through group tickets
+    (140_000_003, 2, None),
+])
+def test_stage3_long_chunks_few_ranks(psi, n, buckets):
+    st = run_case(psi, n, 3, "bf16", steps=2, buckets=buckets, double_buffer=True, sigma=1e-3)
     st.check()
     assert st.mismatches == 0, st
 

@@ -474,46 +474,54 @@ __device__ void reset_groups(const Workspace& ws, uint64_t nchunks) {
     for (uint64_t g = threadIdx.x; g < ngroups; g += blockDim.x) ws.group_ticket[g] = 0u;
 }
 
-// Launch on a persistent grid: as many CTAs as fit on the SMs at once (from
-// the occupancy API), or fewer when `units` (vectors) need fewer, capped at
-// the per-block partial slots.
-// CTAs of `kernel` resident at once on device `dev` (SMs x CTAs per SM),
-// queried once per kernel and device: the occupancy query costs more host
-// time than a small launch.
+// CTAs of `kernel` resident at once on device `dev` (SMs x CTAs per SM, the
+// latter capped at per_sm when per_sm > 0), with the occupancy queried once
+// per kernel and device: the query costs more host time than a small launch.
 template <typename KernelT>
-cudaError_t resident_ctas(KernelT kernel, int dev, uint64_t* out) {
+cudaError_t resident_ctas(KernelT kernel, int dev, int per_sm_cap, uint64_t* out) {
     struct Entry {
         const void* kernel;
         int dev;
-        uint64_t ctas;
+        int sms;
+        int per_sm;
     };
     static Entry cache[512];
     static int used = 0;
     static std::mutex mu;
     std::lock_guard<std::mutex> lock(mu);
+    int sms = 0, per_sm = 0;
+    bool found = false;
     for (int i = 0; i < used; ++i)
         if (cache[i].kernel == reinterpret_cast<const void*>(kernel) && cache[i].dev == dev) {
-            *out = cache[i].ctas;
-            return cudaSuccess;
+            sms = cache[i].sms;
+            per_sm = cache[i].per_sm;
+            found = true;
+            break;
         }
-    int sms = 0, per_sm = 0;
-    cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0);
-    if (e != cudaSuccess) return e;
-    if (per_sm < 1) per_sm = 1;
+    if (!found) {
+        cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0);
+        if (e != cudaSuccess) return e;
+        if (per_sm < 1) per_sm = 1;
+        if (used < 512) cache[used++] = Entry{reinterpret_cast<const void*>(kernel), dev, sms, per_sm};
+    }
+    if (per_sm_cap > 0 && per_sm > per_sm_cap) per_sm = per_sm_cap;
     *out = static_cast<uint64_t>(sms) * static_cast<uint64_t>(per_sm);
-    if (used < 512) cache[used++] = Entry{reinterpret_cast<const void*>(kernel), dev, *out};
     return cudaSuccess;
 }
 
+// Launch on a persistent grid: as many CTAs as fit on the SMs at once (from
+// the occupancy API, or per_sm CTAs per SM when per_sm > 0 caps it lower),
+// or fewer when `nvec` vectors need fewer, capped at the per-block partial
+// slots.
 template <typename KernelT>
-cudaError_t run(KernelT kernel, const Args& a, uint64_t nvec, cudaStream_t s, int* grid_out) {
+cudaError_t run(KernelT kernel, const Args& a, uint64_t nvec, cudaStream_t s, int* grid_out, int per_sm = 0) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     uint64_t cap = 0;
-    if ((e = resident_ctas(kernel, dev, &cap)) != cudaSuccess) return e;
+    if ((e = resident_ctas(kernel, dev, per_sm, &cap)) != cudaSuccess) return e;
     uint64_t want = (nvec + kThreads - 1) / kThreads;
     if (cap > static_cast<uint64_t>(kMaxBlocks)) cap = kMaxBlocks;
     uint64_t grid = want < cap ? want : cap;
@@ -525,8 +533,15 @@ cudaError_t run(KernelT kernel, const Args& a, uint64_t nvec, cudaStream_t s, in
 
 // Launch a chunked kernel: the persistent grid, but no more CTAs than chunks.
 template <int UMAX = kChunkU, typename KernelT>
-cudaError_t run_chunked(KernelT kernel, const Args& a, uint64_t nvec, cudaStream_t s, int* grid_out) {
-    return run(kernel, a, chunk_total<UMAX>(nvec) * kThreads, s, grid_out);
+cudaError_t run_chunked(KernelT kernel, const Args& a, uint64_t nvec, cudaStream_t s, int* grid_out,
+                        int per_sm = 0) {
+    return run(kernel, a, chunk_total<UMAX>(nvec) * kThreads, s, grid_out, per_sm);
+}
+// The same with the chunk cap chosen at run time (the kernel computes the
+// same cap from its arguments).
+template <typename KernelT>
+cudaError_t run_chunked_u(KernelT kernel, const Args& a, uint64_t nvec, int umax, cudaStream_t s, int* grid_out) {
+    return run(kernel, a, chunk_total(nvec, umax) * kThreads, s, grid_out);
 }
 
 }  // namespace

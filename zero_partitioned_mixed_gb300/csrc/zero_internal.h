@@ -28,23 +28,27 @@ constexpr int kCtrSlots = 64;       // launches of one handle that may be in fli
 // 1) for small ones, so that a launch has about kMinChunks chunks or more --
 // enough for every CTA of the persistent grid.  A function of the launch's
 // size only, so the chunk partials stay deterministic.
-// UMAX is the kernel's own cap (the stage 1/2 step measured best at 16,
-// the stage-3 kernels at kChunkU); a larger cap only lowers the count.
+// UMAX is the kernel's own cap (the stage 1/2 step measured best at 16, the
+// gather at kChunkU, the reduce-scatter at 16 for N <= 4 and kChunkU above);
+// a larger cap only lowers the count.
 constexpr uint64_t kMinChunks = 2048;
-template <int UMAX = kChunkU>
-__host__ __device__ inline int chunk_u(uint64_t nvec) {
+__host__ __device__ inline int chunk_u(uint64_t nvec, int umax) {
     const uint64_t u = nvec / (static_cast<uint64_t>(kThreads) * kMinChunks);
-    return u >= static_cast<uint64_t>(UMAX) ? UMAX : (u < 1 ? 1 : static_cast<int>(u));
+    return u >= static_cast<uint64_t>(umax) ? umax : (u < 1 ? 1 : static_cast<int>(u));
 }
-template <int UMAX = kChunkU>
-__host__ __device__ inline uint64_t chunk_len(uint64_t nvec) {
-    return static_cast<uint64_t>(chunk_u<UMAX>(nvec)) * kThreads;
+__host__ __device__ inline uint64_t chunk_len(uint64_t nvec, int umax) {
+    return static_cast<uint64_t>(chunk_u(nvec, umax)) * kThreads;
 }
-template <int UMAX = kChunkU>
-__host__ __device__ inline uint64_t chunk_total(uint64_t nvec) {
-    const uint64_t len = chunk_len<UMAX>(nvec);
+__host__ __device__ inline uint64_t chunk_total(uint64_t nvec, int umax) {
+    const uint64_t len = chunk_len(nvec, umax);
     return (nvec + len - 1) / len;
 }
+template <int UMAX = kChunkU>
+__host__ __device__ inline int chunk_u(uint64_t nvec) { return chunk_u(nvec, UMAX); }
+template <int UMAX = kChunkU>
+__host__ __device__ inline uint64_t chunk_len(uint64_t nvec) { return chunk_len(nvec, UMAX); }
+template <int UMAX = kChunkU>
+__host__ __device__ inline uint64_t chunk_total(uint64_t nvec) { return chunk_total(nvec, UMAX); }
 
 // Chunks and groups of any launch over at most `elems` elements (worst case:
 // 1-wide vectors; below kChunkU vectors per thread a launch has fewer than
