@@ -300,8 +300,11 @@ __global__ void __launch_bounds__(kThreads) k_quantize(const __grid_constant__ A
 // shard (grads[0]) -> for every rank r: codes (params[r]) and scales (qdst[r]).
 // Chunked like the other persistent kernels (zero_device.cuh): a chunk is
 // U iterations of the CTA's 8 warps, kQUnrollGather blocks per warp each.
+// Six CTAs per SM (40 registers, no spill): the quantizing arithmetic wants
+// the extra warps; four per SM (56 registers) measured 2 % slower at N = 8
+// and 6 % at N = 2, and fewer per SM slower still.
 template <int DT>
-__global__ void __launch_bounds__(kThreads) k_gather_q8(const __grid_constant__ Args a) {
+__global__ void __launch_bounds__(kThreads, 6) k_gather_q8(const __grid_constant__ Args a) {
     __shared__ unsigned long long s_c[2];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint64_t nb = (a.count + kQBlock - 1) / kQBlock;
