@@ -417,6 +417,20 @@ class CallTimer:
         return sum(a.elapsed_time(b) for a, b in self.pairs)
 
 
+def _step_ms(parts: dict, wall: CallTimer, steps: int, flushed: bool) -> float:
+    """ms per step of a multi-call step: the device time from the step's first
+    call to its last (gaps between calls included), or, when an L2 flush runs
+    between the calls, the sum of the calls' own durations.  Records which
+    into `parts`, with the per-call sum beside it."""
+    calls = sum(v for k, v in parts.items() if k.endswith("_ms"))
+    parts["calls_ms"] = calls
+    if flushed:
+        parts["timing"] = "sum of the calls' durations (L2 flush between calls excluded)"
+        return calls
+    parts["timing"] = "first call to last call of each step, gaps included"
+    return wall.total_ms() / steps
+
+
 def _line(workload, value, ms, steps, warmup, bytes_per_step, dtype, extra=None):
     peaks, src = measured_peaks()
     gbs = bytes_per_step / (ms * 1e-3) / 1e9
@@ -534,13 +548,15 @@ def bench_stage3(w, buckets, steps, warmup, torch, S, Z, flush_l2=False):
     for _ in range(warmup):
         one_step(CallTimer(torch), CallTimer(torch), CallTimer(torch))
     torch.cuda.synchronize()
-    tg, tr, tf = CallTimer(torch), CallTimer(torch), CallTimer(torch)
+    tg, tr, tf, wall = CallTimer(torch), CallTimer(torch), CallTimer(torch), CallTimer(torch)
     before = _bytes_total(buf)
     for _ in range(steps):
-        one_step(tg, tr, tf)
-    bench_stage3.parts = {"gather_ms": tg.total_ms() / steps, "reduce_scatter_ms": tr.total_ms() / steps,
-                          "finish_ms": tf.total_ms() / steps}
-    ms = sum(bench_stage3.parts.values())
+        with wall:
+            one_step(tg, tr, tf)
+    parts = {"gather_ms": tg.total_ms() / steps, "reduce_scatter_ms": tr.total_ms() / steps,
+             "finish_ms": tf.total_ms() / steps}
+    ms = _step_ms(parts, wall, steps, flush is not None)
+    bench_stage3.parts = parts
     per_step = _bytes_delta(buf, before) / steps
     st = buf.status()
     buf.close()
@@ -579,11 +595,12 @@ def bench_stage2_buckets(w, bucket, steps, warmup, torch, S, Z):
 
     for _ in range(warmup):
         one_step(CallTimer(torch))
-    timer = CallTimer(torch)
+    timer, wall = CallTimer(torch), CallTimer(torch)
     before = _bytes_total(buf)
     for _ in range(steps):
-        one_step(timer)
-    ms = timer.total_ms() / steps
+        with wall:
+            one_step(timer)
+    ms = _step_ms({"calls_ms": timer.total_ms() / steps}, wall, steps, False)
     per_step = _bytes_delta(buf, before) / steps
     st = buf.status()
     buf.close()
@@ -643,13 +660,14 @@ def bench_stage3_zeropp(w, buckets, steps, warmup, torch, S, Z, bits):
 
     for _ in range(warmup):
         one_step(CallTimer(torch), CallTimer(torch), CallTimer(torch))
-    tg, tr, tf = CallTimer(torch), CallTimer(torch), CallTimer(torch)
+    tg, tr, tf, wall = CallTimer(torch), CallTimer(torch), CallTimer(torch), CallTimer(torch)
     before = _bytes_total(buf)
     for _ in range(steps):
-        one_step(tg, tr, tf)
+        with wall:
+            one_step(tg, tr, tf)
     parts = {"gather_ms": tg.total_ms() / steps, "reduce_scatter_ms": tr.total_ms() / steps,
              "finish_ms": tf.total_ms() / steps}
-    ms = sum(parts.values())
+    ms = _step_ms(parts, wall, steps, False)
     per_step = _bytes_delta(buf, before) / steps
     st = buf.status()
     buf.close()
