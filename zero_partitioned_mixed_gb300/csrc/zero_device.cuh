@@ -474,6 +474,20 @@ __device__ void reset_groups(const Workspace& ws, uint64_t nchunks) {
     for (uint64_t g = threadIdx.x; g < ngroups; g += blockDim.x) ws.group_ticket[g] = 0u;
 }
 
+// Programmatic dependent launch.  run() launches every kernel with
+// programmatic stream serialisation, so the next kernel in the stream may be
+// scheduled before this one has finished.  Every kernel launched through
+// run() therefore begins with pdl_enter(): it waits until the previous grid
+// in the stream has completed and its memory is visible (a no-op when the
+// kernel was not launched that way), and only then lets the next grid be
+// scheduled.  The next grid's CTAs take SM slots as this grid's CTAs leave
+// and wait there, which hides the launch latency between the kernels of a
+// step; no two kernels' memory accesses ever overlap.
+__device__ __forceinline__ void pdl_enter() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // CTAs of `kernel` resident at once on device `dev` (SMs x CTAs per SM, the
 // latter capped at per_sm when per_sm > 0), with the occupancy queried once
 // per kernel and device: the query costs more host time than a small launch.
@@ -514,7 +528,7 @@ cudaError_t resident_ctas(KernelT kernel, int dev, int per_sm_cap, uint64_t* out
 // Launch on a persistent grid: as many CTAs as fit on the SMs at once (from
 // the occupancy API, or per_sm CTAs per SM when per_sm > 0 caps it lower),
 // or fewer when `nvec` vectors need fewer, capped at the per-block partial
-// slots.
+// slots.  The kernel must begin with pdl_enter() (see above).
 template <typename KernelT>
 cudaError_t run(KernelT kernel, const Args& a, uint64_t nvec, cudaStream_t s, int* grid_out, int per_sm = 0) {
     int dev = 0;
@@ -527,8 +541,17 @@ cudaError_t run(KernelT kernel, const Args& a, uint64_t nvec, cudaStream_t s, in
     uint64_t grid = want < cap ? want : cap;
     if (grid < 1) grid = 1;
     if (grid_out) *grid_out = static_cast<int>(grid);
-    kernel<<<static_cast<unsigned>(grid), kThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, a);
 }
 
 // Launch a chunked kernel: the persistent grid, but no more CTAs than chunks.

@@ -41,6 +41,7 @@ constexpr int kStepChunkU = 16;
 // rollback kernel then restores the replicas).
 template <int DT, class IO>
 __global__ void __launch_bounds__(kThreads, 3) k_step_spec(const __grid_constant__ Args a) {
+    pdl_enter();
     constexpr int W = IO::W;
     __shared__ Pro pro;
     __shared__ unsigned long long s_c[2];
@@ -129,6 +130,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_step_spec(const __grid_constant
 // scalars for pass 2.
 template <int DT, class IO, bool WS>
 __global__ void __launch_bounds__(kThreads) k_reduce(const __grid_constant__ Args a) {
+    pdl_enter();
     constexpr int W = IO::W;
     __shared__ Pro pro;
     __shared__ unsigned long long s_c[2];
@@ -184,6 +186,7 @@ __global__ void __launch_bounds__(kThreads) k_reduce(const __grid_constant__ Arg
 // replicas (stages 1/2) or to the shard (stage 3, TO_SHARD).
 template <int DT, class IO, bool SRC_WS, bool TO_SHARD>
 __global__ void __launch_bounds__(kThreads) k_apply(const __grid_constant__ Args a) {
+    pdl_enter();
     constexpr int W = IO::W;
     __shared__ Pro pro;
     __shared__ unsigned long long s_c[2];
@@ -239,6 +242,7 @@ __global__ void __launch_bounds__(kThreads) k_apply(const __grid_constant__ Args
 // full replica of master/m/v (rank r at r*psi_pad) and updates all of it.
 template <int DT, class IO>
 __global__ void __launch_bounds__(kThreads, 3) k_apply_stage0(const __grid_constant__ Args a) {
+    pdl_enter();
     constexpr int W = IO::W;
     __shared__ Pro pro;
     __shared__ unsigned long long s_c[2];
@@ -294,6 +298,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_apply_stage0(const __grid_const
 // copies from the live (old) master; otherwise exit at once.
 template <int DT, class IO, bool TO_SHARD>
 __global__ void __launch_bounds__(kThreads) k_rollback(const __grid_constant__ Args a) {
+    pdl_enter();
     constexpr int W = IO::W;
     __shared__ unsigned long long s_c[2];
     const DevStatus* st = a.ws.status;
@@ -335,6 +340,7 @@ __global__ void __launch_bounds__(kThreads) k_rollback(const __grid_constant__ A
 // Otherwise exit at once.
 template <int DT, class IO>
 __global__ void __launch_bounds__(kThreads) k_fixup(const __grid_constant__ Args a) {
+    pdl_enter();
     constexpr int W = IO::W;
     __shared__ Pro pro;
     __shared__ unsigned long long s_c[2];
@@ -411,6 +417,7 @@ __global__ void k_commit_redo(DevStatus* st) {
 constexpr int kGatherPerSm = 3;
 template <class IO>
 __global__ void __launch_bounds__(kThreads) k_gather(const __grid_constant__ Args a) {
+    pdl_enter();
     constexpr int W = IO::W;
     __shared__ unsigned long long s_c[2];
     const uint64_t nvec = a.count / W;
@@ -466,6 +473,7 @@ __host__ __device__ inline int rs_chunk_cap(int n_ranks) { return n_ranks <= 4 ?
 
 template <int DT, class IO, bool SPEC, bool TO_REPLICAS>
 __global__ void __launch_bounds__(kThreads, 3) k_rs(const __grid_constant__ Args a) {
+    pdl_enter();
     constexpr int W = IO::W;
     __shared__ Pro pro;
     __shared__ unsigned long long s_c[2];
@@ -546,6 +554,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_rs(const __grid_constant__ Args
 // order, then commit / skip (SPEC) or decide clip and scalars (two-pass).
 template <bool SPEC>
 __global__ void __launch_bounds__(kThreads) k_finalize3(const __grid_constant__ Args a) {
+    pdl_enter();
     double q;
     int f;
     gather_partials(a.ws.bucket_norm, a.ws.bucket_flag, a.bucket_index, q, f);

@@ -282,6 +282,7 @@ __device__ __forceinline__ void quantize_blocks_u(const unsigned short* src, uin
 // and {scale, lo} pairs (qdst[0]).
 template <int DT, int BITS>
 __global__ void __launch_bounds__(kThreads) k_quantize(const __grid_constant__ Args a) {
+    pdl_enter();
     const int lane = threadIdx.x & 31;
     const uint64_t nb = (a.count + kQBlock - 1) / kQBlock;
     const unsigned short* src = static_cast<const unsigned short*>(a.grads[0]) + a.base;
@@ -305,6 +306,7 @@ __global__ void __launch_bounds__(kThreads) k_quantize(const __grid_constant__ A
 // and 6 % at N = 2, and fewer per SM slower still.
 template <int DT>
 __global__ void __launch_bounds__(kThreads, 6) k_gather_q8(const __grid_constant__ Args a) {
+    pdl_enter();
     __shared__ unsigned long long s_c[2];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint64_t nb = (a.count + kQBlock - 1) / kQBlock;
@@ -348,6 +350,7 @@ __global__ void __launch_bounds__(kThreads, 6) k_gather_q8(const __grid_constant
 // codes (grads[0]) + scales (qsrc[0]) -> 16-bit buffer (params[0]), count elements.
 template <int DT, int BITS>
 __global__ void __launch_bounds__(kThreads) k_dequantize(const __grid_constant__ Args a) {
+    pdl_enter();
     const uint64_t nv8 = (a.count + 7) / 8;
     for (uint64_t t = thread_id(); t < nv8; t += grid_threads()) {
         const uint64_t e0 = t * 8;
@@ -435,6 +438,7 @@ __device__ __forceinline__ void reduce_group_q(const Args& a, uint64_t j, const 
 // int8) than the balance gains.
 template <int DT, class IO, int BITS, bool SPEC>
 __global__ void __launch_bounds__(kThreads, BITS == 4 ? 4 : 3) k_rs_q(const __grid_constant__ Args a) {
+    pdl_enter();
     constexpr int W = IO::W;
     __shared__ Pro pro;
     prologue_reduce(a, pro, SPEC);
