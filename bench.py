@@ -894,9 +894,11 @@ def run_other(args, ws, rank, local):
                 else:
                     ms, bps, st = bench_dense(w, stage, args.steps, args.warmup, torch, S, Z, flush_l2=flush,
                                               sets_max=1)
-                lines.append(_line(w.name, psi / (ms * 1e-3), ms, args.steps, args.warmup, bps, "bf16",
-                                   {"psi": psi, "n_ranks": n, "stage": stage,
-                                    "l2": "256 MiB written between timed calls" if flush else "inputs larger than L2"}))
+                extra = {"psi": psi, "n_ranks": n, "stage": stage,
+                         "l2": "256 MiB written between timed calls" if flush else "inputs larger than L2"}
+                if stage == 3:
+                    extra.update(bench_stage3.parts)
+                lines.append(_line(w.name, psi / (ms * 1e-3), ms, args.steps, args.warmup, bps, "bf16", extra))
                 print(json.dumps(lines[-1]), flush=True)
         return 0
     for ln in lines:
