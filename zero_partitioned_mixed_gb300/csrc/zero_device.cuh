@@ -555,16 +555,17 @@ cudaError_t run(KernelT kernel, const Args& a, uint64_t nvec, cudaStream_t s, in
 }
 
 // Launch a chunked kernel: the persistent grid, but no more CTAs than chunks.
-template <int UMAX = kChunkU, typename KernelT>
+template <int UMAX = kChunkU, uint64_t TARGET = kMinChunks, typename KernelT>
 cudaError_t run_chunked(KernelT kernel, const Args& a, uint64_t nvec, cudaStream_t s, int* grid_out,
                         int per_sm = 0) {
-    return run(kernel, a, chunk_total<UMAX>(nvec) * kThreads, s, grid_out, per_sm);
+    return run(kernel, a, chunk_total<UMAX, TARGET>(nvec) * kThreads, s, grid_out, per_sm);
 }
-// The same with the chunk cap chosen at run time (the kernel computes the
-// same cap from its arguments).
+// The same with the chunk cap and target chosen at run time (the kernel
+// computes the same pair from its arguments).
 template <typename KernelT>
-cudaError_t run_chunked_u(KernelT kernel, const Args& a, uint64_t nvec, int umax, cudaStream_t s, int* grid_out) {
-    return run(kernel, a, chunk_total(nvec, umax) * kThreads, s, grid_out);
+cudaError_t run_chunked_u(KernelT kernel, const Args& a, uint64_t nvec, int umax, uint64_t target,
+                          cudaStream_t s, int* grid_out) {
+    return run(kernel, a, chunk_total(nvec, umax, target) * kThreads, s, grid_out);
 }
 
 }  // namespace

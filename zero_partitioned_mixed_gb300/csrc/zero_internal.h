@@ -24,37 +24,42 @@ constexpr int kGroup = 32;
 constexpr uint64_t kDirectChunks = 4096;   // up to this many chunks, no group stage
 constexpr int kCtrSlots = 64;       // launches of one handle that may be in flight at once
 
-// Vectors per thread in a chunk: kChunkU for large launches, fewer (down to
-// 1) for small ones, so that a launch has about kMinChunks chunks or more --
-// enough for every CTA of the persistent grid.  A function of the launch's
-// size only, so the chunk partials stay deterministic.
-// UMAX is the kernel's own cap (the stage 1/2 step measured best at 16, the
-// gather at kChunkU, the reduce-scatter at 16 for N <= 4 and kChunkU above);
-// a larger cap only lowers the count.
-constexpr uint64_t kMinChunks = 2048;
-__host__ __device__ inline int chunk_u(uint64_t nvec, int umax) {
-    const uint64_t u = nvec / (static_cast<uint64_t>(kThreads) * kMinChunks);
+// Vectors per thread in a chunk: UMAX for large launches, fewer (down to 1)
+// for smaller ones, so that a launch has about TARGET chunks or more --
+// enough for every CTA of the persistent grid and a short tail.  A function
+// of the launch's size only, so the chunk partials stay deterministic.
+// UMAX is the kernel's own cap and TARGET the chunk count it aims at (a
+// launch gets about TARGET chunks or more, unless UMAX caps U first).
+// Measured per kernel: the stage 1/2 step does best with UMAX 16 and TARGET
+// 16384 (long chunks for large launches, many for mid-sized ones), the
+// two-pass kernels with TARGET 16384, the reduce-scatter into replicas with
+// 8192, the gather and the reduce-scatter into the shard with the default.
+// Any (UMAX, TARGET) keeps the partials deterministic.
+constexpr uint64_t kMinChunks = 2048;        // the default TARGET
+constexpr uint64_t kMaxChunkTarget = 16384;  // the largest TARGET of a kernel that writes chunk partials
+__host__ __device__ inline int chunk_u(uint64_t nvec, int umax, uint64_t target = kMinChunks) {
+    const uint64_t u = nvec / (static_cast<uint64_t>(kThreads) * target);
     return u >= static_cast<uint64_t>(umax) ? umax : (u < 1 ? 1 : static_cast<int>(u));
 }
-__host__ __device__ inline uint64_t chunk_len(uint64_t nvec, int umax) {
-    return static_cast<uint64_t>(chunk_u(nvec, umax)) * kThreads;
+__host__ __device__ inline uint64_t chunk_len(uint64_t nvec, int umax, uint64_t target = kMinChunks) {
+    return static_cast<uint64_t>(chunk_u(nvec, umax, target)) * kThreads;
 }
-__host__ __device__ inline uint64_t chunk_total(uint64_t nvec, int umax) {
-    const uint64_t len = chunk_len(nvec, umax);
+__host__ __device__ inline uint64_t chunk_total(uint64_t nvec, int umax, uint64_t target = kMinChunks) {
+    const uint64_t len = chunk_len(nvec, umax, target);
     return (nvec + len - 1) / len;
 }
-template <int UMAX = kChunkU>
-__host__ __device__ inline int chunk_u(uint64_t nvec) { return chunk_u(nvec, UMAX); }
-template <int UMAX = kChunkU>
-__host__ __device__ inline uint64_t chunk_len(uint64_t nvec) { return chunk_len(nvec, UMAX); }
-template <int UMAX = kChunkU>
-__host__ __device__ inline uint64_t chunk_total(uint64_t nvec) { return chunk_total(nvec, UMAX); }
+template <int UMAX = kChunkU, uint64_t TARGET = kMinChunks>
+__host__ __device__ inline int chunk_u(uint64_t nvec) { return chunk_u(nvec, UMAX, TARGET); }
+template <int UMAX = kChunkU, uint64_t TARGET = kMinChunks>
+__host__ __device__ inline uint64_t chunk_len(uint64_t nvec) { return chunk_len(nvec, UMAX, TARGET); }
+template <int UMAX = kChunkU, uint64_t TARGET = kMinChunks>
+__host__ __device__ inline uint64_t chunk_total(uint64_t nvec) { return chunk_total(nvec, UMAX, TARGET); }
 
 // Chunks and groups of any launch over at most `elems` elements (worst case:
-// 1-wide vectors; below kChunkU vectors per thread a launch has fewer than
-// 2 * kMinChunks chunks).
+// 1-wide vectors at kChunkU vectors per thread; below that a launch has at
+// most 2 * TARGET chunks).
 inline uint64_t max_chunks(uint64_t elems) {
-    const uint64_t a = elems / kChunkVec + 1, b = 2 * kMinChunks + 1;
+    const uint64_t a = elems / kChunkVec + 1, b = 2 * kMaxChunkTarget + 1;
     return a > b ? a : b;
 }
 inline uint64_t max_groups(uint64_t elems) { return max_chunks(elems) / kGroup + 1; }

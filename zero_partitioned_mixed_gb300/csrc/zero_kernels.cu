@@ -35,6 +35,18 @@ namespace {
 // barriers for its long iterations (ψ = 2^29, N = 2: 2.67 against 2.77 ms
 // at 4; the flat 1.5e9 step: 12.45 against 12.54 ms).
 constexpr int kStepChunkU = 16;
+// Chunk targets (chunks a launch aims at before the cap): a mid-sized launch
+// is cut finer so that its last chunks end together.  GPT-2 small (1.2e8
+// parameters, N = 8): the one-pass step 1.048 ms at 16384 against 1.087 ms
+// at 2048, the two-pass step 1.203 against 1.213 ms; ZeRO-2 buckets of 5e7
+// reduced into the replicas 13.07 ms at 8192 against 13.21 ms at 2048.  The
+// flat 1.5e9 step is capped first and does not change.
+constexpr uint64_t kStepChunks = 16384;
+constexpr uint64_t kTwoPassChunks = 16384;
+constexpr uint64_t kRsReplicaChunks = 8192;
+static_assert(kStepChunks <= kMaxChunkTarget && kTwoPassChunks <= kMaxChunkTarget &&
+                  kRsReplicaChunks <= kMaxChunkTarget,
+              "the workspace holds the partials of at most 2 * kMaxChunkTarget chunks");
 // Stages 1/2, one pass: reduce-scatter + unscale + flag + norm partial +
 // AdamW from the live slot into the shadow slot + cast + all-gather.  The
 // last block commits the shadow slot, or records the overflow (the
@@ -50,8 +62,9 @@ __global__ void __launch_bounds__(kThreads, 3) k_step_spec(const __grid_constant
     const uint64_t src = static_cast<uint64_t>(pro.live) * a.slot_stride;
     const uint64_t dst = static_cast<uint64_t>(pro.live ^ 1) * a.slot_stride;
     const uint64_t nvec = a.count / W;
-    const uint64_t clen = chunk_len<kStepChunkU>(nvec), nchunks = chunk_total<kStepChunkU>(nvec);
-    const int U = chunk_u<kStepChunkU>(nvec);
+    const uint64_t clen = chunk_len<kStepChunkU, kStepChunks>(nvec);
+    const uint64_t nchunks = chunk_total<kStepChunkU, kStepChunks>(nvec);
+    const int U = chunk_u<kStepChunkU, kStepChunks>(nvec);
     ChunkCtr* ctr = a.ws.ctrs + a.ctr_slot;
     int bad = 0;
     // Overflow is the existence of one non-finite averaged gradient, and an
@@ -137,8 +150,9 @@ __global__ void __launch_bounds__(kThreads) k_reduce(const __grid_constant__ Arg
     __shared__ double s_wp[2][kThreads / 32];
     prologue_reduce(a, pro, false);
     const uint64_t nvec = a.count / W;
-    const uint64_t clen = chunk_len(nvec), nchunks = chunk_total(nvec);
-    const int U = chunk_u(nvec);
+    const uint64_t clen = chunk_len<kChunkU, kTwoPassChunks>(nvec);
+    const uint64_t nchunks = chunk_total<kChunkU, kTwoPassChunks>(nvec);
+    const int U = chunk_u<kChunkU, kTwoPassChunks>(nvec);
     ChunkCtr* ctr = a.ws.ctrs + a.ctr_slot;
     int bad = 0;
     Chunks ch(ctr, s_c, nchunks);
@@ -194,8 +208,9 @@ __global__ void __launch_bounds__(kThreads) k_apply(const __grid_constant__ Args
     if (pro.overflow) return;   // every CTA: the counter stays untouched
     const uint64_t off = static_cast<uint64_t>(pro.live) * a.slot_stride;
     const uint64_t nvec = a.count / W;
-    const uint64_t clen = chunk_len(nvec), nchunks = chunk_total(nvec);
-    const int U = chunk_u(nvec);
+    const uint64_t clen = chunk_len<kChunkU, kTwoPassChunks>(nvec);
+    const uint64_t nchunks = chunk_total<kChunkU, kTwoPassChunks>(nvec);
+    const int U = chunk_u<kChunkU, kTwoPassChunks>(nvec);
     ChunkCtr* ctr = a.ws.ctrs + a.ctr_slot;
     Chunks ch(ctr, s_c, nchunks);
     for (;;) {
@@ -483,8 +498,9 @@ __global__ void __launch_bounds__(kThreads, 3) k_rs(const __grid_constant__ Args
     const uint64_t dst = static_cast<uint64_t>(pro.live ^ 1) * a.slot_stride;
     const uint64_t nvec = a.count / W;
     const int umax = rs_chunk_cap(a.n_ranks);
-    const uint64_t clen = chunk_len(nvec, umax), nchunks = chunk_total(nvec, umax);
-    const int U = chunk_u(nvec, umax);
+    const uint64_t target = TO_REPLICAS ? kRsReplicaChunks : kMinChunks;
+    const uint64_t clen = chunk_len(nvec, umax, target), nchunks = chunk_total(nvec, umax, target);
+    const int U = chunk_u(nvec, umax, target);
     ChunkCtr* ctr = a.ws.ctrs + a.ctr_slot;
     int bad = 0;
     Chunks ch(ctr, s_c, nchunks);
@@ -589,20 +605,21 @@ template <int DT, class IO>
 cudaError_t launch_dw(Kind kind, const Args& a, cudaStream_t s, int* grid_out) {
     const uint64_t nvec = a.count / IO::W;
     switch (kind) {
-        case Kind::kStepSpec: return run_chunked<kStepChunkU>(k_step_spec<DT, IO>, a, nvec, s, grid_out);
-        case Kind::kReduceWs: return run_chunked(k_reduce<DT, IO, true>, a, nvec, s, grid_out);
-        case Kind::kReduceNoWs: return run_chunked(k_reduce<DT, IO, false>, a, nvec, s, grid_out);
-        case Kind::kApplyWs: return run_chunked(k_apply<DT, IO, true, false>, a, nvec, s, grid_out);
-        case Kind::kApplyReread: return run_chunked(k_apply<DT, IO, false, false>, a, nvec, s, grid_out);
-        case Kind::kApplyWsShard: return run_chunked(k_apply<DT, IO, true, true>, a, nvec, s, grid_out);
+        case Kind::kStepSpec: return run_chunked<kStepChunkU, kStepChunks>(k_step_spec<DT, IO>, a, nvec, s, grid_out);
+        case Kind::kReduceWs: return run_chunked<kChunkU, kTwoPassChunks>(k_reduce<DT, IO, true>, a, nvec, s, grid_out);
+        case Kind::kReduceNoWs: return run_chunked<kChunkU, kTwoPassChunks>(k_reduce<DT, IO, false>, a, nvec, s, grid_out);
+        case Kind::kApplyWs: return run_chunked<kChunkU, kTwoPassChunks>(k_apply<DT, IO, true, false>, a, nvec, s, grid_out);
+        case Kind::kApplyReread: return run_chunked<kChunkU, kTwoPassChunks>(k_apply<DT, IO, false, false>, a, nvec, s, grid_out);
+        case Kind::kApplyWsShard: return run_chunked<kChunkU, kTwoPassChunks>(k_apply<DT, IO, true, true>, a, nvec, s, grid_out);
         case Kind::kApplyStage0: return run_chunked(k_apply_stage0<DT, IO>, a, nvec, s, grid_out);
         case Kind::kRollbackReplicas: return run_chunked(k_rollback<DT, IO, false>, a, nvec, s, grid_out);
         case Kind::kRollbackShard: return run_chunked(k_rollback<DT, IO, true>, a, nvec, s, grid_out);
         case Kind::kFixupReplicas: return run_chunked(k_fixup<DT, IO>, a, nvec, s, grid_out);
         case Kind::kGather: return run_chunked(k_gather<IO>, a, nvec, s, grid_out, IO::W == 8 ? kGatherPerSm : 0);
-        case Kind::kRsSpec: return run_chunked_u(k_rs<DT, IO, true, false>, a, nvec, rs_chunk_cap(a.n_ranks), s, grid_out);
-        case Kind::kRsSpecReplicas: return run_chunked_u(k_rs<DT, IO, true, true>, a, nvec, rs_chunk_cap(a.n_ranks), s, grid_out);
-        case Kind::kRsWs: return run_chunked_u(k_rs<DT, IO, false, false>, a, nvec, rs_chunk_cap(a.n_ranks), s, grid_out);
+        case Kind::kRsSpec: return run_chunked_u(k_rs<DT, IO, true, false>, a, nvec, rs_chunk_cap(a.n_ranks), kMinChunks, s, grid_out);
+        case Kind::kRsSpecReplicas: return run_chunked_u(k_rs<DT, IO, true, true>, a, nvec, rs_chunk_cap(a.n_ranks), kRsReplicaChunks, s,
+                                                            grid_out);
+        case Kind::kRsWs: return run_chunked_u(k_rs<DT, IO, false, false>, a, nvec, rs_chunk_cap(a.n_ranks), kMinChunks, s, grid_out);
     }
     return cudaErrorInvalidValue;
 }

@@ -238,11 +238,14 @@ __device__ __forceinline__ uint32_t load_code1(const void* codes, uint64_t e) {
 __device__ __forceinline__ uint64_t warp_id() { return (static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; }
 __device__ __forceinline__ uint64_t warp_count() { return (static_cast<uint64_t>(gridDim.x) * blockDim.x) >> 5; }
 
-// Warp-iterations per chunk for the block-quantizing kernels: 4 when a
-// launch has plenty of work, fewer for small ones (at least kMinChunks
-// chunks when possible).
+// Warp-iterations per chunk for the block-quantizing kernels: as few as
+// leave a launch about kQChunks chunks, at most 4.  The quantized gather
+// measured best with the finest chunks (no partials to commit): at
+// ψ = 2^29, N = 8, 2e8-element buckets, a step's gathers took 1.4 % less
+// than with 2048 chunks per launch.
+constexpr uint64_t kQChunks = 32768;
 __host__ __device__ inline int q_chunk_u(uint64_t iters) {
-    const uint64_t u = iters / kMinChunks;
+    const uint64_t u = iters / kQChunks;
     return u >= 4 ? 4 : (u < 1 ? 1 : static_cast<int>(u));
 }
 
