@@ -345,7 +345,7 @@ ZERO_API int zero_bytes_moved(zero_handle_t h, zero_bytes_t* out);
  * and calls no cudaMalloc, cudaFree or other allocating routine.
  *   Its scratch -- the status word, the norm partials, the chunk counters
  *   and the fp32 averaged gradient -- lives in one static device array of
- *   ZERO_NOALLOC_MAX_PSI_PAD floats plus 84,832 bytes (about 16.1 MiB),
+ *   ZERO_NOALLOC_MAX_PSI_PAD floats plus 324,960 bytes (about 16.3 MiB),
  *   which every GPU that loads the library holds until the
  *   process exits.  psi_pad above ZERO_NOALLOC_MAX_PSI_PAD is rejected
  *   with ZERO_EINVAL.
