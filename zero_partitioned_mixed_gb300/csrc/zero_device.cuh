@@ -348,8 +348,8 @@ __device__ __forceinline__ uint64_t thread_id() {
 // tail where only the slow ones stream (about 7 % of the step on a GB300).
 // Chunked kernels instead take chunk after chunk from their launch's counter;
 // thread 0 fetches the next index while the block works on the current one.
-// Thread t of whichever CTA takes chunk c handles the vectors
-// start(c) + u*kThreads + t, u < units(c) (ChunkGeo, zero_internal.h).
+// With U = chunk_u(nvec), thread t of whichever CTA takes chunk c handles the
+// vectors c*U*kThreads + u*kThreads + t, u < U.
 class Chunks {
   public:
     // A CTA's first chunk is its own index (the grid has no more CTAs than
@@ -390,8 +390,8 @@ class Chunks {
 };
 
 // vector u of this thread in chunk c (chunks of `len` = U * kThreads vectors)
-__device__ __forceinline__ uint64_t chunk_vec(const ChunkGeo& g, uint64_t c, int u) {
-    return g.start(c) + static_cast<uint64_t>(u) * kThreads + threadIdx.x;
+__device__ __forceinline__ uint64_t chunk_vec(uint64_t c, uint64_t len, int u) {
+    return c * len + static_cast<uint64_t>(u) * kThreads + threadIdx.x;
 }
 
 __device__ __forceinline__ uint64_t group_count(uint64_t nchunks) { return (nchunks + kGroup - 1) / kGroup; }
@@ -558,14 +558,14 @@ cudaError_t run(KernelT kernel, const Args& a, uint64_t nvec, cudaStream_t s, in
 template <int UMAX = kChunkU, uint64_t TARGET = kMinChunks, typename KernelT>
 cudaError_t run_chunked(KernelT kernel, const Args& a, uint64_t nvec, cudaStream_t s, int* grid_out,
                         int per_sm = 0) {
-    return run(kernel, a, ChunkGeo(nvec, UMAX, TARGET).nchunks * kThreads, s, grid_out, per_sm);
+    return run(kernel, a, chunk_total<UMAX, TARGET>(nvec) * kThreads, s, grid_out, per_sm);
 }
 // The same with the chunk cap and target chosen at run time (the kernel
 // computes the same pair from its arguments).
 template <typename KernelT>
 cudaError_t run_chunked_u(KernelT kernel, const Args& a, uint64_t nvec, int umax, uint64_t target,
                           cudaStream_t s, int* grid_out) {
-    return run(kernel, a, ChunkGeo(nvec, umax, target).nchunks * kThreads, s, grid_out);
+    return run(kernel, a, chunk_total(nvec, umax, target) * kThreads, s, grid_out);
 }
 
 }  // namespace

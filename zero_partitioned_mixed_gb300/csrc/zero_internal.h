@@ -41,41 +41,26 @@ __host__ __device__ inline int chunk_u(uint64_t nvec, int umax, uint64_t target 
     const uint64_t u = nvec / (static_cast<uint64_t>(kThreads) * target);
     return u >= static_cast<uint64_t>(umax) ? umax : (u < 1 ? 1 : static_cast<int>(u));
 }
-
-// A launch's chunks.  The bulk of the vectors goes in chunks of U vectors
-// per thread (U from chunk_u), the last kTailChunks * kThreads vectors or
-// so in chunks of one vector per thread: CTAs that run out of work then
-// wait at most one short chunk for the rest, while the bulk keeps the low
-// bookkeeping cost of long chunks.  Chunk c covers the vectors from
-// start(c) on, units(c) per thread; start() rises with c.  A function of
-// the launch's size alone, so the chunk partials stay deterministic.
-constexpr uint64_t kTailChunks = 2048;
-struct ChunkGeo {
-    uint64_t nvec;     // vectors in the launch
-    uint64_t nbig;     // chunks of ubig units
-    uint64_t bulk;     // vectors they cover
-    uint64_t nchunks;  // all chunks
-    int ubig;
-    __host__ __device__ ChunkGeo(uint64_t n, int umax, uint64_t target) : nvec(n) {
-        ubig = chunk_u(n, umax, target);
-        const uint64_t big = static_cast<uint64_t>(ubig) * kThreads;
-        const uint64_t tail = kTailChunks * kThreads;
-        nbig = (ubig > 1 && n > tail) ? (n - tail) / big : 0;
-        bulk = nbig * big;
-        nchunks = nbig + (n - bulk + kThreads - 1) / kThreads;
-    }
-    __host__ __device__ uint64_t start(uint64_t c) const {
-        return c < nbig ? c * static_cast<uint64_t>(ubig) * kThreads : bulk + (c - nbig) * kThreads;
-    }
-    __host__ __device__ int units(uint64_t c) const { return c < nbig ? ubig : 1; }
-};
+__host__ __device__ inline uint64_t chunk_len(uint64_t nvec, int umax, uint64_t target = kMinChunks) {
+    return static_cast<uint64_t>(chunk_u(nvec, umax, target)) * kThreads;
+}
+__host__ __device__ inline uint64_t chunk_total(uint64_t nvec, int umax, uint64_t target = kMinChunks) {
+    const uint64_t len = chunk_len(nvec, umax, target);
+    return (nvec + len - 1) / len;
+}
+template <int UMAX = kChunkU, uint64_t TARGET = kMinChunks>
+__host__ __device__ inline int chunk_u(uint64_t nvec) { return chunk_u(nvec, UMAX, TARGET); }
+template <int UMAX = kChunkU, uint64_t TARGET = kMinChunks>
+__host__ __device__ inline uint64_t chunk_len(uint64_t nvec) { return chunk_len(nvec, UMAX, TARGET); }
+template <int UMAX = kChunkU, uint64_t TARGET = kMinChunks>
+__host__ __device__ inline uint64_t chunk_total(uint64_t nvec) { return chunk_total(nvec, UMAX, TARGET); }
 
 // Chunks and groups of any launch over at most `elems` elements (worst case:
 // 1-wide vectors at kChunkU vectors per thread; below that a launch has at
-// most 2 * TARGET chunks), plus the tail's one-unit chunks.
+// most 2 * TARGET chunks).
 inline uint64_t max_chunks(uint64_t elems) {
     const uint64_t a = elems / kChunkVec + 1, b = 2 * kMaxChunkTarget + 1;
-    return (a > b ? a : b) + kTailChunks + 64;
+    return a > b ? a : b;
 }
 inline uint64_t max_groups(uint64_t elems) { return max_chunks(elems) / kGroup + 1; }
 

@@ -62,8 +62,9 @@ __global__ void __launch_bounds__(kThreads, 3) k_step_spec(const __grid_constant
     const uint64_t src = static_cast<uint64_t>(pro.live) * a.slot_stride;
     const uint64_t dst = static_cast<uint64_t>(pro.live ^ 1) * a.slot_stride;
     const uint64_t nvec = a.count / W;
-    const ChunkGeo geo(nvec, kStepChunkU, kStepChunks);
-    const uint64_t nchunks = geo.nchunks;
+    const uint64_t clen = chunk_len<kStepChunkU, kStepChunks>(nvec);
+    const uint64_t nchunks = chunk_total<kStepChunkU, kStepChunks>(nvec);
+    const int U = chunk_u<kStepChunkU, kStepChunks>(nvec);
     ChunkCtr* ctr = a.ws.ctrs + a.ctr_slot;
     int bad = 0;
     // Overflow is the existence of one non-finite averaged gradient, and an
@@ -81,8 +82,8 @@ __global__ void __launch_bounds__(kThreads, 3) k_step_spec(const __grid_constant
         ch.prefetch();
         reach = c + 1;
         double cacc = 0.0;
-        for (int u = 0, U = geo.units(c); u < U; ++u) {
-            const uint64_t vi = chunk_vec(geo, c, u);
+        for (int u = 0; u < U; ++u) {
+            const uint64_t vi = chunk_vec(c, clen, u);
             if (vi >= nvec) break;
             const uint32_t seen_next = *stop;
             const uint64_t gi = vi * W;
@@ -119,7 +120,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_step_spec(const __grid_constant
     }
     // a CTA works on its chunks in increasing order: every vector written
     // lies below the largest reach, which bounds an overflow rollback
-    if (threadIdx.x == 0) atomicMax(reinterpret_cast<unsigned long long*>(&a.ws.status->hwm1), geo.start(reach) + 1ull);
+    if (threadIdx.x == 0) atomicMax(reinterpret_cast<unsigned long long*>(&a.ws.status->hwm1), reach * clen + 1ull);
     const int flag = __syncthreads_or(bad);
     if (publish(a, 0.0, flag, a.ws.partials, a.ws.flags)) {
         double q;
@@ -149,8 +150,9 @@ __global__ void __launch_bounds__(kThreads) k_reduce(const __grid_constant__ Arg
     __shared__ double s_wp[2][kThreads / 32];
     prologue_reduce(a, pro, false);
     const uint64_t nvec = a.count / W;
-    const ChunkGeo geo(nvec, kChunkU, kTwoPassChunks);
-    const uint64_t nchunks = geo.nchunks;
+    const uint64_t clen = chunk_len<kChunkU, kTwoPassChunks>(nvec);
+    const uint64_t nchunks = chunk_total<kChunkU, kTwoPassChunks>(nvec);
+    const int U = chunk_u<kChunkU, kTwoPassChunks>(nvec);
     ChunkCtr* ctr = a.ws.ctrs + a.ctr_slot;
     int bad = 0;
     Chunks ch(ctr, s_c, nchunks);
@@ -159,8 +161,8 @@ __global__ void __launch_bounds__(kThreads) k_reduce(const __grid_constant__ Arg
         if (c >= nchunks) break;
         ch.prefetch();
         double cacc = 0.0;
-        for (int u = 0, U = geo.units(c); u < U; ++u) {
-            const uint64_t vi = chunk_vec(geo, c, u);
+        for (int u = 0; u < U; ++u) {
+            const uint64_t vi = chunk_vec(c, clen, u);
             if (vi >= nvec) break;
             const uint64_t gi = vi * W;
             float g[W];
@@ -206,16 +208,17 @@ __global__ void __launch_bounds__(kThreads) k_apply(const __grid_constant__ Args
     if (pro.overflow) return;   // every CTA: the counter stays untouched
     const uint64_t off = static_cast<uint64_t>(pro.live) * a.slot_stride;
     const uint64_t nvec = a.count / W;
-    const ChunkGeo geo(nvec, kChunkU, kTwoPassChunks);
-    const uint64_t nchunks = geo.nchunks;
+    const uint64_t clen = chunk_len<kChunkU, kTwoPassChunks>(nvec);
+    const uint64_t nchunks = chunk_total<kChunkU, kTwoPassChunks>(nvec);
+    const int U = chunk_u<kChunkU, kTwoPassChunks>(nvec);
     ChunkCtr* ctr = a.ws.ctrs + a.ctr_slot;
     Chunks ch(ctr, s_c, nchunks);
     for (;;) {
       const uint64_t c = ch.current();
       if (c >= nchunks) break;
       ch.prefetch();
-      for (int u = 0, U = geo.units(c); u < U; ++u) {
-        const uint64_t vi = chunk_vec(geo, c, u);
+      for (int u = 0; u < U; ++u) {
+        const uint64_t vi = chunk_vec(c, clen, u);
         if (vi >= nvec) break;
         const uint64_t gi = vi * W;
         float g[W], p[W], m[W], v[W];
@@ -261,16 +264,16 @@ __global__ void __launch_bounds__(kThreads, 3) k_apply_stage0(const __grid_const
     prologue_reduce(a, pro, false);
     if (pro.overflow) return;   // every CTA: the counter stays untouched
     const uint64_t nvec = a.count / W;
-    const ChunkGeo geo(nvec, kChunkU, kMinChunks);
-    const uint64_t nchunks = geo.nchunks;
+    const uint64_t clen = chunk_len(nvec), nchunks = chunk_total(nvec);
+    const int U = chunk_u(nvec);
     ChunkCtr* ctr = a.ws.ctrs + a.ctr_slot;
     Chunks ch(ctr, s_c, nchunks);
     for (;;) {
       const uint64_t c = ch.current();
       if (c >= nchunks) break;
       ch.prefetch();
-      for (int u = 0, U = geo.units(c); u < U; ++u) {
-        const uint64_t vi = chunk_vec(geo, c, u);
+      for (int u = 0; u < U; ++u) {
+        const uint64_t vi = chunk_vec(c, clen, u);
         if (vi >= nvec) break;
         const uint64_t gi = vi * W;
         float g[W];
@@ -317,16 +320,16 @@ __global__ void __launch_bounds__(kThreads) k_rollback(const __grid_constant__ A
     if (!st->overflow) return;   // every CTA: the counter stays untouched
     const uint64_t off = static_cast<uint64_t>(st->live_slot) * a.slot_stride;
     const uint64_t nvec = a.count / W;
-    const ChunkGeo geo(nvec, kChunkU, kMinChunks);
-    const uint64_t nchunks = geo.nchunks;
+    const uint64_t clen = chunk_len(nvec), nchunks = chunk_total(nvec);
+    const int U = chunk_u(nvec);
     ChunkCtr* ctr = a.ws.ctrs + a.ctr_slot;
     Chunks ch(ctr, s_c, nchunks);
     for (;;) {
         const uint64_t c = ch.current();
         if (c >= nchunks) break;
         ch.prefetch();
-        for (int u = 0, U = geo.units(c); u < U; ++u) {
-            const uint64_t vi = chunk_vec(geo, c, u);
+        for (int u = 0; u < U; ++u) {
+            const uint64_t vi = chunk_vec(c, clen, u);
             if (vi >= nvec) break;
             const uint64_t gi = a.base + vi * W;
             float p[W];
@@ -366,16 +369,16 @@ __global__ void __launch_bounds__(kThreads) k_fixup(const __grid_constant__ Args
     // a rollback restores only what the stopped pass may have written
     const uint64_t hw = st->hwm1;
     const uint64_t lim = (overflow && hw != 0 && hw - 1 < nvec) ? hw - 1 : nvec;
-    const ChunkGeo geo(lim, kChunkU, kMinChunks);
-    const uint64_t nchunks = geo.nchunks;
+    const uint64_t clen = chunk_len(lim), nchunks = chunk_total(lim);
+    const int U = chunk_u(lim);
     ChunkCtr* ctr = a.ws.ctrs + a.ctr_slot;
     Chunks ch(ctr, s_c, nchunks);
     for (;;) {
       const uint64_t c = ch.current();
       if (c >= nchunks) break;
       ch.prefetch();
-      for (int u = 0, U = geo.units(c); u < U; ++u) {
-        const uint64_t vi = chunk_vec(geo, c, u);
+      for (int u = 0; u < U; ++u) {
+        const uint64_t vi = chunk_vec(c, clen, u);
         if (vi >= lim) break;
         const uint64_t gi = vi * W;
         float p[W];
@@ -433,8 +436,8 @@ __global__ void __launch_bounds__(kThreads) k_gather(const __grid_constant__ Arg
     constexpr int W = IO::W;
     __shared__ unsigned long long s_c[2];
     const uint64_t nvec = a.count / W;
-    const ChunkGeo geo(nvec, kChunkU, kMinChunks);
-    const uint64_t nchunks = geo.nchunks;
+    const uint64_t clen = chunk_len(nvec), nchunks = chunk_total(nvec);
+    const int U = chunk_u(nvec);
     ChunkCtr* ctr = a.ws.ctrs + a.ctr_slot;
     Chunks ch(ctr, s_c, nchunks);
     for (;;) {
@@ -445,10 +448,9 @@ __global__ void __launch_bounds__(kThreads) k_gather(const __grid_constant__ Arg
             static_assert(kChunkU == 4, "one batch of loads covers a chunk");
             uint4 x[kChunkU];
             uint64_t vi[kChunkU];
-            const int U = geo.units(c);
 #pragma unroll
             for (int u = 0; u < kChunkU; ++u) {
-                vi[u] = u < U ? chunk_vec(geo, c, u) : nvec;
+                vi[u] = u < U ? chunk_vec(c, clen, u) : nvec;
                 if (vi[u] < nvec) x[u] = __ldcs(reinterpret_cast<const uint4*>(a.grads[0]) + (a.base / 8 + vi[u]));
             }
             for (int r = 0; r < a.n_ranks; ++r) {
@@ -458,8 +460,8 @@ __global__ void __launch_bounds__(kThreads) k_gather(const __grid_constant__ Arg
                     if (vi[u] < nvec) __stcs(out + vi[u], x[u]);
             }
         } else {
-            for (int u = 0, U = geo.units(c); u < U; ++u) {
-                const uint64_t vi = chunk_vec(geo, c, u);
+            for (int u = 0; u < U; ++u) {
+                const uint64_t vi = chunk_vec(c, clen, u);
                 if (vi >= nvec) break;
                 const uint64_t j = vi * W;
                 uint32_t x[W];
@@ -497,8 +499,8 @@ __global__ void __launch_bounds__(kThreads, 3) k_rs(const __grid_constant__ Args
     const uint64_t nvec = a.count / W;
     const int umax = rs_chunk_cap(a.n_ranks);
     const uint64_t target = TO_REPLICAS ? kRsReplicaChunks : kMinChunks;
-    const ChunkGeo geo(nvec, umax, target);
-    const uint64_t nchunks = geo.nchunks;
+    const uint64_t clen = chunk_len(nvec, umax, target), nchunks = chunk_total(nvec, umax, target);
+    const int U = chunk_u(nvec, umax, target);
     ChunkCtr* ctr = a.ws.ctrs + a.ctr_slot;
     int bad = 0;
     Chunks ch(ctr, s_c, nchunks);
@@ -507,8 +509,8 @@ __global__ void __launch_bounds__(kThreads, 3) k_rs(const __grid_constant__ Args
       if (c >= nchunks) break;
       ch.prefetch();
       double acc = 0.0;
-      for (int u = 0, U = geo.units(c); u < U; ++u) {
-        const uint64_t vi = chunk_vec(geo, c, u);
+      for (int u = 0; u < U; ++u) {
+        const uint64_t vi = chunk_vec(c, clen, u);
         if (vi >= nvec) break;
         const uint64_t j = vi * W;
         const uint64_t gi = a.base + j;

@@ -36,10 +36,9 @@ constexpr size_t kGhatBytes = static_cast<size_t>(kNoAllocMaxPsiPad) * sizeof(fl
 constexpr size_t round32(size_t x) { return (x + 31) / 32 * 32; }
 // chunk scheduling: counters and group tickets (zeroed every call), chunk and group partials
 constexpr size_t kCtrBytes = round32(static_cast<size_t>(zg::kCtrSlots) * sizeof(zg::ChunkCtr));
-constexpr size_t kChunks = (kNoAllocMaxPsiPad / zg::kChunkVec + 1 > 2 * zg::kMaxChunkTarget + 1
-                                ? kNoAllocMaxPsiPad / zg::kChunkVec + 1
-                                : 2 * zg::kMaxChunkTarget + 1) +
-                           zg::kTailChunks + 64;
+constexpr size_t kChunks = kNoAllocMaxPsiPad / zg::kChunkVec + 1 > 2 * zg::kMaxChunkTarget + 1
+                               ? kNoAllocMaxPsiPad / zg::kChunkVec + 1
+                               : 2 * zg::kMaxChunkTarget + 1;
 constexpr size_t kGroups = kChunks / zg::kGroup + 1;
 constexpr size_t kTicketBytes = round32(kGroups * sizeof(uint32_t));
 constexpr size_t kChunkPartBytes = round32(kChunks * sizeof(double));
