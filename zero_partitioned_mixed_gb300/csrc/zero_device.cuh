@@ -160,8 +160,18 @@ __device__ __forceinline__ void prologue_reduce(const Args& a, Pro& pro, bool wi
         pro.clip_f = st->clip_f;
         pro.use_clip = st->use_clip;
         pro.overflow = st->overflow;
-        if (with_scalars) pro.sc = make_scalars(a.hyper, st->t + 1);
-        else pro.sc = st->sc;
+        if (with_scalars) {
+            const HyperDev& k = st->sc_key;
+            const HyperDev& h = a.hyper;
+            const bool hit = st->sc_t == st->t + 1 && __float_as_uint(k.lr) == __float_as_uint(h.lr) &&
+                             __float_as_uint(k.beta1) == __float_as_uint(h.beta1) &&
+                             __float_as_uint(k.beta2) == __float_as_uint(h.beta2) &&
+                             __float_as_uint(k.eps) == __float_as_uint(h.eps) &&
+                             __float_as_uint(k.weight_decay) == __float_as_uint(h.weight_decay);
+            pro.sc = hit ? st->sc_next : make_scalars(h, st->t + 1);
+        } else {
+            pro.sc = st->sc;
+        }
     }
     __syncthreads();
 }
@@ -266,6 +276,15 @@ __device__ void gather_partials(const double* slot_norm, const int32_t* slot_fla
     }
     q = block_sum(s);
     flag = __syncthreads_or(f);
+}
+
+// After a step is finalised: the next step's one-pass scalars, once, for
+// the kernels' prologues (same function and inputs as there, so the same
+// bits).
+__device__ void cache_next_scalars(DevStatus* st, const HyperDev& h) {
+    st->sc_next = make_scalars(h, st->t + 1);
+    st->sc_key = h;
+    st->sc_t = st->t + 1;
 }
 
 // Overflow: skip.  The scale halves (floor 1.0); t and the state stay.

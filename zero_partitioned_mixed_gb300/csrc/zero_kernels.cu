@@ -132,6 +132,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_step_spec(const __grid_constant
             ctr->next = 0ull;   // a pass cut short made fewer than nchunks grabs
             if (f) status_skip(st, q);
             else status_decide_spec(st, q, a.hyper);
+            cache_next_scalars(st, a.hyper);
             st->stop = 0u;
             st->ticket = 0u;
         }
@@ -189,6 +190,7 @@ __global__ void __launch_bounds__(kThreads) k_reduce(const __grid_constant__ Arg
             DevStatus* st = a.ws.status;
             if (f) status_skip(st, q);
             else status_decide_two_pass(st, q, a.hyper);
+            cache_next_scalars(st, a.hyper);
             st->ticket = 0u;
         }
     }
@@ -579,6 +581,7 @@ __global__ void __launch_bounds__(kThreads) k_finalize3(const __grid_constant__ 
         if (f) status_skip(st, q);
         else if (SPEC) status_commit_spec(st, q);
         else status_decide_two_pass(st, q, a.hyper);
+        cache_next_scalars(st, a.hyper);
     }
 }
 
@@ -598,6 +601,7 @@ __global__ void k_set_scaler(DevStatus* st, float loss_scale, int64_t t, int32_t
     st->ticket = 0u;
     st->stop = 0u;
     st->hwm1 = 0ull;
+    st->sc_t = -1;
 }
 
 // ------------------------------------------------------------------ launch
