@@ -89,10 +89,12 @@ def _draw(shape, sigma, seed, dtype=torch.float32, absolute=False):
 def run_case(psi: int, n: int, stage: int, dtype: str = "bf16", steps: int = 2, align: int = 8,
              mode: int = 0, double_buffer: bool = True, loss_scale: float = 1.0, hyper_kw=None,
              buckets: Optional[Sequence[Tuple[int, int]]] = None, inject=None, sigma: float = 1e-2,
-             seed: int = 0, warm: bool = True) -> Stats:
+             seed: int = 0, warm: bool = True, hyper_steps=None) -> Stats:
     """Run `steps` steps on the GPU and in the oracle; compare after each step.
 
     inject: list of (step, rank, index, value) written into the gradients.
+    hyper_steps: per step, hyper-parameter overrides on top of hyper_kw (a
+    schedule: learning rate, weight decay, ... changing between steps).
     """
     hyper_kw = dict(hyper_kw or {})
     hb, ho = hyper_pair(mode=mode, **hyper_kw)
@@ -125,6 +127,8 @@ def run_case(psi: int, n: int, stage: int, dtype: str = "bf16", steps: int = 2, 
     if stage == 3 and buckets is None:
         buckets = [(0, P)]
     for k in range(steps):
+        if hyper_steps is not None:
+            hb, ho = hyper_pair(mode=mode, **{**hyper_kw, **hyper_steps[k]})
         scale_now = ost.loss_scale
         # gradients for this step (already multiplied by the current scale)
         grads = torch.zeros((n, buf.stride), dtype=td, device="cuda")

@@ -492,6 +492,21 @@ def test_stage3_long_chunks_few_ranks(psi, n, buckets):
     assert st.mismatches == 0, st
 
 
+@pytest.mark.parametrize("stage,mode", [(1, 3), (2, 1), (3, 0), (1, 4)])
+def test_hyper_parameters_changing_between_steps(stage, mode):
+    # A learning-rate schedule, and a weight decay that changes once: the
+    # one-pass kernels read step scalars that the previous step's finaliser
+    # computed for the hyper-parameters it was given, and must compute their
+    # own whenever this step's differ.  Step 3 repeats step 2's values (the
+    # cached scalars are valid again).
+    sched = [dict(lr=1e-3), dict(lr=5e-4), dict(lr=5e-4), dict(lr=2.5e-4, weight_decay=0.05),
+             dict(lr=1e-4, weight_decay=0.05)]
+    st = run_case(250_003, 4, stage, "bf16", steps=len(sched), mode=mode, double_buffer=True,
+                  hyper_steps=sched)
+    st.check()
+    assert st.mismatches == 0, st
+
+
 @pytest.mark.parametrize("chunks", [456, 457, 915])
 @pytest.mark.parametrize("stage", [1, 3])
 def test_chunk_counts_around_the_grid(stage, chunks):
