@@ -98,9 +98,10 @@ struct DevStatus {
     uint64_t hwm1;      // one-pass step: 1 + a bound on the vectors it wrote (every write is
                         // below it); 0 = unknown (the whole range).  Reset after each step.
     // The scalars of step sc_t under the hyper-parameters sc_key, computed once
-    // by the thread that finalised the step before (sc_t = its t + 1).  A
-    // one-pass kernel whose t + 1 and hyper-parameters match reads them
-    // instead of computing them in every CTA.
+    // by the thread that finalised the bucketed step before (sc_t = its t + 1).
+    // A one-pass kernel whose t + 1 and hyper-parameters match reads them
+    // instead of computing them in every CTA; a step of one launch computes
+    // its own (the cost only moves between kernels there).
     StepScalars sc_next;
     HyperDev sc_key;
     int64_t sc_t;

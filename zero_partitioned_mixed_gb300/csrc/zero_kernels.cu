@@ -132,7 +132,6 @@ __global__ void __launch_bounds__(kThreads, 3) k_step_spec(const __grid_constant
             ctr->next = 0ull;   // a pass cut short made fewer than nchunks grabs
             if (f) status_skip(st, q);
             else status_decide_spec(st, q, a.hyper);
-            cache_next_scalars(st, a.hyper);
             st->stop = 0u;
             st->ticket = 0u;
         }
@@ -190,7 +189,6 @@ __global__ void __launch_bounds__(kThreads) k_reduce(const __grid_constant__ Arg
             DevStatus* st = a.ws.status;
             if (f) status_skip(st, q);
             else status_decide_two_pass(st, q, a.hyper);
-            cache_next_scalars(st, a.hyper);
             st->ticket = 0u;
         }
     }
@@ -581,6 +579,8 @@ __global__ void __launch_bounds__(kThreads) k_finalize3(const __grid_constant__ 
         if (f) status_skip(st, q);
         else if (SPEC) status_commit_spec(st, q);
         else status_decide_two_pass(st, q, a.hyper);
+        // the next step's reduce-scatters (one per bucket) read these
+        // instead of computing them in every CTA of every launch
         cache_next_scalars(st, a.hyper);
     }
 }

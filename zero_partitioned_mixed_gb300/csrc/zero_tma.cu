@@ -284,7 +284,6 @@ __global__ void __launch_bounds__(kTmaThreads, 2) k_step_tma(const __grid_consta
             if (f & 2) status_abort(st, qsum);
             else if (f) status_skip(st, qsum);
             else status_decide_spec(st, qsum, a.hyper);
-            cache_next_scalars(st, a.hyper);
             st->ticket = 0u;
         }
     }
