@@ -464,7 +464,7 @@ def _repeat_bitwise(stage, mode, psi, bucket, n):
 
 
 def test_overflow_stop_on_the_grouped_path():
-    # 140M elements over 2 ranks: 17.5M vectors, 17090 chunks of 4 x 256 --
+    # 140M elements over 2 ranks: 17.5M vectors, 4273 chunks of 16 x 256 --
     # above the 4096 chunks summed directly, so norm partials go through
     # group tickets.  An inf at 30 % stops the pass with groups left
     # incomplete; the finaliser must reset their tickets (the next steps'

@@ -47,6 +47,11 @@ constexpr uint64_t kRsReplicaChunks = 8192;
 static_assert(kStepChunks <= kMaxChunkTarget && kTwoPassChunks <= kMaxChunkTarget &&
                   kRsReplicaChunks <= kMaxChunkTarget,
               "the workspace holds the partials of at most 2 * kMaxChunkTarget chunks");
+// The step's target is kStepChunks from N = 8 up.  With N <= 4 an iteration
+// moves few bytes, the chunk bookkeeping weighs more, and the default target
+// measured better (the bandwidth sweep's stage-1 points at N = 2: 2^24
+// 0.119 against 0.129 ms, 2^27 0.696 against 0.716 ms).
+__host__ __device__ inline uint64_t step_chunk_target(int n_ranks) { return n_ranks <= 4 ? kMinChunks : kStepChunks; }
 // Stages 1/2, one pass: reduce-scatter + unscale + flag + norm partial +
 // AdamW from the live slot into the shadow slot + cast + all-gather.  The
 // last block commits the shadow slot, or records the overflow (the
@@ -62,9 +67,10 @@ __global__ void __launch_bounds__(kThreads, 3) k_step_spec(const __grid_constant
     const uint64_t src = static_cast<uint64_t>(pro.live) * a.slot_stride;
     const uint64_t dst = static_cast<uint64_t>(pro.live ^ 1) * a.slot_stride;
     const uint64_t nvec = a.count / W;
-    const uint64_t clen = chunk_len<kStepChunkU, kStepChunks>(nvec);
-    const uint64_t nchunks = chunk_total<kStepChunkU, kStepChunks>(nvec);
-    const int U = chunk_u<kStepChunkU, kStepChunks>(nvec);
+    const uint64_t target = step_chunk_target(a.n_ranks);
+    const uint64_t clen = chunk_len(nvec, kStepChunkU, target);
+    const uint64_t nchunks = chunk_total(nvec, kStepChunkU, target);
+    const int U = chunk_u(nvec, kStepChunkU, target);
     ChunkCtr* ctr = a.ws.ctrs + a.ctr_slot;
     int bad = 0;
     // Overflow is the existence of one non-finite averaged gradient, and an
@@ -609,7 +615,8 @@ template <int DT, class IO>
 cudaError_t launch_dw(Kind kind, const Args& a, cudaStream_t s, int* grid_out) {
     const uint64_t nvec = a.count / IO::W;
     switch (kind) {
-        case Kind::kStepSpec: return run_chunked<kStepChunkU, kStepChunks>(k_step_spec<DT, IO>, a, nvec, s, grid_out);
+        case Kind::kStepSpec:
+            return run_chunked_u(k_step_spec<DT, IO>, a, nvec, kStepChunkU, step_chunk_target(a.n_ranks), s, grid_out);
         case Kind::kReduceWs: return run_chunked<kChunkU, kTwoPassChunks>(k_reduce<DT, IO, true>, a, nvec, s, grid_out);
         case Kind::kReduceNoWs: return run_chunked<kChunkU, kTwoPassChunks>(k_reduce<DT, IO, false>, a, nvec, s, grid_out);
         case Kind::kApplyWs: return run_chunked<kChunkU, kTwoPassChunks>(k_apply<DT, IO, true, false>, a, nvec, s, grid_out);
