@@ -368,6 +368,14 @@ ZERO_API int zero_bytes_moved(zero_handle_t h, zero_bytes_t* out);
  */
 #define ZERO_NOALLOC_MAX_PSI_PAD (1ull << 22)
 
+/*
+ * zero_noalloc_scratch_bytes -- bytes of the static device array that
+ * zero_step_noalloc uses, per GPU that loads the library:
+ * 4 * ZERO_NOALLOC_MAX_PSI_PAD + 324,960.  A host query: no CUDA call, no
+ * GPU needed, no error.
+ */
+ZERO_API uint64_t zero_noalloc_scratch_bytes(void);
+
 ZERO_API int zero_step_noalloc(uint64_t psi, int n_ranks, int stage, int dtype, int align,
                       const void* const* grads, void* const* params,
                       float* master, float* m, float* v, const zero_hyper_t* hyper,

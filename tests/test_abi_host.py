@@ -94,3 +94,16 @@ def test_pointer_array_holds_the_rows_and_passes_through():
     assert [arr[i] for i in range(5)] == [t.data_ptr() for t in rows]
     assert B._ptr_array(arr) is arr
     assert B._ptr_array(None) is None
+
+
+def test_noalloc_scratch_size_matches_the_header():
+    # the header states the size of zero_step_noalloc's static array; the
+    # library reports the size it was built with (a host query, no GPU)
+    import re
+    import zero_partitioned_mixed_gb300 as Z
+    hdr = open(os.path.join(ROOT, "include", "zero_gb300.h")).read()
+    psi_pad = int(re.search(r"#define ZERO_NOALLOC_MAX_PSI_PAD \(1ull << (\d+)\)", hdr).group(1))
+    extra = [int(x.replace(",", "")) for x in re.findall(r"ZERO_NOALLOC_MAX_PSI_PAD floats plus ([\d,]+) bytes", hdr)]
+    extra += [int(x.replace(",", "")) for x in re.findall(r"4 \* ZERO_NOALLOC_MAX_PSI_PAD \+ ([\d,]+)\.", hdr)]
+    assert len(extra) == 2 and extra[0] == extra[1], extra
+    assert Z.zero_noalloc_scratch_bytes() == 4 * (1 << psi_pad) + extra[0]

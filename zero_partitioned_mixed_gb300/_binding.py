@@ -24,6 +24,7 @@ EXPORTS = (
     "zero_bytes_moved", "zero_last_error", "zero_destroy", "zero_step_noalloc",
     "zero_reduce_scatter_bucket_replicas", "zero_quantize_blocks", "zero_dequantize_blocks",
     "zero_gather_bucket_q8", "zero_reduce_scatter_bucket_q", "zero_debug_hold_staged",
+    "zero_noalloc_scratch_bytes",
 )
 ZERO_Q_BLOCK = 256
 
@@ -99,8 +100,10 @@ def load_library():
                                        C.POINTER(Hyper), C.c_float, C.c_int64, P, P]
     lib.zero_destroy.argtypes = [P]
     lib.zero_destroy.restype = None
+    lib.zero_noalloc_scratch_bytes.argtypes = []
+    lib.zero_noalloc_scratch_bytes.restype = U64
     for name in EXPORTS:
-        if name not in ("zero_last_error", "zero_destroy"):
+        if name not in ("zero_last_error", "zero_destroy", "zero_noalloc_scratch_bytes"):
             getattr(lib, name).restype = C.c_int
     _lib = lib
     return lib
@@ -262,6 +265,11 @@ def zero_bytes_moved(h) -> dict:
     b = Bytes()
     _check(load_library().zero_bytes_moved(h, C.byref(b)), h)
     return {f: getattr(b, f) for f, _ in Bytes._fields_}
+
+
+def zero_noalloc_scratch_bytes() -> int:
+    """Bytes of the static device array behind zero_step_noalloc (host query)."""
+    return int(load_library().zero_noalloc_scratch_bytes())
 
 
 def zero_step_noalloc(psi: int, n_ranks: int, stage: int, dtype: int, align: int, grads, params,

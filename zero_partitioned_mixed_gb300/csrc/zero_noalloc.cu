@@ -96,6 +96,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 }  // namespace
 
+extern "C" uint64_t zero_noalloc_scratch_bytes(void) { return kScratchBytes; }
+
 extern "C" int zero_step_noalloc(uint64_t psi, int n_ranks, int stage, int dtype, int align,
                                  const void* const* grads, void* const* params, float* master, float* m,
                                  float* v, const zero_hyper_t* hyper, float loss_scale, int64_t steps_applied,
