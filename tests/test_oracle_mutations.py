@@ -39,6 +39,9 @@ PIN_RUNS = [
     (pins.test_overflow_skips_step_and_halves_scale, dict(stage=1, bad=np.inf)),
     (pins.test_overflow_skips_step_and_halves_scale, dict(stage=3, bad=np.nan)),
     (pins.test_norm_of_constant_gradient, {}),
+    (pins.test_rank_sum_is_left_to_right_from_positive_zero, {}),
+    (pins.test_norm_accumulates_in_double, dict(stage=0)),
+    (pins.test_norm_accumulates_in_double, dict(stage=2)),
     (pins.test_clip_scales_gradient_to_max_norm, {}),
     (pins.test_replicas_equal_cast_of_master, {}),
     (pins.test_quantizer_is_lossless_on_its_grid, {}),
@@ -227,6 +230,37 @@ def persist_step_stale_replicas(state, bucket_grads, buckets, h, p0):
     return out, res, old
 
 
+def rank_sum_reversed(grads_f32):
+    s = np.zeros(np.asarray(grads_f32[0]).shape, np.float32)
+    for g in reversed(list(grads_f32)):
+        s = s + np.asarray(g, np.float32)
+    return s
+
+
+def rank_sum_from_first_rank(grads_f32):
+    gs = [np.asarray(g, np.float32) for g in grads_f32]
+    s = gs[0].copy()
+    for g in gs[1:]:
+        s = s + g
+    return s
+
+
+def norm_shards_in_fp32(ghat_shards, part):
+    total = np.float32(0.0)
+    for r, real in enumerate(part.real):
+        x = np.asarray(ghat_shards[r][:real], np.float32)
+        total = np.float32(total + np.sum(x * x, dtype=np.float32))
+    return math.sqrt(float(total))
+
+
+def norm_full_in_fp32(ghat, part):
+    total = np.float32(0.0)
+    for off, real in zip(part.offsets, part.real):
+        x = np.asarray(ghat[off:off + real], np.float32)
+        total = np.float32(total + np.sum(x * x, dtype=np.float32))
+    return math.sqrt(float(total))
+
+
 MUTANTS = [
     ("adam_update", adam_swapped_beta),
     ("adam_update", adam_no_decay),
@@ -235,6 +269,10 @@ MUTANTS = [
     ("step_scalars", scalars_no_bias_correction),
     ("step_scalars", scalars_t_off_by_one),
     ("rank_sum", rank_sum_drops_last),
+    ("rank_sum", rank_sum_reversed),
+    ("rank_sum", rank_sum_from_first_rank),
+    ("_norm_from_shards", norm_shards_in_fp32),
+    ("grad_norm", norm_full_in_fp32),
     ("unscale", unscale_forgets_scale),
     ("unscale", unscale_forgets_n),
     ("partition", partition_off_by_one),

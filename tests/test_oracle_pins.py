@@ -396,6 +396,30 @@ def test_norm_of_constant_gradient():
     assert res.norm == 0.375 * 8
 
 
+def test_rank_sum_is_left_to_right_from_positive_zero():
+    # The reduction order the pages leave open is fixed here as ranks 0..N-1,
+    # each addition rounded in fp32, starting from +0.  Two cases checkable by
+    # hand pin it: 1e8 - 1e8 + 1 is 1 left to right, but 0 right to left
+    # (1 - 1e8 rounds to -1e8 in fp32); and -0 + -0 from +0 is +0, while
+    # starting from the first rank would keep -0.
+    s = O.rank_sum([np.array([1e8], np.float32), np.array([-1e8], np.float32), np.array([1.0], np.float32)])
+    assert s.dtype == np.float32 and s[0] == np.float32(1.0)
+    z = O.rank_sum([np.array([-0.0], np.float32), np.array([-0.0], np.float32)])
+    assert z[0] == 0.0 and not np.signbit(z[0])
+
+
+@pytest.mark.parametrize("stage", [0, 1, 2, 3])
+def test_norm_accumulates_in_double(stage):
+    # One rank, g_hat = [2^26, 1, 1, 1, 1] (exact in bf16): the sum of squares
+    # 2^52 + 4 is exact in fp64 (spacing 1 there) but 2^52 in fp32 (spacing
+    # 2^29), so the norm is sqrt(2^52 + 4), not 2^26.
+    part = O.partition(5, 1, 1)
+    g = O.rne16(np.array([[2.0 ** 26, 1, 1, 1, 1]], np.float32), O.BF16)
+    st = O.init_state(stage, O.BF16, part, np.zeros(5, np.float32))
+    _, res = O.step(st, g, O.Hyper(eps=1e-8), [(0, 5)] if stage == 3 else None)
+    assert res.norm == math.sqrt(2.0 ** 52 + 4) and res.norm != 2.0 ** 26
+
+
 def test_clip_scales_gradient_to_max_norm():
     part, master, m, v, grads = _random_case(13, 500, 2, O.FP16)
     h_free = O.Hyper(beta1=0.75, eps=1e-8)
