@@ -40,6 +40,7 @@ PIN_RUNS = [
     (pins.test_overflow_skips_step_and_halves_scale, dict(stage=3, bad=np.nan)),
     (pins.test_norm_of_constant_gradient, {}),
     (pins.test_rank_sum_is_left_to_right_from_positive_zero, {}),
+    (pins.test_unscale_is_one_rounded_division, {}),
     (pins.test_norm_accumulates_in_double, dict(stage=0)),
     (pins.test_norm_accumulates_in_double, dict(stage=2)),
     (pins.test_clip_scales_gradient_to_max_norm, {}),
@@ -245,6 +246,10 @@ def rank_sum_from_first_rank(grads_f32):
     return s
 
 
+def unscale_two_roundings(s, n_ranks, loss_scale):
+    return ((np.asarray(s, np.float32) / np.float32(n_ranks)) / np.float32(loss_scale)).astype(np.float32)
+
+
 def norm_shards_in_fp32(ghat_shards, part):
     total = np.float32(0.0)
     for r, real in enumerate(part.real):
@@ -275,6 +280,7 @@ MUTANTS = [
     ("grad_norm", norm_full_in_fp32),
     ("unscale", unscale_forgets_scale),
     ("unscale", unscale_forgets_n),
+    ("unscale", unscale_two_roundings),
     ("partition", partition_off_by_one),
     ("partition", partition_no_padding),
     ("rne16", rne16_truncates),

@@ -408,6 +408,26 @@ def test_rank_sum_is_left_to_right_from_positive_zero():
     assert z[0] == 0.0 and not np.signbit(z[0])
 
 
+def _nearest_f32(x):
+    # the fp32 value nearest the rational x, ties to even mantissa, found
+    # among the neighbours of its double approximation (exact arithmetic)
+    from fractions import Fraction
+    d = np.float32(float(x))
+    cands = [np.nextafter(d, np.float32(-np.inf)), d, np.nextafter(d, np.float32(np.inf))]
+    return min(cands, key=lambda c: (abs(Fraction(float(c)) - x), int(np.float32(c).view(np.uint32)) & 1))
+
+
+def test_unscale_is_one_rounded_division():
+    # g_hat = s / f32(N * scale): one division, rounded once.  With N = 3 and
+    # scale = 1000 (not powers of two) dividing by N and then by the scale
+    # rounds twice, and these sums are ones where that changes the result.
+    from fractions import Fraction
+    s = np.array([41.32598114013672, 1042.513427734375, -128.53466796875], np.float32)
+    got = O.unscale(s, 3, 1000.0)
+    want = [_nearest_f32(Fraction(float(x)) / 3000) for x in s]
+    assert got.dtype == np.float32 and [float(x) for x in got] == [float(x) for x in want]
+
+
 @pytest.mark.parametrize("stage", [0, 1, 2, 3])
 def test_norm_accumulates_in_double(stage):
     # One rank, g_hat = [2^26, 1, 1, 1, 1] (exact in bf16): the sum of squares
