@@ -54,6 +54,14 @@ PIN_RUNS = [
     (pins.test_persistent_threshold_is_strict_and_degenerate_cases, {}),
     (pins.test_persistent_comm_and_memory_endpoints, {}),
     (pins.test_persistence_moves_no_value, dict(dt="fp16")),
+    (pins.test_unpadded_toy_would_not_print_156, {}),
+    (pins.test_bytes_per_param_at_32, {}),
+    (pins.test_table1_model_sizes_fit_32gb, {}),
+    (pins.test_ring_stage3_cell_is_the_documented_gap, {}),
+    (pins.test_widen16_exact_roundtrip, {}),
+    (pins.test_overflow_in_padding_is_ignored_and_scale_floor, {}),
+    (pins.test_quantized_gather_reproduces_grid_weights, {}),
+    (pins.test_guide_threshold_on_the_model_lists, {}),
 ]
 
 
@@ -246,6 +254,12 @@ def rank_sum_from_first_rank(grads_f32):
     return s
 
 
+def skip_without_floor(state):
+    out = state.copy()
+    out.loss_scale = state.loss_scale / 2.0
+    return out
+
+
 def unscale_two_roundings(s, n_ranks, loss_scale):
     return ((np.asarray(s, np.float32) / np.float32(n_ranks)) / np.float32(loss_scale)).astype(np.float32)
 
@@ -288,6 +302,7 @@ MUTANTS = [
     ("clip_factor", clip_wrong_comparison),
     ("_norm_from_shards", norm_wrong_shard_index),
     ("_skip", skip_keeps_scale),
+    ("_skip", skip_without_floor),
     ("quantize_blocks", quant_qmax_off_by_one),
     ("quantize_blocks", quant_floor),
     ("dequantize_blocks", dequant_forgets_lo),
