@@ -106,11 +106,11 @@ struct Io1 {
 
 // ------------------------------------------------------------------ scalars
 // Adam coefficients of step t, formed in double and rounded once to fp32.
-__device__ StepScalars make_scalars(const HyperDev& h, int64_t t) {
+// Two halves with one double pow() each, so that two threads can form them
+// at once (an FP64 pow is a long dependent chain on GB300).
+__device__ void scalars_b1_part(const HyperDev& h, int64_t t, StepScalars& s) {
     const double lr = h.lr, b1 = h.beta1, b2 = h.beta2, wd = h.weight_decay;
     const double bc1 = __dsub_rn(1.0, pow(b1, static_cast<double>(t)));
-    const double bc2 = __dsub_rn(1.0, pow(b2, static_cast<double>(t)));
-    StepScalars s;
     s.b1 = h.beta1;
     s.b2 = h.beta2;
     s.a1 = __double2float_rn(__dsub_rn(1.0, b1));
@@ -118,7 +118,16 @@ __device__ StepScalars make_scalars(const HyperDev& h, int64_t t) {
     s.eps = h.eps;
     s.dfac = __double2float_rn(__dsub_rn(1.0, __dmul_rn(lr, wd)));
     s.step_size = __double2float_rn(__ddiv_rn(lr, bc1));
-    s.bc2s = __double2float_rn(__dsqrt_rn(bc2));
+}
+__device__ float scalars_bc2s(const HyperDev& h, int64_t t) {
+    const double b2 = h.beta2;
+    const double bc2 = __dsub_rn(1.0, pow(b2, static_cast<double>(t)));
+    return __double2float_rn(__dsqrt_rn(bc2));
+}
+__device__ StepScalars make_scalars(const HyperDev& h, int64_t t) {
+    StepScalars s;
+    scalars_b1_part(h, t, s);
+    s.bc2s = scalars_bc2s(h, t);
     return s;
 }
 
@@ -145,7 +154,22 @@ struct Pro {
 // Prologue of kernels that reduce gradients: unscale denominator N*scale
 // (fp32 product, as the oracle forms it) and, for the one-pass kernels,
 // the Adam coefficients of step t+1.
+// The status word holds the step scalars for (t + 1, these hyper-parameters).
+__device__ __forceinline__ bool scalars_cached(const DevStatus* st, const HyperDev& h) {
+    const HyperDev& k = st->sc_key;
+    return st->sc_t == st->t + 1 && __float_as_uint(k.lr) == __float_as_uint(h.lr) &&
+           __float_as_uint(k.beta1) == __float_as_uint(h.beta1) &&
+           __float_as_uint(k.beta2) == __float_as_uint(h.beta2) &&
+           __float_as_uint(k.eps) == __float_as_uint(h.eps) &&
+           __float_as_uint(k.weight_decay) == __float_as_uint(h.weight_decay);
+}
+
 __device__ __forceinline__ void prologue_reduce(const Args& a, Pro& pro, bool with_scalars) {
+    // not cached: thread 32 forms bc2s while thread 0 forms the rest
+    if (with_scalars && threadIdx.x == 32) {
+        const DevStatus* st = a.ws.status;
+        if (!scalars_cached(st, a.hyper)) pro.sc.bc2s = scalars_bc2s(a.hyper, st->t + 1);
+    }
     if (threadIdx.x == 0) {
         const DevStatus* st = a.ws.status;
         const float den = __fmul_rn(static_cast<float>(a.n_ranks), st->loss_scale);
@@ -161,14 +185,8 @@ __device__ __forceinline__ void prologue_reduce(const Args& a, Pro& pro, bool wi
         pro.use_clip = st->use_clip;
         pro.overflow = st->overflow;
         if (with_scalars) {
-            const HyperDev& k = st->sc_key;
-            const HyperDev& h = a.hyper;
-            const bool hit = st->sc_t == st->t + 1 && __float_as_uint(k.lr) == __float_as_uint(h.lr) &&
-                             __float_as_uint(k.beta1) == __float_as_uint(h.beta1) &&
-                             __float_as_uint(k.beta2) == __float_as_uint(h.beta2) &&
-                             __float_as_uint(k.eps) == __float_as_uint(h.eps) &&
-                             __float_as_uint(k.weight_decay) == __float_as_uint(h.weight_decay);
-            pro.sc = hit ? st->sc_next : make_scalars(h, st->t + 1);
+            if (scalars_cached(st, a.hyper)) pro.sc = st->sc_next;
+            else scalars_b1_part(a.hyper, st->t + 1, pro.sc);
         } else {
             pro.sc = st->sc;
         }
