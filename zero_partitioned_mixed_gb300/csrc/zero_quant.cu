@@ -157,24 +157,6 @@ __device__ __forceinline__ void load_codes8(const void* codes, uint64_t e0, uint
     }
 }
 
-// A lane's 8 codes at element e0 (e0 % 8 == 0) as exact floats: the byte
-// (or nibble) is placed under the exponent of 2^23 and 2^23 subtracted.
-template <int BITS>
-__device__ __forceinline__ void load_codes8_f(const void* codes, uint64_t e0, float (&f)[8]) {
-    if (BITS == 8) {
-        const uint2 w = __ldcs(reinterpret_cast<const uint2*>(static_cast<const unsigned char*>(codes) + e0));
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            f[k] = __fsub_rn(__uint_as_float(__byte_perm(w.x, 0x4B000000u, 0x7540u | k)), kTwo23);
-            f[4 + k] = __fsub_rn(__uint_as_float(__byte_perm(w.y, 0x4B000000u, 0x7540u | k)), kTwo23);
-        }
-    } else {
-        const uint32_t w = __ldcs(reinterpret_cast<const unsigned int*>(static_cast<const unsigned char*>(codes) + (e0 >> 1)));
-#pragma unroll
-        for (int k = 0; k < 8; ++k) f[k] = __fsub_rn(__uint_as_float(((w >> (4 * k)) & 0xFu) | 0x4B000000u), kTwo23);
-    }
-}
-
 // Two fp32 lanes in one 64-bit register for the packed add/sub/mul.rn.f32x2
 // of sm_100 and later: each half is an ordinary fp32 operation rounded once,
 // so results are those of the scalar instructions, at half the issue cost.
