@@ -31,6 +31,8 @@ PIN_RUNS = [
     (pins.test_tiny_case_by_hand, dict(stage=3, dt="bf16")),
     (pins.test_tiny_case_by_hand, dict(stage=0, dt="fp16")),
     (pins.test_loss_scale_divides_out, dict(stage=2)),
+    (pins.test_padding_gradients_are_ignored, dict(stage=1)),
+    (pins.test_padding_gradients_are_ignored, dict(stage=3)),
     (pins.test_all_stages_identical, dict(dt="bf16")),
     (pins.test_all_reduce_is_reduce_scatter_then_all_gather, {}),
     (pins.test_adam_step1_is_lr_times_sign, {}),
@@ -254,6 +256,23 @@ def rank_sum_from_first_rank(grads_f32):
     return s
 
 
+def update_shards_with_padding(state, ghat_shards, h, norm):
+    # each owner updates its whole shard, padding included
+    part = state.part
+    c = Z.clip_factor(norm, h.max_norm)
+    sc = Z.step_scalars(h, state.t + 1)
+    out = state.copy()
+    for r, off in enumerate(part.offsets):
+        gr = np.asarray(ghat_shards[r][:part.shard], np.float32)
+        if c is not None:
+            gr = gr * c
+        sl = slice(off, off + part.shard)
+        p, m, v = Z.adam_update(state.master[sl], state.m[sl], state.v[sl], gr, sc)
+        out.master[sl], out.m[sl], out.v[sl] = p, m, v
+    out.t = state.t + 1
+    return out, c
+
+
 def skip_without_floor(state):
     out = state.copy()
     out.loss_scale = state.loss_scale / 2.0
@@ -303,6 +322,7 @@ MUTANTS = [
     ("_norm_from_shards", norm_wrong_shard_index),
     ("_skip", skip_keeps_scale),
     ("_skip", skip_without_floor),
+    ("_update_shards", update_shards_with_padding),
     ("quantize_blocks", quant_qmax_off_by_one),
     ("quantize_blocks", quant_floor),
     ("dequantize_blocks", dequant_forgets_lo),

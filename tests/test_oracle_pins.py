@@ -216,6 +216,28 @@ def test_tiny_case_by_hand(stage, dt):
         assert np.array_equal(res.gathered_bwd[1][0], before[3:8])
 
 
+@pytest.mark.parametrize("stage", [0, 1, 2, 3])
+def test_padding_gradients_are_ignored(stage):
+    # The padding [psi, psi_pad) of every gradient row is read as zero and
+    # the padding of master, m, v and the 16-bit copies stays zero: finite
+    # garbage there changes nothing (the tiny case, psi = 5 of psi_pad = 8).
+    part = O.partition(5, 2, 2)
+    h = O.Hyper(lr=2.0 ** -6, beta1=0.5, beta2=0.75, eps=0.0)
+    p0 = np.array([0.5, 0.25, 0.0, -0.5, 1.0], np.float32)
+    buckets = [(0, 3), (3, 8)] if stage == 3 else None
+    clean = _tiny_grads(O.FP16)
+    dirty = clean.copy()
+    dirty[:, 5:] = _bits([0.75, -3.0, 1.5], O.FP16)
+    a, _ = O.step(O.init_state(stage, O.FP16, part, p0), clean, h, buckets)
+    b, _ = O.step(O.init_state(stage, O.FP16, part, p0), dirty, h, buckets)
+    for x, y in ((a.master, b.master), (a.m, b.m), (a.v, b.v), (a.params, b.params)):
+        assert x.tobytes() == y.tobytes()
+    mb = b.master if stage != 0 else b.master[0]
+    assert np.all(mb[5:8] == 0) and np.all((b.m if stage != 0 else b.m[0])[5:8] == 0)
+    qb = b.params if stage == 3 else b.params[0]
+    assert np.all(qb[5:8] == 0)
+
+
 @pytest.mark.parametrize("stage", [1, 2, 3])
 def test_loss_scale_divides_out(stage):
     # Loss scaling: gradients computed at scale 2^10 and unscaled by 2^10 give
