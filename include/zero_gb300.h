@@ -36,6 +36,12 @@
  *    events); gathers may overlap them on another stream.  At most 64
  *    launches of one handle may be in flight at once: each takes the next
  *    of 64 work counters, round-robin.
+ *  - The streaming kernels are launched with programmatic stream
+ *    serialisation: the next one may be scheduled while the previous one
+ *    drains, and waits in its first instruction until that one has
+ *    completed.  Stream order is unchanged for the caller; a caller's own
+ *    kernel or copy on the same stream runs after the library's work as
+ *    usual, and the calls can be captured into a CUDA graph.
  *  - Elements [psi, psi_pad) are padding: gradients there are ignored, and
  *    master/m/v/params there are written as 0.
  *  - The loss scale, the count t of applied Adam steps and the live slot of
