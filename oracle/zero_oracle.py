@@ -685,11 +685,13 @@ def quantize_blocks(x: np.ndarray, bits: int, block: int = Q_BLOCK):
     "CMU 11-868 L18" notes, other memory optimizations (ZeRO++): parameters
     are block-quantized from FP16 to INT8 with zero-point quantization for
     the forward gather, and the backward reduce-scatter is quantized to INT8
-    or INT4.  Reading taken: blocks of `block` consecutive elements from the
+    or INT4.  The notes give no formula; the reading taken is the plain
+    zero-point definition: blocks of `block` consecutive elements from the
     start of the buffer (the last one may be short); per block lo = min,
-    hi = max, scale = (hi - lo) / (2^bits - 1) and inv = (2^bits - 1) / (hi - lo)
-    in fp32; code q = rint((x - lo) * inv) clamped to [0, 2^bits - 1], or 0
-    when scale is 0 (one division per block, a multiply per element).  min/max propagate NaN (a NaN element makes its whole block NaN
+    hi = max and scale = (hi - lo) / (2^bits - 1); code q = rint((x - lo) / scale)
+    clamped to [0, 2^bits - 1], or 0 when scale is 0.  Every operation is
+    one fp32 operation rounded once (subtract, divide, then round half to
+    even).  min/max propagate NaN (a NaN element makes its whole block NaN
     after dequantization, so overflow detection still sees it); a code that
     comes out NaN is stored as 0.  Returns
     (codes uint8, one per element; scale fp32; lo fp32).
@@ -713,8 +715,7 @@ def quantize_blocks(x: np.ndarray, bits: int, block: int = Q_BLOCK):
         scale[k], lo[k] = s, l
         if s != 0:
             with np.errstate(invalid="ignore", divide="ignore", over="ignore"):
-                inv = qmax / rng
-                q = np.rint((blk - l) * inv)
+                q = np.rint((blk - l) / s)
             q = np.where(np.isnan(q), 0, q)          # a NaN's code is 0 (its block is NaN anyway)
             codes[k * block:(k + 1) * block] = np.clip(q, 0, qmax).astype(np.uint8)
     return codes, scale, lo

@@ -49,6 +49,7 @@ PIN_RUNS = [
     (pins.test_replicas_equal_cast_of_master, {}),
     (pins.test_quantizer_is_lossless_on_its_grid, {}),
     (pins.test_quantizer_error_bound_and_order, {}),
+    (pins.test_quantizer_code_is_one_division_by_the_scale, {}),
     (pins.test_quantizer_constant_block_and_nan, {}),
     (pins.test_int4_packing, {}),
     (pins.test_quantized_reduce_scatter_equals_plain_on_grid_gradients, dict(bits=8)),
@@ -200,6 +201,24 @@ def quant_floor(x, bits, block=Z.Q_BLOCK):
     return np.clip(q, 0, (1 << bits) - 1).astype(np.uint8), scale, lo
 
 
+def quant_multiplies_by_inverse(x, bits, block=Z.Q_BLOCK):
+    # codes from (x - lo) * f32((2^bits - 1) / (hi - lo)) instead of (x - lo) / scale
+    x = np.asarray(x, np.float32)
+    codes, scale, lo = orig_quant(x, bits, block)
+    qmax = np.float32((1 << bits) - 1)
+    out = np.zeros(x.size, np.uint8)
+    for b in range(scale.size):
+        blk = x[b * block:(b + 1) * block]
+        if scale[b] == 0:
+            continue
+        with np.errstate(invalid="ignore", divide="ignore", over="ignore"):
+            inv = qmax / np.float32(np.float32(blk.max() + np.float32(0)) - lo[b])
+            q = np.rint((blk - lo[b]) * inv)
+        q = np.where(np.isnan(q), 0, q)
+        out[b * block:(b + 1) * block] = np.clip(q, 0, qmax).astype(np.uint8)
+    return out, scale, lo
+
+
 def dequant_forgets_lo(codes, scale, lo, block=Z.Q_BLOCK):
     return orig_dequant(codes, scale, np.zeros_like(lo), block)
 
@@ -325,6 +344,7 @@ MUTANTS = [
     ("_update_shards", update_shards_with_padding),
     ("quantize_blocks", quant_qmax_off_by_one),
     ("quantize_blocks", quant_floor),
+    ("quantize_blocks", quant_multiplies_by_inverse),
     ("dequantize_blocks", dequant_forgets_lo),
     ("pack_int4", pack4_swapped_nibbles),
     ("persistent_layout", persist_threshold_inclusive),

@@ -503,6 +503,48 @@ def test_quantizer_is_lossless_on_its_grid():
     assert np.array_equal(c4, k4.astype(np.uint8)) and s4[0] == np.float32(0.125)
 
 
+def _rint_even(q):
+    # nearest integer to the rational q, ties to even
+    return round(q)
+
+
+def test_quantizer_code_is_one_division_by_the_scale():
+    # The notes name zero-point block quantization and give no formula, so the
+    # oracle takes the plain definition: code = rint((x - lo) / scale), the
+    # subtraction and the division each one fp32 operation rounded once.
+    # Forming 1 / scale once per block and multiplying by it rounds
+    # differently for values near the middle between two levels; the blocks
+    # here are made of such values (lo = 0, so x - lo is exact) and their
+    # codes are worked out in exact rational arithmetic.
+    from fractions import Fraction
+    rng = np.random.default_rng(41)
+    for bits in (8, 4):
+        qmax = (1 << bits) - 1
+        hi = np.float32(rng.uniform(0.5, 2.0))
+        s = _nearest_f32(Fraction(float(hi)) / qmax)
+        inv = _nearest_f32(Fraction(qmax) / Fraction(float(hi)))
+        vals, want, differ = [], [], 0
+        for k in range(qmax):
+            mid = np.float32((k + 0.5) * float(s))
+            for step in (-2, -1, 0, 1, 2):
+                x = mid
+                for _ in range(abs(step)):
+                    x = np.nextafter(x, np.float32(np.inf if step > 0 else -np.inf))
+                fx = Fraction(float(x))
+                code = min(qmax, max(0, _rint_even(Fraction(float(_nearest_f32(fx / Fraction(float(s))))))))
+                short = min(qmax, max(0, _rint_even(Fraction(float(_nearest_f32(fx * Fraction(float(inv))))))))
+                if code != short and len(vals) < 254:
+                    vals.append(x)
+                    want.append(code)
+                    differ += 1
+        assert differ >= 3, differ
+        block = np.array([0.0, hi] + vals, np.float32)
+        codes, scale, lo = O.quantize_blocks(block, bits, block=block.size)
+        assert scale[0] == s and lo[0] == 0.0
+        assert list(codes[:2]) == [0, qmax]
+        assert [int(c) for c in codes[2:]] == want
+
+
 def test_quantizer_error_bound_and_order():
     rng = np.random.default_rng(22)
     x = rng.normal(0, 3, 5000).astype(np.float32)
