@@ -43,9 +43,10 @@ Readings taken where the pages are silent:
 * Overflow: any non-finite g_hat over the real elements -> the step is
   skipped, all model state is left bit-identical, the loss scale halves
   (floor 1.0) and t does not advance.
-* Norm: sum of g_hat**2 in fp64, per owner shard then over ranks in rank
-  order; clip factor c = max_norm / (norm + 1e-6) in double, applied as
-  g_hat * f32(c) only when max_norm > 0 and c < 1.
+* Norm: sum of g_hat**2 in fp64, left to right within each owner shard,
+  then the shards' sums in rank order; clip factor c = max_norm /
+  (norm + 1e-6) in double, applied as g_hat * f32(c) only when
+  max_norm > 0 and c < 1.
 * Cast: IEEE round-to-nearest-even to fp16 (overflow to inf) or bf16.
 * Padding elements [psi, psi_pad) are never updated; they stay zero.
 """
@@ -65,7 +66,7 @@ __all__ = [
     "FP16", "BF16", "Partition", "partition", "model_state_bytes",
     "comm_elems_paper", "comm_elems_ring", "comm_elems_ring_allreduce_zero1",
     "widen16", "rne16", "Hyper", "StepScalars", "step_scalars",
-    "rank_sum", "unscale", "has_overflow", "grad_norm", "clip_factor",
+    "rank_sum", "unscale", "has_overflow", "sq_sum_sequential", "grad_norm", "clip_factor",
     "adam_update", "State", "StepResult", "init_state", "step",
     "step_stage0", "step_stage1", "step_stage2", "step_stage3",
     "all_reduce_mean", "reduce_scatter_mean", "all_gather",
@@ -297,17 +298,27 @@ def has_overflow(ghat_real: np.ndarray) -> bool:
     return not bool(np.all(np.isfinite(ghat_real)))
 
 
+def sq_sum_sequential(x: np.ndarray) -> float:
+    """sum of x_i**2 in fp64, added left to right from +0 (one rounding per addition).
+
+    np.cumsum adds strictly in order; its last entry is the sequential sum.
+    """
+    x = np.asarray(x, np.float64)
+    if x.size == 0:
+        return 0.0
+    return float(np.cumsum(x * x)[-1])
+
+
 def grad_norm(ghat: np.ndarray, part: Partition) -> float:
     """Global L2 norm over the flattened gradient (real elements only).
 
     ZeRO summary, residual states: the gradient-norm computation runs over
     the flattened gradient buffer.  Each owner sums its shard's squares in
-    fp64, then the ranks' sums are added in rank order.
+    fp64 sequentially, then the ranks' sums are added in rank order.
     """
     total = 0.0
     for off, real in zip(part.offsets, part.real):
-        x = np.asarray(ghat[off:off + real], np.float64)
-        total = total + float(np.sum(x * x))
+        total = total + sq_sum_sequential(ghat[off:off + real])
     return math.sqrt(total)
 
 
@@ -477,10 +488,10 @@ def _update_shards(state: State, ghat_shards: Sequence[np.ndarray], h: Hyper,
 
 
 def _norm_from_shards(ghat_shards: Sequence[np.ndarray], part: Partition) -> float:
+    """The norm of grad_norm, from the owners' shards of the averaged gradient."""
     total = 0.0
     for r, real in enumerate(part.real):
-        x = np.asarray(ghat_shards[r][:real], np.float64)
-        total = total + float(np.sum(x * x))
+        total = total + sq_sum_sequential(ghat_shards[r][:real])
     return math.sqrt(total)
 
 

@@ -46,6 +46,7 @@ PIN_RUNS = [
     (pins.test_norm_accumulates_in_double, dict(stage=0)),
     (pins.test_norm_accumulates_in_double, dict(stage=2)),
     (pins.test_clip_scales_gradient_to_max_norm, {}),
+    (pins.test_norm_sums_each_shard_left_to_right, dict(stage=1)),
     (pins.test_replicas_equal_cast_of_master, {}),
     (pins.test_quantizer_is_lossless_on_its_grid, {}),
     (pins.test_quantizer_error_bound_and_order, {}),
@@ -310,6 +311,15 @@ def norm_shards_in_fp32(ghat_shards, part):
     return math.sqrt(float(total))
 
 
+def norm_shards_pairwise(ghat_shards, part):
+    # numpy's own summation order (several accumulators, then pairwise)
+    total = 0.0
+    for r, real in enumerate(part.real):
+        x = np.asarray(ghat_shards[r][:real], np.float64)
+        total = total + float(np.sum(x * x))
+    return math.sqrt(total)
+
+
 def norm_full_in_fp32(ghat, part):
     total = np.float32(0.0)
     for off, real in zip(part.offsets, part.real):
@@ -329,6 +339,7 @@ MUTANTS = [
     ("rank_sum", rank_sum_reversed),
     ("rank_sum", rank_sum_from_first_rank),
     ("_norm_from_shards", norm_shards_in_fp32),
+    ("_norm_from_shards", norm_shards_pairwise),
     ("grad_norm", norm_full_in_fp32),
     ("unscale", unscale_forgets_scale),
     ("unscale", unscale_forgets_n),

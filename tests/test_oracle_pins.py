@@ -462,6 +462,21 @@ def test_norm_accumulates_in_double(stage):
     assert res.norm == math.sqrt(2.0 ** 52 + 4) and res.norm != 2.0 ** 26
 
 
+@pytest.mark.parametrize("stage", [1, 3])
+def test_norm_sums_each_shard_left_to_right(stage):
+    # Each owner adds its shard's squares in order, in fp64.  One rank,
+    # bf16 g_hat = [1, 2^-27 x 16]: every square 2^-54 is below half an ulp
+    # of 1, so each addition after the first rounds back to 1 and the norm
+    # is exactly 1.  Adding the small squares first (pairwise or several
+    # accumulators) gives 1 + 2^-50 and a norm above 1.
+    part = O.partition(17, 1, 1)
+    g = O.rne16(np.array([[1.0] + [2.0 ** -27] * 16], np.float32), O.BF16)
+    assert np.array_equal(O.widen16(g, O.BF16)[0][1:], np.full(16, 2.0 ** -27, np.float32))
+    st = O.init_state(stage, O.BF16, part, np.zeros(17, np.float32))
+    _, res = O.step(st, g, O.Hyper(eps=1e-8), [(0, 17)] if stage == 3 else None)
+    assert res.norm == 1.0
+
+
 def test_clip_scales_gradient_to_max_norm():
     part, master, m, v, grads = _random_case(13, 500, 2, O.FP16)
     h_free = O.Hyper(beta1=0.75, eps=1e-8)
