@@ -72,7 +72,8 @@ __all__ = [
     "all_reduce_mean", "reduce_scatter_mean", "all_gather",
     "Q_BLOCK", "quantize_blocks", "dequantize_blocks", "pack_int4", "unpack_int4",
     "quantized_gather", "step_stage3_quantized",
-    "persistent_layout", "comm_elems_persistent", "model_state_bytes_persistent",
+    "persistent_layout", "comm_elems_persistent", "comm_elems_ring_persistent",
+    "model_state_bytes_persistent",
     "step_stage3_persistent",
 ]
 
@@ -621,6 +622,17 @@ def comm_elems_persistent(psi: int, psi_pers: int) -> int:
     the stage 1/2 parameters are refreshed.
     """
     return 2 * (psi - psi_pers) + psi + psi_pers
+
+
+def comm_elems_ring_persistent(psi: int, psi_pers: int, n_ranks: int) -> int:
+    """Ring-model elements sent per rank per ZeRO-3 step with a persistent region.
+
+    Each collective moves (N-1)/N of its elements ("zero-stages-simulation"
+    README, stage table): the forward and backward gathers of the
+    partitioned psi - psi_pers, the reduce-scatter of psi and the refresh
+    gather of psi_pers, i.e. (N-1)/N of comm_elems_persistent, rounded down.
+    """
+    return (n_ranks - 1) * comm_elems_persistent(psi, psi_pers) // n_ranks
 
 
 def model_state_bytes_persistent(psi: int, psi_pers: int, n_ranks: int, k: int = 12) -> int:

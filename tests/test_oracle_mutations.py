@@ -249,6 +249,10 @@ def persist_comm_no_refresh(psi, psi_pers):
     return 2 * (psi - psi_pers) + psi
 
 
+def persist_ring_no_refresh(psi, psi_pers, n_ranks):
+    return (n_ranks - 1) * (3 * psi - 2 * psi_pers) // n_ranks
+
+
 def persist_msb_no_replicas(psi, psi_pers, n_ranks, k=12):
     return ((4 + k) * psi) // n_ranks
 
@@ -361,6 +365,7 @@ MUTANTS = [
     ("persistent_layout", persist_threshold_inclusive),
     ("persistent_layout", persist_small_first),
     ("comm_elems_persistent", persist_comm_no_refresh),
+    ("comm_elems_ring_persistent", persist_ring_no_refresh),
     ("model_state_bytes_persistent", persist_msb_no_replicas),
     ("step_stage3_persistent", persist_step_stale_replicas),
 ]

@@ -692,6 +692,14 @@ def test_persistent_comm_and_memory_endpoints():
         assert O.comm_elems_persistent(pp, 1000) == 3 * pp - 1000
         assert O.model_state_bytes_persistent(pp, 0, n) == O.model_state_bytes(pp, n, 3)
         assert O.model_state_bytes_persistent(pp, pp, n) == O.model_state_bytes(pp, n, 2) + 2 * pp // n
+        # the ring model at the same ends: ZeRO-3's and ZeRO-2's (N-1)/N counts
+        assert O.comm_elems_ring_persistent(pp, 0, n) == O.comm_elems_ring(pp, n, 3)
+        assert O.comm_elems_ring_persistent(pp, pp, n) == O.comm_elems_ring(pp, n, 2)
+        # in between: (N-1)/N of each of the four collectives, summed exactly
+        from fractions import Fraction
+        k = Fraction(n - 1, n)
+        exact = 2 * k * (pp - 1000) + k * pp + k * 1000
+        assert O.comm_elems_ring_persistent(pp, 1000, n) == math.floor(exact)
 
 
 @pytest.mark.parametrize("dt", [O.FP16, O.BF16])
