@@ -65,6 +65,48 @@ def test_quantize_and_dequantize_match_oracle(dtype, bits, count):
     assert np.array_equal(bits16(out[:count]), want)
 
 
+def _near_midpoint_blocks(dtype, bits, n_blocks, seed):
+    # 256-element blocks [0, hi, x, ...] of 16-bit values x for which
+    # rint(x / scale) and rint(x * (1 / scale)) give different codes: the
+    # values near the middle between two levels that tell the plain division
+    # from a reciprocal multiply.  Found by enumerating every positive finite
+    # 16-bit value below hi.
+    qmax = np.float32((1 << bits) - 1)
+    top = 0x7C00 if dtype == "fp16" else 0x7F80
+    allv = O.widen16(np.arange(1, top, dtype=np.uint16), dtype)
+    rng = np.random.default_rng(seed)
+    his = allv[(allv > 0.25) & (allv < 4.0)]
+    blocks, differing = [], 0
+    for hi in rng.permutation(his):
+        x = allv[allv < hi]
+        with np.errstate(over="ignore"):
+            d = x[np.rint(x / np.float32(hi / qmax)) != np.rint(x * np.float32(qmax / hi))]
+        if d.size == 0:
+            continue
+        fill = rng.choice(x, 254 - d.size) if d.size < 254 else np.zeros(0, np.float32)
+        blk = np.concatenate([[np.float32(0), hi], d[:254], fill]).astype(np.float32)
+        blocks.append(blk)
+        differing += min(d.size, 254)
+        if len(blocks) == n_blocks:
+            break
+    return np.concatenate(blocks), differing
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("bits", [8, 4])
+def test_quantizer_divides_by_the_scale(dtype, bits):
+    x, differing = _near_midpoint_blocks(dtype, bits, 64, 3 + bits)
+    assert differing >= 40
+    xb = O.rne16(x, dtype)
+    assert np.array_equal(O.widen16(xb, dtype), x)
+    dev = torch.from_numpy(xb.view(np.int16)).cuda().view(S.torch_dtype(dtype))
+    codes, scales = _quantize_gpu(dev, dtype, bits)
+    packed, scale, lo = _oracle_codes(xb, dtype, bits)
+    assert np.array_equal(codes.cpu().numpy()[:packed.size], packed)
+    sc = scales.cpu().numpy()[:2 * _nb(x.size)]
+    assert np.array_equal(sc[0::2].view(np.uint32), scale.view(np.uint32))
+
+
 @pytest.mark.parametrize("a,b", [(0, 70_000), (1024, 1032), (13, 5_013), (256, 257)])
 def test_quantized_gather_matches_oracle(a, b):
     psi, n, dt = 80_000, 4, "bf16"

@@ -5,10 +5,10 @@
 // the forward gather (qwZ), and the backward reduce-scatter is quantized to
 // INT8 or INT4 (qgZ).  Format (the same as the CPU oracle's): blocks of 256
 // elements from the start of the buffer or bucket; per block lo = min,
-// hi = max (NaN propagates), scale = (hi - lo) / (2^bits - 1) and
-// inv = (2^bits - 1) / (hi - lo), code = rint((x - lo) * inv) clamped to
-// [0, 2^bits - 1] (0 when scale is 0, 0 for a NaN); dequantized
-// x' = lo + code * scale.
+// hi = max (NaN propagates), scale = (hi - lo) / (2^bits - 1), code =
+// rint((x - lo) / scale) clamped to [0, 2^bits - 1] (0 when scale is 0, 0
+// for a NaN), the subtraction and the division each rounded once;
+// dequantized x' = lo + code * scale.
 //
 // Two exact bit-level shortcuts keep the per-element cost to a few adds:
 // for 0 <= u < 2^22, u + 2^23 (rounded to nearest even) holds rint(u) in its
@@ -52,10 +52,27 @@ __device__ __forceinline__ float warp_qmax(float a) {
 
 constexpr float kTwo23 = 8388608.0f;
 
-// rint(clamp(u, 0, top)) as an integer; a NaN u gives 0 (fmaxf returns the
-// other operand).
-__device__ __forceinline__ uint32_t code_of(float x, float lo, float inv, float top) {
-    const float u = fminf(fmaxf(__fmul_rn(__fsub_rn(x, lo), inv), 0.0f), top);
+// rint(clamp(q, 0, top)) as an integer for q = (x - lo) / scale rounded once
+// (IEEE division); a NaN q gives 0 (fmaxf returns the other operand).
+//
+// The division is taken only where it can matter.  With rcp = 1/scale
+// rounded once, u = d * rcp (d = x - lo) differs from the exact d / scale by
+// a factor (1 + e1)(1 + e2), |e1|, |e2| <= 2^-24, and the rounded quotient q
+// from it by at most 2^-24 relative, so |u - q| < u * 2^-22.  rint(clamp(.))
+// is constant between consecutive half-integers, so u and q give the same
+// code unless a half-integer lies within u * 2^-22 of u.  The test below
+// takes the division whenever one lies within u * 2^-20 (a margin of 4):
+// for values spread over the levels that is about one element in 4000.
+// fast is false for a block whose scale is not a normal number in
+// [2^-100, 2^100] (the bounds above assume no underflow or overflow), and
+// then every element is divided.
+__device__ __forceinline__ uint32_t code_of(float x, float lo, float scale, float rcp, bool fast, float top) {
+    const float d = __fsub_rn(x, lo);
+    float q = __fmul_rn(d, rcp);
+    // 0 <= q < 2^23 here, so q - floor(q) is exact
+    const float off = fabsf(__fsub_rn(__fsub_rn(q, floorf(q)), 0.5f));
+    if (!fast || !(off > __fmul_rn(fabsf(q), 0x1p-20f))) q = __fdiv_rn(d, scale);
+    const float u = fminf(fmaxf(q, 0.0f), top);
     return __float_as_uint(__fadd_rn(u, kTwo23)) & 0x1FFu;
 }
 
@@ -87,9 +104,11 @@ __device__ __forceinline__ int load_lane8(const void* src, uint64_t e0, uint64_t
     return nv;
 }
 
-// Block min/max over the warp; every lane gets {scale, inv, lo}.
+// Block min/max over the warp; every lane gets {scale, lo}, the rounded
+// reciprocal of the scale and whether code_of may screen with it.
 template <int BITS>
-__device__ __forceinline__ void block_scale(const float (&x)[8], int nv, float& scale, float& inv, float& lo) {
+__device__ __forceinline__ void block_scale(const float (&x)[8], int nv, float& scale, float& lo, float& rcp,
+                                            bool& fast) {
     float mn = __int_as_float(0x7F800000), mx = -__int_as_float(0x7F800000);
 #pragma unroll
     for (int k = 0; k < 8; ++k)
@@ -104,7 +123,8 @@ __device__ __forceinline__ void block_scale(const float (&x)[8], int nv, float& 
     const float range = __fsub_rn(mx, mn);
     const float top = static_cast<float>((1 << BITS) - 1);
     scale = __fdiv_rn(range, top);
-    inv = __fdiv_rn(top, range);
+    fast = scale >= 0x1p-100f && scale <= 0x1p100f;
+    rcp = fast ? __frcp_rn(scale) : 0.0f;
 }
 
 // Eight byte codes (each < 256) packed little-endian into 8 bytes.
@@ -254,11 +274,12 @@ __device__ __forceinline__ void quantize_blocks_u(const unsigned short* src, uin
 #pragma unroll
     for (int u = 0; u < kQUnroll; ++u) {
         if (blk0 + u >= nb) break;
-        float scale, inv, lo;
-        block_scale<BITS>(x[u], nv[u], scale, inv, lo);
+        float scale, lo, rcp;
+        bool fast;
+        block_scale<BITS>(x[u], nv[u], scale, lo, rcp, fast);
         uint32_t q[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) q[k] = (k < nv[u] && scale != 0.0f) ? code_of(x[u][k], lo, inv, top) : 0u;
+        for (int k = 0; k < 8; ++k) q[k] = (k < nv[u] && scale != 0.0f) ? code_of(x[u][k], lo, scale, rcp, fast, top) : 0u;
         emit(blk0 + u, (blk0 + u) * kQBlock + static_cast<uint64_t>(lane) * 8, nv[u], q, scale, lo);
     }
 }
