@@ -121,7 +121,9 @@ typedef struct {
 
 typedef struct {
     uint64_t psi, psi_pad, shard, n_ranks, stage;
-    uint64_t model_state_bytes_per_rank;  /* 16/4+12/N/2+14/N/16/N bytes x psi_pad, exact */
+    uint64_t model_state_bytes_per_rank;  /* 16/4+12/N/2+14/N/16/N bytes x psi_pad, exact
+                                             (stage 3 with a resident region: see
+                                             zero_set_persistent) */
     uint64_t comm_elems_paper;            /* 2 psi_pad (stages 0-2), 3 psi_pad (stage 3) */
     uint64_t comm_elems_ring;             /* 2(N-1)/N psi_pad, 3(N-1)/N psi_pad for stage 3 */
     uint64_t hbm_read_bytes, hbm_write_bytes;   /* algorithmic HBM bytes of the last call */
@@ -270,9 +272,9 @@ ZERO_API int zero_reduce_scatter_bucket_replicas(zero_handle_t h, uint64_t a, ui
  * backward reduce-scatter to INT8 or INT4.)
  * Format: blocks of ZERO_Q_BLOCK elements counted from the start of the
  * buffer (or bucket); per block lo = min and hi = max (a NaN makes both NaN),
- * scale = (hi - lo) / (2^bits - 1) and inv = (2^bits - 1) / (hi - lo) in
- * fp32, code = rint((x - lo) * inv) clamped to [0, 2^bits - 1] (0 when
- * scale == 0; 0 for a NaN); dequantized
+ * scale = (hi - lo) / (2^bits - 1) in fp32, code = rint((x - lo) / scale)
+ * with the subtraction and the division each rounded once, clamped to
+ * [0, 2^bits - 1] (0 when scale == 0; 0 for a NaN); dequantized
  * x' = lo + code * scale (fp32 multiply, then add).  Codes: one byte per
  * element (bits = 8) or two per byte with the even element in the low nibble
  * (bits = 4); `scales` holds one {scale, lo} float pair per block.  Code
@@ -329,6 +331,25 @@ ZERO_API int zero_get_status(zero_handle_t h, void* stream, zero_result_t* out);
 ZERO_API int zero_debug_hold_staged(zero_handle_t h, int64_t tile);
 
 /*
+ * zero_set_persistent -- tell a stage-3 handle that the flat region
+ * [p0, psi_pad) stays replicated: every rank keeps a resident 16-bit copy of
+ * it, refreshed by one gather after each update, and its buckets are not
+ * gathered before forward or backward.
+ *   ("ZeRO Stage 1/2/3" guide, ZeRO-3 config: param_persistence_threshold,
+ *    parameters below it stay replicated; ZeRO summary Sec. 5 and Sec. 7 for
+ *    the P_os+g+p memory and communication it changes.)
+ * Host-only bookkeeping: it changes what zero_bytes_moved reports and
+ * nothing that runs on the device (the caller makes the gathers; see the
+ * package's ZeRO-3 schedule).  With psi_pers = psi_pad - p0:
+ *   model_state_bytes_per_rank = 16 psi_pad / N + 2 psi_pers
+ *   comm_elems_paper           = 3 psi_pad - psi_pers
+ *   comm_elems_ring            = floor((N - 1)(3 psi_pad - psi_pers) / N)
+ * p0 = psi_pad (the default) means no resident region.
+ * Errors: EINVAL (NULL handle, stage != 3, p0 > psi_pad).
+ */
+ZERO_API int zero_set_persistent(zero_handle_t h, uint64_t p0);
+
+/*
  * zero_bytes_moved -- D4/D5 accounting and algorithmic HBM bytes.
  *   (ZeRO summary Sec. 5 memory equations and Sec. 7 communication volume;
  *    "zero-stages-simulation" README: byte-accurate memory tracker and a
@@ -342,13 +363,12 @@ ZERO_API int zero_bytes_moved(zero_handle_t h, zero_bytes_t* out);
  * zero_step_noalloc -- the two-pass step of stages 1/2 for callers that
  * cannot allocate device memory.  The ZeRO pages have no counterpart: this
  * is a packaging of zero_step for such callers.
- * Some callers may not call cudaMalloc: code inside a CUDA stream capture
- * (allocation there is an error in the default capture mode), code in a
- * framework whose caching allocator owns the device memory (a foreign
- * cudaMalloc also synchronises the whole device), or code under a memory
- * budget fixed before training starts.  zero_init_partition allocates a
- * workspace, so those callers use this call instead.  It takes no handle
- * and calls no cudaMalloc, cudaFree or other allocating routine.
+ * Some callers may not call cudaMalloc: code in a framework whose caching
+ * allocator owns the device memory (a foreign cudaMalloc also synchronises
+ * the whole device), or code under a memory budget fixed before training
+ * starts.  zero_init_partition allocates a workspace, so those callers use
+ * this call instead.  It takes no handle and calls no cudaMalloc, cudaFree
+ * or other allocating routine.
  *   Its scratch -- the status word, the norm partials, the chunk counters
  *   and the fp32 averaged gradient -- lives in one static device array of
  *   ZERO_NOALLOC_MAX_PSI_PAD floats plus 324,960 bytes (about 16.3 MiB),
@@ -363,8 +383,12 @@ ZERO_API int zero_bytes_moved(zero_handle_t h, zero_bytes_t* out);
  * Arguments are those of zero_init_partition and zero_step (stages 1/2,
  * one state slot, updated in place), plus:
  *   loss_scale, steps_applied  host values of the loss scale and of t
- *           before this step (the caller keeps them between calls)
- *   result  DEVICE pointer (8-byte aligned) receiving the step's
+ *           before this step.  The caller keeps them between calls: it
+ *           passes what the previous call's result reported, so it reads
+ *           that result back (after synchronising the stream) first.
+ *   result  pointer the GPU can write (device, managed or pinned host
+ *           memory; pageable host memory is refused), 8-byte aligned,
+ *           receiving the step's
  *           zero_result_t, stream-ordered: overflow, applied, norm, clip
  *           factor, the loss scale after this step (halved on overflow,
  *           floor 1.0), t after this step, and steps_skipped = 1 if this

@@ -24,7 +24,7 @@ EXPORTS = (
     "zero_bytes_moved", "zero_last_error", "zero_destroy", "zero_step_noalloc",
     "zero_reduce_scatter_bucket_replicas", "zero_quantize_blocks", "zero_dequantize_blocks",
     "zero_gather_bucket_q8", "zero_reduce_scatter_bucket_q", "zero_debug_hold_staged",
-    "zero_noalloc_scratch_bytes",
+    "zero_noalloc_scratch_bytes", "zero_set_persistent",
 )
 ZERO_Q_BLOCK = 256
 
@@ -94,6 +94,7 @@ def load_library():
     lib.zero_get_status.argtypes = [P, P, C.POINTER(Result)]
     lib.zero_debug_hold_staged.argtypes = [P, C.c_int64]
     lib.zero_bytes_moved.argtypes = [P, C.POINTER(Bytes)]
+    lib.zero_set_persistent.argtypes = [P, U64]
     lib.zero_last_error.argtypes = [P]
     lib.zero_last_error.restype = C.c_char_p
     lib.zero_step_noalloc.argtypes = [U64, I32, I32, I32, I32, C.POINTER(P), C.POINTER(P), P, P, P,
@@ -259,6 +260,10 @@ def zero_get_status(h, stream=None) -> dict:
 
 def zero_debug_hold_staged(h, tile: int) -> None:
     _check(load_library().zero_debug_hold_staged(h, int(tile)), h)
+
+
+def zero_set_persistent(h, p0: int) -> None:
+    _check(load_library().zero_set_persistent(h, int(p0)), h)
 
 
 def zero_bytes_moved(h) -> dict:

@@ -49,6 +49,7 @@ struct zero_handle {
     zero_hyper_t rs_hyper{};
     // accounting
     uint64_t last_r = 0, last_w = 0, tot_r = 0, tot_w = 0;
+    uint64_t persist_from = 0;   // stage 3: start of the resident region (psi_pad = none)
     uint64_t hold_tile1 = 0;   // zero_debug_hold_staged, for the next staged step
     uint64_t launch_seq = 0;   // chunked launches: counter slot = launch_seq % kCtrSlots
     std::string err;
@@ -315,6 +316,7 @@ int zero_init_partition(uint64_t psi, int n_ranks, int stage, int dtype, int ali
     h->flags = flags;
     h->psi_pad = (psi + unit - 1) / unit * unit;
     h->shard = h->psi_pad / static_cast<uint64_t>(n_ranks);
+    h->persist_from = h->psi_pad;
     for (int r = 0; r < n_ranks; ++r) {
         const uint64_t off = static_cast<uint64_t>(r) * h->shard;
         h->offsets.push_back(off);
@@ -701,6 +703,14 @@ int zero_debug_hold_staged(zero_handle_t h, int64_t tile) {
     return ZERO_OK;
 }
 
+int zero_set_persistent(zero_handle_t h, uint64_t p0) {
+    if (!h) return fail(nullptr, ZERO_EINVAL, "handle is NULL");
+    if (h->stage != 3) return fail(h, ZERO_EINVAL, "zero_set_persistent is for stage 3");
+    if (p0 > h->psi_pad) return fail(h, ZERO_EINVAL, "p0 must satisfy 0 <= p0 <= psi_pad");
+    h->persist_from = p0;
+    return ZERO_OK;
+}
+
 int zero_bytes_moved(zero_handle_t h, zero_bytes_t* out) {
     if (!h) return fail(nullptr, ZERO_EINVAL, "handle is NULL");
     if (!out) return fail(h, ZERO_EINVAL, "out is NULL");
@@ -710,14 +720,23 @@ int zero_bytes_moved(zero_handle_t h, zero_bytes_t* out) {
     out->shard = h->shard;
     out->n_ranks = N;
     out->stage = static_cast<uint64_t>(h->stage);
+    // the resident region of a stage-3 handle (zero_set_persistent): each
+    // rank keeps its 16-bit copy, which is gathered once per step (after the
+    // update) instead of before forward and before backward
+    const uint64_t pers = P - h->persist_from;
     switch (h->stage) {
         case 0: out->model_state_bytes_per_rank = 16 * P; break;
         case 1: out->model_state_bytes_per_rank = 4 * P + 12 * P / N; break;
         case 2: out->model_state_bytes_per_rank = 2 * P + 14 * P / N; break;
-        default: out->model_state_bytes_per_rank = 16 * P / N; break;
+        default: out->model_state_bytes_per_rank = 16 * P / N + 2 * pers; break;
     }
-    out->comm_elems_paper = (h->stage == 3 ? 3 : 2) * P;
-    out->comm_elems_ring = (h->stage == 3 ? 3 : 2) * (P / N) * (N - 1);
+    if (h->stage == 3) {
+        out->comm_elems_paper = 3 * P - pers;
+        out->comm_elems_ring = (N - 1) * (3 * P - pers) / N;
+    } else {
+        out->comm_elems_paper = 2 * P;
+        out->comm_elems_ring = 2 * (P / N) * (N - 1);
+    }
     out->hbm_read_bytes = h->last_r;
     out->hbm_write_bytes = h->last_w;
     out->hbm_read_total = h->tot_r;

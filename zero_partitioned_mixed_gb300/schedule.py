@@ -60,6 +60,8 @@ class Zero3Schedule:
         for a, b in self.buckets:
             if a < self.p0 < b:
                 raise ValueError("a bucket straddles the persistence boundary")
+        # the handle's accounting counts the resident region's memory and traffic
+        B.zero_set_persistent(buf.h, self.p0)
         self.gathered = [i for i, (a, b) in enumerate(self.buckets) if b <= self.p0 and a < self.p0]
         gset = set(self.gathered)
         self.kept = [i for i in range(len(self.buckets)) if i not in gset]
