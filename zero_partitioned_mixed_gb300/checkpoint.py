@@ -5,6 +5,12 @@ back, or the N replicas at stage 0), the 16-bit parameters, and the
 device-side scaler state (loss scale, applied-step count t).  Resuming
 copies them into slot 0 of fresh buffers and sets the scaler, so the next
 step computes exactly what it would have without the interruption.
+
+What is reproduced is the arithmetic state: master, m, v, the 16-bit
+parameters, the loss scale and t, and with them every later step, bit for
+bit.  The count of skipped (overflowed) steps is a statistic outside that
+state; setting the scaler restarts it at 0, so after a resume it counts the
+skips since the resume only.
 """
 
 from __future__ import annotations

@@ -2,12 +2,11 @@
 // cannot allocate device memory.
 //
 // Who needs it: code that runs where cudaMalloc is not allowed or not
-// wanted -- inside a CUDA stream capture (allocation there is an error in
-// the default capture mode), inside a framework whose caching allocator
-// owns the device memory and must not see a foreign cudaMalloc (which also
-// synchronises the whole device), or under a fixed memory budget decided
-// before training starts.  zero_init_partition allocates a workspace, so
-// such callers cannot use the handle-based entry points.
+// wanted -- inside a framework whose caching allocator owns the device
+// memory and must not see a foreign cudaMalloc (which also synchronises the
+// whole device), or under a fixed memory budget decided before training
+// starts.  zero_init_partition allocates a workspace, so such callers
+// cannot use the handle-based entry points.
 //
 // Instead, every piece of scratch this path needs -- the status word, the
 // norm partials and flags, the chunk counters, and the fp32 averaged gradient of up to
@@ -15,6 +14,10 @@
 // Each GPU that loads the library holds that array until the process exits.
 // The kernels are the library's existing two-pass kernels; only the place
 // their scratch lives differs.
+//
+// The loss scale and the step count t are host arguments: a caller passes
+// the values that the previous call's result reported, so it reads that
+// result back (after synchronising the stream) before the next call.
 
 #include <cstdint>
 #include <cstring>
@@ -127,6 +130,17 @@ extern "C" int zero_step_noalloc(uint64_t psi, int n_ranks, int stage, int dtype
                                      std::to_string(kNoAllocMaxPsiPad) + " elements); use zero_step");
     }
     if (!result || (reinterpret_cast<uintptr_t>(result) & 7u)) return fail(ZERO_EINVAL, "result must be an 8-byte aligned device pointer");
+    {
+        // the result is written by a kernel: refuse memory the GPU cannot
+        // reach (pageable host memory) before anything is launched
+        cudaPointerAttributes pa;
+        const cudaError_t pe = cudaPointerGetAttributes(&pa, result);
+        if (pe != cudaSuccess || (pa.type != cudaMemoryTypeDevice && pa.type != cudaMemoryTypeManaged &&
+                                  pa.type != cudaMemoryTypeHost)) {
+            cudaGetLastError();
+            return fail(ZERO_EINVAL, "result must be device, managed or pinned host memory");
+        }
+    }
 
     zg::Args a;
     std::memset(&a, 0, sizeof(a));
