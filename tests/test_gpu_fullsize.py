@@ -1,10 +1,16 @@
 """Parity at the full sizes of the workloads, in the launch configuration the
-bench times: the 1.5B stage-1 step (with its overflow step), the GPT-2-small
-stage-2 step with clipping, the toy buffer at all four stages, and one
-Llama-7B ZeRO-3 step.  Elements are compared on samples (both ends, every
-shard boundary, the injected index and random positions) against the
-oracle computing them one by one; the global norm and overflow flag of the
-first steps are compared against the oracle over all elements.
+bench times, over every element: the 1.5B stage-1 step (with its overflow
+step), the GPT-2-small stage-2 step with clipping, the toy buffer at all
+four stages, one Llama-7B ZeRO-3 step, and corners of the bandwidth sweep
+(psi = 2^30 at N = 2, 2^29 at N = 4, 2^27 at N = 64).
+
+Each applied step is checked in full: its new fp32 state and every 16-bit
+copy against the oracle's update of the state the step started from (read
+back from the device's other state slot, itself checked by the step
+before), its global norm and overflow flag against the oracle's over all
+elements (tests/_fullsize.py streams the buffers chunk by chunk).  A
+skipped step must leave the state and copies unchanged: their digests are
+compared with those taken after the last applied step.
 """
 
 import numpy as np
@@ -12,8 +18,8 @@ import pytest
 import torch
 
 import oracle as O
-from _fullsize import NormPool, gather_bits16, gather_f32, oracle_sampled_step, sample_indices
-from _parity import NORM_RTOL, ULP16, ULP32, bits16, bits32, run_case, ulp16, ulp32
+from _fullsize import FullCheck
+from _parity import NORM_RTOL, ULP16, ULP32, run_case
 from zero_partitioned_mixed_gb300 import _binding as B
 from zero_partitioned_mixed_gb300 import synth as S
 from zero_partitioned_mixed_gb300.buffers import RankBuffers
@@ -22,8 +28,8 @@ pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
 
 @pytest.fixture(scope="module")
-def pool():
-    p = NormPool()
+def fc():
+    p = FullCheck()
     yield p
     p.close()
 
@@ -33,24 +39,18 @@ def _hyper(w, mode=B.ZERO_MODE_AUTO):
             O.Hyper(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay, w.max_norm))
 
 
-def _check_samples(buf, slot, idx_t, p, m, v, dtype, n, stage):
-    gm, gmm, gv = buf.state(slot)
-    for dev, ref in ((gm, p), (gmm, m), (gv, v)):
-        got = gather_f32(dev, idx_t)
-        assert int(ulp32(got.view(np.uint32), ref.view(np.uint32)).max()) <= ULP32
-        assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
-    want_q = O.rne16(p, dtype)
-    if stage == 3:
-        q = gather_bits16(buf.params, idx_t)
-        assert int(ulp16(q, want_q).max()) <= ULP16 and np.array_equal(q, want_q)
-    else:
-        q = gather_bits16(buf.params, idx_t)    # (N, K)
-        for r in range(n):
-            assert int(ulp16(q[r], want_q).max()) <= ULP16 and np.array_equal(q[r], want_q)
+def _assert_exact(tal, count):
+    assert tal.compared == count, (tal.compared, count)
+    assert tal.max_ulp32 <= ULP32 and tal.max_ulp16 <= ULP16
+    assert tal.mismatches == 0, f"{tal.mismatches} of {tal.compared} elements differ"
+
+
+def _assert_norm(got, want):
+    assert abs(got - want) <= NORM_RTOL * want, (got, want)
 
 
 @pytest.mark.parametrize("mode", [B.ZERO_MODE_AUTO, B.ZERO_MODE_SPECULATIVE_STAGED])
-def test_flat_1p5b_stage1_four_steps_with_overflow(pool, mode):
+def test_flat_1p5b_stage1_four_steps_with_overflow(fc, mode):
     # the bench's workload in both of its launch configurations
     w = S.FLAT15B
     hb, ho = _hyper(w, mode)
@@ -63,44 +63,45 @@ def test_flat_1p5b_stage1_four_steps_with_overflow(pool, mode):
     S.draw_moments(w, mm, vv, w.psi)
     buf.params[:, :P].copy_(mv.to(S.torch_dtype(dt)).unsqueeze(0).expand(n, P))
     grads = torch.empty((n, buf.stride), dtype=S.torch_dtype(dt), device="cuda")
-    inj = S.inject_index(w, w.psi)
-    idx = sample_indices(P, part, 1 << 16, 5, extra=[inj, inj - 1, inj + 1])
-    idx_t = torch.from_numpy(idx).cuda()
-    valid = (idx < w.psi).astype(np.float32)
-    p, m, v = gather_f32(mv, idx_t), gather_f32(mm, idx_t), gather_f32(vv, idx_t)
     buf.set_scaler(w.loss_scale, 0, 0)
-    scale, t = w.loss_scale, 0
+    scale, t, slot, saved = w.loss_scale, 0, 0, None
     for k in range(w.steps):
         for r in range(n):
             S.draw_grads(w, grads[r], w.psi, k + 1, r, scale)
         if k + 1 == w.inject_step:
             S.inject_inf(w, grads[w.inject_rank], w.psi)
-        gs = gather_bits16(grads, idx_t)
-        if k == 0:
-            norm, bad_full = pool.norm_and_flag([grads[r] for r in range(n)], w.psi, part, dt, scale)
         buf.step(hb, [grads[r] for r in range(n)])
         st = buf.status()
-        p2, m2, v2, bad = oracle_sampled_step(p, m, v, gs, n, dt, scale, ho, t + 1, None, valid)
-        assert bool(st["overflow"]) == bad == (k + 1 == w.inject_step)
-        if k == 0:
-            assert not bad_full
-            assert abs(st["grad_norm"] - norm) <= NORM_RTOL * norm
-        if bad:
-            scale = max(scale / 2, 1.0)
-        else:
+        assert bool(st["overflow"]) == (k + 1 == w.inject_step)
+        if not st["overflow"]:
+            tal = fc.compare(0, P, psi=w.psi, part=part, dtype=dt, grads=grads, old=buf.state(slot),
+                             new=buf.state(st["state_slot"]), q=buf.params, loss_scale=scale,
+                             sc=O.step_scalars(ho, t + 1), digest=True)
+            assert not tal.bad
+            _assert_exact(tal, (3 + n) * P)
+            _assert_norm(st["grad_norm"], tal.norm(n))
+            saved = tal.digests
             t += 1
-            p, m, v = p2, m2, v2
+        else:
+            # the oracle's flag over every element; state and replicas untouched
+            tal = fc.compare(0, P, psi=w.psi, part=part, dtype=dt, grads=grads, loss_scale=scale)
+            assert tal.bad
+            assert st["state_slot"] == slot
+            kept = fc.compare(0, P, psi=w.psi, part=part, dtype=dt, new=buf.state(slot), q=buf.params,
+                              digest=True)
+            assert kept.digests == saved
+            scale = max(scale / 2, 1.0)
+        slot = st["state_slot"]
         assert st["steps_applied"] == t and st["loss_scale"] == np.float32(scale)
-        _check_samples(buf, st["state_slot"], idx_t, p, m, v, dt, n, 1)
     buf.close()
     del grads, buf
     torch.cuda.empty_cache()
 
 
 @pytest.mark.parametrize("double_buffer", [False, True])
-def test_gpt2_small_stage2_clip_five_steps(pool, double_buffer):
-    # two-pass (clip decided before the update) and speculative (redo only
-    # if the norm exceeds max_norm, which it does not here)
+def test_gpt2_small_stage2_clip_five_steps(fc, double_buffer):
+    # two-pass (clip decided before the update, state updated in place) and
+    # speculative (redo only if the norm exceeds max_norm, which it does not here)
     w = S.GPT2
     hb, ho = _hyper(w)
     n, dt = w.n_ranks, w.dtype
@@ -113,25 +114,25 @@ def test_gpt2_small_stage2_clip_five_steps(pool, double_buffer):
     buf.params[:, :P].copy_(mv.to(S.torch_dtype(dt)).unsqueeze(0).expand(n, P))
     sv = S.fan_in_scale(S.gpt2_small_shapes(), "cuda")
     grads = torch.empty((n, buf.stride), dtype=S.torch_dtype(dt), device="cuda")
-    idx = sample_indices(P, part, 1 << 16, 6)
-    idx_t = torch.from_numpy(idx).cuda()
-    valid = (idx < w.psi).astype(np.float32)
-    p, m, v = gather_f32(mv, idx_t), gather_f32(mm, idx_t), gather_f32(vv, idx_t)
     buf.set_scaler(1.0, 0, 0)
+    slot = 0
     for k in range(w.steps):
         for r in range(n):
             S.draw_grads(w, grads[r], w.psi, k + 1, r, 1.0, sv)
-        norm, bad_full = pool.norm_and_flag([grads[r] for r in range(n)], w.psi, part, dt, 1.0)
+        pre = fc.compare(0, P, psi=w.psi, part=part, dtype=dt, grads=grads)
+        norm = pre.norm(n)
         clip = O.clip_factor(norm, w.max_norm)
-        gs = gather_bits16(grads, idx_t)
+        old = buf.state(slot) if double_buffer else [x.clone() for x in buf.state(0)]
         buf.step(hb, [grads[r] for r in range(n)])
         st = buf.status()
-        assert not bad_full and not st["overflow"]
-        assert abs(st["grad_norm"] - norm) <= NORM_RTOL * norm
+        assert not pre.bad and not st["overflow"]
+        _assert_norm(st["grad_norm"], norm)
         assert st["clip_coef"] == (float(clip) if clip is not None else 1.0)
-        p, m, v, bad = oracle_sampled_step(p, m, v, gs, n, dt, 1.0, ho, k + 1, clip, valid)
-        assert not bad
-        _check_samples(buf, st["state_slot"], idx_t, p, m, v, dt, n, 2)
+        tal = fc.compare(0, P, psi=w.psi, part=part, dtype=dt, grads=grads, old=old,
+                         new=buf.state(st["state_slot"]), q=buf.params, sc=O.step_scalars(ho, k + 1), clip=clip)
+        _assert_exact(tal, (3 + n) * P)
+        slot = st["state_slot"]
+        del old
     buf.close()
     del grads, sv, buf
     torch.cuda.empty_cache()
@@ -149,38 +150,27 @@ def test_toy_buffer_all_stages_full(stage):
     assert st.mismatches == 0
 
 
-def test_llama7b_zero3_one_step():
-    w = S.LLAMA7B
-    hb, ho = _hyper(w)
+def _zero3_step(fc, w, buf, part, buckets, hb, ho, step, shard0=None):
+    """One ZeRO-3 step over the given buckets (gathers before forward and
+    backward, then each bucket's gradients drawn on the device and
+    reduce-scattered), checked in full.  shard0: a device copy of the
+    16-bit shard before the step, or None to take one."""
     n, dt = w.n_ranks, w.dtype
     td = S.torch_dtype(dt)
-    buf = RankBuffers(w.psi, n, 3, dt, double_buffer=True)
-    P = buf.psi_pad
-    part = O.partition(w.psi, n, 8)
-    buckets = S.layer_buckets(S.llama7b_shapes(), P)
-    assert len(buckets) == 34 and buckets[1][1] - buckets[1][0] == 202_383_360
-    mv, mm, vv = buf.state(0)
-    S.draw_master(w, mv, w.psi)
-    S.draw_moments(w, mm, vv, w.psi)
-    buf.params[:P].copy_(mv.to(td))
-    idx = sample_indices(P, part, 1 << 16, 7, extra=[a for a, _ in buckets] + [b - 1 for _, b in buckets])
-    idx_t = torch.from_numpy(idx).cuda()
-    shard0 = gather_bits16(buf.params, idx_t)
-    p, m, v = gather_f32(mv, idx_t), gather_f32(mm, idx_t), gather_f32(vv, idx_t)
     lmax = max(b - a for a, b in buckets)
     lpad = (lmax + 7) // 8 * 8
     outs = torch.empty((n, lpad), dtype=td, device="cuda")
     gbuf = torch.empty((n, lpad), dtype=td, device="cuda")
-    gs = np.zeros((n, idx.size), np.uint16)
-    buf.set_scaler(1.0, 0, 0)
+    if shard0 is None:
+        shard0 = buf.params.clone()
 
     def check_gather(a, b):
-        sel = (idx >= a) & (idx < b)
-        loc = torch.from_numpy(idx[sel] - a).cuda()
-        got = gather_bits16(outs, loc)
+        # the gather is a copy of the owners' values: every rank's row equals the shard
         for r in range(n):
-            assert np.array_equal(got[r], shard0[sel])
+            assert torch.equal(outs[r, :b - a], shard0[a:b])
 
+    st0 = buf.status()
+    slot = st0["state_slot"]
     for (a, b) in buckets:                       # forward
         buf.gather(a, b, [outs[r] for r in range(n)])
         check_gather(a, b)
@@ -189,18 +179,86 @@ def test_llama7b_zero3_one_step():
         buf.gather(a, b, [outs[r] for r in range(n)])
         check_gather(a, b)
         for r in range(n):
-            S.draw_grads(w, gbuf[r], w.psi, 1, r, 1.0, offset=a)
-        sel = np.nonzero((idx >= a) & (idx < b))[0]
-        loc = torch.from_numpy(idx[sel] - a).cuda()
-        gs[:, sel] = gather_bits16(gbuf, loc)
+            S.draw_grads(w, gbuf[r], w.psi, step, r, 1.0, offset=a)
         buf.reduce_scatter(a, b, [gbuf[r] for r in range(n)], hb)
     buf.step(hb)
     st = buf.status()
-    valid = (idx < w.psi).astype(np.float32)
-    p2, m2, v2, bad = oracle_sampled_step(p, m, v, gs, n, dt, 1.0, ho, 1, None, valid)
-    assert not bad and not st["overflow"] and st["applied"] and st["steps_applied"] == 1
-    assert st["grad_norm"] > 0
-    _check_samples(buf, st["state_slot"], idx_t, p2, m2, v2, dt, n, 3)
+    assert not st["overflow"] and st["applied"] and st["steps_applied"] == st0["steps_applied"] + 1
+    # the same gradients again (same generator, offset and buffer length), bucket by bucket
+    tal = None
+    for (a, b) in buckets:
+        for r in range(n):
+            S.draw_grads(w, gbuf[r], w.psi, step, r, 1.0, offset=a)
+        tal = fc.compare(a, b, psi=w.psi, part=part, dtype=dt, grads=gbuf, g_base=a, old=buf.state(slot),
+                         new=buf.state(st["state_slot"]), q=buf.params, loss_scale=1.0,
+                         sc=O.step_scalars(ho, st0["steps_applied"] + 1), tally=tal)
+    assert not tal.bad
+    _assert_exact(tal, 4 * part.psi_pad)
+    _assert_norm(st["grad_norm"], tal.norm(n))
+    del outs, gbuf, shard0
+
+
+def test_llama7b_zero3_one_step(fc):
+    w = S.LLAMA7B
+    hb, ho = _hyper(w)
+    n, dt = w.n_ranks, w.dtype
+    buf = RankBuffers(w.psi, n, 3, dt, double_buffer=True)
+    P = buf.psi_pad
+    part = O.partition(w.psi, n, 8)
+    buckets = S.layer_buckets(S.llama7b_shapes(), P)
+    assert len(buckets) == 34 and buckets[1][1] - buckets[1][0] == 202_383_360
+    mv, mm, vv = buf.state(0)
+    S.draw_master(w, mv, w.psi)
+    S.draw_moments(w, mm, vv, w.psi)
+    buf.params[:P].copy_(mv.to(S.torch_dtype(dt)))
+    buf.set_scaler(1.0, 0, 0)
+    _zero3_step(fc, w, buf, part, buckets, hb, ho, 1)
     buf.close()
-    del outs, gbuf, buf
+    del buf
+    torch.cuda.empty_cache()
+
+
+# corners of the bandwidth sweep: the longest chunks of the one-pass step
+# (psi = 2^30, N = 2), the reduce-scatter's chunk cap for N <= 4, and the
+# widest rank loops (N = 64); bf16 N(0, 1e-3^2), Adam defaults, 2 steps
+SWEEP_CORNERS = [(1 << 30, 2, 1), (1 << 30, 2, 3), (1 << 29, 4, 3), (1 << 27, 64, 1), (1 << 27, 64, 3)]
+
+
+@pytest.mark.parametrize("psi,n,stage", SWEEP_CORNERS)
+def test_sweep_corner(fc, psi, n, stage):
+    w = S.Workload(f"sweep_psi{psi}_n{n}", psi, n, stage, "bf16", 2, grad_sigma=1e-3)
+    hb, ho = _hyper(w)
+    dt = w.dtype
+    td = S.torch_dtype(dt)
+    buf = RankBuffers(psi, n, stage, dt, double_buffer=True, alloc_grads=False)
+    P = buf.psi_pad
+    part = O.partition(psi, n, 8)
+    mv, mm, vv = buf.state(0)
+    S.draw_master(w, mv, psi)
+    S.draw_moments(w, mm, vv, psi)
+    buf.set_scaler(1.0, 0, 0)
+    if stage == 3:
+        buf.params[:P].copy_(mv.to(td))
+        buckets = S.flat_buckets(P, n, 50_000_000)
+        for k in range(w.steps):
+            _zero3_step(fc, w, buf, part, buckets, hb, ho, k + 1)
+    else:
+        buf.params[:, :P].copy_(mv.to(td).unsqueeze(0).expand(n, P))
+        grads = torch.empty((n, buf.stride), dtype=td, device="cuda")
+        slot = 0
+        for k in range(w.steps):
+            for r in range(n):
+                S.draw_grads(w, grads[r], psi, k + 1, r, 1.0)
+            buf.step(hb, [grads[r] for r in range(n)])
+            st = buf.status()
+            assert not st["overflow"] and st["steps_applied"] == k + 1
+            tal = fc.compare(0, P, psi=psi, part=part, dtype=dt, grads=grads, old=buf.state(slot),
+                             new=buf.state(st["state_slot"]), q=buf.params, sc=O.step_scalars(ho, k + 1))
+            assert not tal.bad
+            _assert_exact(tal, (3 + n) * P)
+            _assert_norm(st["grad_norm"], tal.norm(n))
+            slot = st["state_slot"]
+        del grads
+    buf.close()
+    del buf
     torch.cuda.empty_cache()
