@@ -2,8 +2,8 @@
 
 The step is elementwise apart from the global norm and the overflow flag.
 A full-size step is therefore checked chunk by chunk: the main thread copies
-one chunk of the device buffers to host memory (the N gradient rows, the
-fp32 state before and after the step, the 16-bit copies), and a pool of
+one chunk of the device buffers to pinned host memory (the N gradient rows,
+the fp32 state before and after the step, the 16-bit copies), and a pool of
 threads runs the oracle on it (numpy drops the GIL in its array loops).
 Every element is compared bit for bit.  Each chunk also returns its sums
 of squares per owner shard (left to right, fp64); the global norm adds them
@@ -135,30 +135,31 @@ def _check_chunk(start: int, psi: int, shard: int, n: int, dtype: str, gbits: Op
     return out
 
 
-def _host16(t, lo: int, hi: int) -> np.ndarray:
-    """Columns [lo, hi) of a (R, cols) or (cols,) 16-bit device tensor as (R, hi - lo) uint16."""
-    import torch
-    rows = t.unsqueeze(0) if t.dim() == 1 else t
-    host = torch.empty((rows.shape[0], hi - lo), dtype=torch.int16)
-    for r in range(rows.shape[0]):
-        host[r].copy_(rows[r, lo:hi].view(torch.int16))
-    return host.numpy().view(np.uint16)
-
-
-def _host32(t, lo: int, hi: int) -> np.ndarray:
-    return t[lo:hi].cpu().numpy()
-
-
 class FullCheck:
-    """Streams device buffers to host chunk by chunk and runs the oracle on them in threads."""
+    """Streams device buffers to host chunk by chunk and runs the oracle on them in threads.
 
-    def __init__(self, workers: Optional[int] = None, chunk: int = CHUNK):
+    The chunks land in a ring of pinned host slots (async copies on a side
+    stream, one event per chunk that its worker waits on); a slot is reused
+    once the worker that read it has finished.
+    """
+
+    def __init__(self, workers: Optional[int] = None, slot_bytes: int = 1 << 29, max_chunk: int = CHUNK):
         self.workers = workers or max(1, min(16, (os.cpu_count() or 2)))
         self.pool = ThreadPoolExecutor(self.workers)
-        self.chunk = chunk
+        self.slot_bytes = slot_bytes
+        self.max_chunk = max_chunk
+        self.slots = [None] * (2 * self.workers)
+        self.stream = None
 
     def close(self):
         self.pool.shutdown(wait=True)
+        self.slots = []
+
+    def _slot(self, i: int):
+        import torch
+        if self.slots[i] is None:
+            self.slots[i] = torch.empty(self.slot_bytes, dtype=torch.uint8, pin_memory=True)
+        return self.slots[i]
 
     def compare(self, a: int, b: int, *, psi: int, part: O.Partition, dtype: str,
                 grads=None, g_base: int = 0, old=None, new=None, q=None, q_base: int = 0,
@@ -173,19 +174,68 @@ class FullCheck:
         replicas or the (cols,) stage-3 shard, flat element i at column
         i - q_base.  sc: the step's Adam scalars when the step applied.
         """
+        import torch
         tally = tally or Tally()
-        pending = deque()
         n = part.n_ranks
-        for s in range(a, b, self.chunk):
-            e = min(b, s + self.chunk)
-            gb = _host16(grads, s - g_base, e - g_base) if grads is not None else None
-            o3 = [_host32(x, s, e) for x in old] if old is not None else None
-            n3 = [_host32(x, s, e) for x in new] if new is not None else None
-            qh = _host16(q, s - q_base, e - q_base) if q is not None else None
-            pending.append(self.pool.submit(_check_chunk, s, psi, part.shard, n, dtype, gb, o3, n3, qh,
-                                            loss_scale, sc, clip, digest))
-            while len(pending) >= 2 * self.workers:
+        qrows = None if q is None else (q.unsqueeze(0) if q.dim() == 1 else q)
+        ng = grads.shape[0] if grads is not None else 0
+        nq = qrows.shape[0] if qrows is not None else 0
+        per_elem = 2 * ng + 4 * 3 * ((old is not None) + (new is not None)) + 2 * nq
+        chunk = self.max_chunk
+        while chunk > 1024 and chunk * per_elem + 16 * 256 > self.slot_bytes:
+            chunk //= 2
+        if self.stream is None:
+            self.stream = torch.cuda.Stream()
+        self.stream.wait_stream(torch.cuda.current_stream())
+        pending = deque()
+        k = 0
+        for s in range(a, b, chunk):
+            e = min(b, s + chunk)
+            L = e - s
+            if len(pending) == len(self.slots):
                 tally.merge(pending.popleft().result())
+            buf = self._slot(k % len(self.slots))
+            k += 1
+            off = 0
+
+            def take(nbytes):
+                nonlocal off
+                v = buf[off:off + nbytes]
+                off += (nbytes + 255) // 256 * 256
+                return v
+
+            with torch.cuda.stream(self.stream):
+                gb = o3 = n3 = qh = None
+                if grads is not None:
+                    t = take(2 * ng * L).view(torch.int16).view(ng, L)
+                    for r in range(ng):
+                        t[r].copy_(grads[r, s - g_base:e - g_base].view(torch.int16), non_blocking=True)
+                    gb = t.numpy().view(np.uint16)
+                if old is not None:
+                    o3 = []
+                    for x in old:
+                        t = take(4 * L).view(torch.float32)
+                        t.copy_(x[s:e], non_blocking=True)
+                        o3.append(t.numpy())
+                if new is not None:
+                    n3 = []
+                    for x in new:
+                        t = take(4 * L).view(torch.float32)
+                        t.copy_(x[s:e], non_blocking=True)
+                        n3.append(t.numpy())
+                if qrows is not None:
+                    t = take(2 * nq * L).view(torch.int16).view(nq, L)
+                    for r in range(nq):
+                        t[r].copy_(qrows[r, s - q_base:e - q_base].view(torch.int16), non_blocking=True)
+                    qh = t.numpy().view(np.uint16)
+                ev = torch.cuda.Event()
+                ev.record(self.stream)
+
+            def job(ev=ev, s=s, gb=gb, o3=o3, n3=n3, qh=qh):
+                ev.synchronize()
+                return _check_chunk(s, psi, part.shard, n, dtype, gb, o3, n3, qh, loss_scale, sc, clip, digest)
+
+            pending.append(self.pool.submit(job))
         while pending:
             tally.merge(pending.popleft().result())
         return tally
