@@ -599,10 +599,12 @@ def bench_dense(w, stage, steps, warmup, torch, S, Z, flush_l2=False, sets_max=5
     return ms, per_step, st
 
 
-def bench_stage3(w, buckets, steps, warmup, torch, S, Z, flush_l2=False):
+def bench_stage3(w, buckets, steps, warmup, torch, S, Z, flush_l2=False, fused=True):
     """ZeRO-3: per step, gather every bucket (forward), then per bucket in reverse
     gather again and reduce-scatter, then finish the step.  One drawn gradient
-    buffer of the largest bucket is reused for every bucket (timing only)."""
+    buffer of the largest bucket is reused for every bucket (timing only).
+    fused: in backward each reduce-scatter carries the next bucket's gather
+    (zero_reduce_scatter_gather_bucket), into two alternating output sets."""
     from zero_partitioned_mixed_gb300.buffers import RankBuffers
     buf = RankBuffers(w.psi, w.n_ranks, 3, w.dtype, double_buffer=(w.max_norm == 0))
     P, N = buf.psi_pad, w.n_ranks
@@ -616,27 +618,41 @@ def bench_stage3(w, buckets, steps, warmup, torch, S, Z, flush_l2=False):
     gbuf = torch.empty((N, lpad), dtype=td, device="cuda")
     for r in range(N):
         S.draw_grads(w, gbuf[r], lmax, 1, r, w.loss_scale)
-    outs = torch.empty((N, lpad), dtype=td, device="cuda")
+    outs = torch.empty((2 if fused else 1, N, lpad), dtype=td, device="cuda")
     buf.set_scaler(w.loss_scale, 0, 0)
     hyp = Z.hyper(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay, w.max_norm,
                   Z.ZERO_MODE_AUTO)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda") if flush_l2 else None
     grows = Z.pointer_array([gbuf[r] for r in range(N)])
-    orows = Z.pointer_array([outs[r] for r in range(N)])
+    orows = [Z.pointer_array([o[r] for r in range(N)]) for o in outs]
+    back = list(reversed(buckets))
 
     def one_step(tg, tr, tf):
         for (a, b) in buckets:
             if flush is not None:
                 flush.zero_()
             with tg:
-                buf.gather(a, b, orows)
-        for (a, b) in reversed(buckets):
-            if flush is not None:
-                flush.zero_()
+                buf.gather(a, b, orows[0])
+        if fused:
             with tg:
-                buf.gather(a, b, orows)
-            with tr:
-                buf.reduce_scatter(a, b, grows, hyp)
+                buf.gather(back[0][0], back[0][1], orows[0])
+            for k, (a, b) in enumerate(back):
+                if flush is not None:
+                    flush.zero_()
+                with tr:
+                    if k + 1 < len(back):
+                        buf.reduce_scatter_gather(a, b, grows, hyp, back[k + 1][0], back[k + 1][1],
+                                                  orows[(k + 1) % 2])
+                    else:
+                        buf.reduce_scatter(a, b, grows, hyp)
+        else:
+            for (a, b) in back:
+                if flush is not None:
+                    flush.zero_()
+                with tg:
+                    buf.gather(a, b, orows[0])
+                with tr:
+                    buf.reduce_scatter(a, b, grows, hyp)
         with tf:
             buf.step(hyp)
 
@@ -650,6 +666,8 @@ def bench_stage3(w, buckets, steps, warmup, torch, S, Z, flush_l2=False):
             one_step(tg, tr, tf)
     parts = {"gather_ms": tg.total_ms() / steps, "reduce_scatter_ms": tr.total_ms() / steps,
              "finish_ms": tf.total_ms() / steps}
+    if fused:
+        parts["reduce_scatter_ms_note"] = "backward reduce-scatters with the next bucket's gather fused in"
     ms = _step_ms(parts, wall, steps, flush is not None)
     bench_stage3.parts = parts
     per_step = _bytes_delta(buf, before) / steps
@@ -771,10 +789,11 @@ def bench_stage3_zeropp(w, buckets, steps, warmup, torch, S, Z, bits):
     return ms, per_step, st, quant_ms, lmax, parts
 
 
-def bench_schedule(w, buckets, steps, warmup, torch, S, Z, prefetch, graph):
+def bench_schedule(w, buckets, steps, warmup, torch, S, Z, prefetch, graph, fuse=True):
     """Whole ZeRO-3 steps through Zero3Schedule (gathers one bucket ahead on a
-    side stream when `prefetch`; the step replayed from a CUDA graph when
-    `graph`), timed with events on the main stream around each step."""
+    side stream when `prefetch`; backward gathers carried by the reduce-scatters
+    when `fuse`; the step replayed from a CUDA graph when `graph`), timed with
+    events on the main stream around each step."""
     from zero_partitioned_mixed_gb300.buffers import RankBuffers
     from zero_partitioned_mixed_gb300.schedule import Zero3Schedule
     buf = RankBuffers(w.psi, w.n_ranks, 3, w.dtype, double_buffer=True)
@@ -791,7 +810,7 @@ def bench_schedule(w, buckets, steps, warmup, torch, S, Z, prefetch, graph):
     rows = Z.pointer_array([gbuf[r] for r in range(N)])
     buf.set_scaler(w.loss_scale, 0, 0)
     hyp = Z.hyper(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay, w.max_norm, Z.ZERO_MODE_AUTO)
-    sched = Zero3Schedule(buf, buckets, prefetch=prefetch)
+    sched = Zero3Schedule(buf, buckets, prefetch=prefetch, fuse=fuse)
     grads = lambda i: rows
     for _ in range(warmup):
         sched.step(hyp, grads)
@@ -916,9 +935,14 @@ def run_other(args, ws, rank, local):
         w = S.Workload(f"flat_psi{psi}_n{n}_stage3_bf16", psi, n, 3, "bf16", 1, grad_sigma=1e-3)
         pp = ((psi + n * 8 - 1) // (n * 8)) * (n * 8)
         buckets = S.flat_buckets(pp, n, args.bucket or max(64, psi // 4))
-        if args.workload == "flat-zero3":
-            ms, bps, st = bench_stage3(w, buckets, args.steps, args.warmup, torch, S, Z)
-            parts = bench_stage3.parts
+        if args.workload == "flat-zero3" and args.prefetch:
+            # whole steps through Zero3Schedule: each gather one bucket ahead on a side stream
+            ms = bench_schedule(w, buckets, args.steps, args.warmup, torch, S, Z, True, False)
+            bps = (6 * n + 30) * pp
+            parts = {"schedule": "Zero3Schedule, gathers one bucket ahead on a side stream"}
+        elif args.workload == "flat-zero3":
+            ms, bps, st = bench_stage3(w, buckets, args.steps, args.warmup, torch, S, Z, fused=not args.separate)
+            parts = dict(bench_stage3.parts, fused=not args.separate)
         else:
             ms, bps, st, _, _, parts = bench_stage3_zeropp(w, buckets, args.steps, args.warmup, torch, S, Z,
                                                            args.rs_bits)
@@ -932,11 +956,12 @@ def run_other(args, ws, rank, local):
         # stream (Llama-7B), and eager vs CUDA-graph replay (toy buffer, launch-bound)
         w = S.LLAMA7B
         buckets = S.layer_buckets(S.llama7b_shapes(), w.psi)
-        for prefetch in (False, True):
-            ms = bench_schedule(w, buckets, args.steps, args.warmup, torch, S, Z, prefetch, False)
-            lines.append(_line(f"{w.name}_{'prefetch' if prefetch else 'sequential'}", w.psi / (ms * 1e-3), ms,
-                               args.steps, args.warmup, (6 * 8 + 30) * w.psi, w.dtype,
-                               {"stage": 3, "buckets": len(buckets), "prefetch": prefetch}))
+        for prefetch, fuse in ((False, False), (True, False), (False, True), (True, True)):
+            ms = bench_schedule(w, buckets, args.steps, args.warmup, torch, S, Z, prefetch, False, fuse)
+            lines.append(_line(f"{w.name}_{'prefetch' if prefetch else 'sequential'}{'_fused' if fuse else ''}",
+                               w.psi / (ms * 1e-3), ms, args.steps, args.warmup, (6 * 8 + 30) * w.psi, w.dtype,
+                               {"stage": 3, "buckets": len(buckets), "prefetch": prefetch,
+                                "fused_backward_gathers": fuse}))
         toy = dataclasses.replace(S.TOY, stage=3)
         tb = S.flat_buckets(637_952, 32, 50_000)
         for graph in (False, True):
@@ -975,10 +1000,11 @@ def run_other(args, ws, rank, local):
     elif args.workload == "llama7b":
         w = S.LLAMA7B
         buckets = S.layer_buckets(S.llama7b_shapes(), w.psi)
-        ms, bps, st = bench_stage3(w, buckets, args.steps, args.warmup, torch, S, Z)
+        ms, bps, st = bench_stage3(w, buckets, args.steps, args.warmup, torch, S, Z, fused=not args.separate)
         lines.append(_line(w.name, w.psi / (ms * 1e-3), ms, args.steps, args.warmup, bps, w.dtype,
                            {"stage": 3, "buckets": len(buckets), "mode": "speculative, fused per bucket",
-                            "l2": "inputs larger than L2", **bench_stage3.parts}))
+                            "l2": "inputs larger than L2", "fused_backward_gathers": not args.separate,
+                            **bench_stage3.parts}))
     elif args.workload == "sweep":
         stages = [int(x) for x in args.stages.split(",")]
         for psi, n in S.sweep_points():
@@ -990,7 +1016,7 @@ def run_other(args, ws, rank, local):
                 if stage == 3:
                     pp = ((psi + n * 8 - 1) // (n * 8)) * (n * 8)
                     ms, bps, st = bench_stage3(w, S.flat_buckets(pp, n, 50_000_000), args.steps, args.warmup,
-                                               torch, S, Z, flush_l2=flush)
+                                               torch, S, Z, flush_l2=flush, fused=not args.separate)
                 else:
                     ms, bps, st = bench_dense(w, stage, args.steps, args.warmup, torch, S, Z, flush_l2=flush,
                                               sets_max=1)
@@ -1028,6 +1054,11 @@ def main(argv=None):
     ap.add_argument("--bucket", type=int, default=None,
                     help="flat-zero3 / flat-zeropp: elements per bucket (default psi / 4)")
     ap.add_argument("--stages", default="1,2,3", help="sweep: stages to run")
+    ap.add_argument("--prefetch", action="store_true",
+                    help="flat-zero3: run whole steps through the ZeRO-3 schedule with side-stream prefetch")
+    ap.add_argument("--separate", action="store_true",
+                    help="stage-3 workloads (flat-zero3, llama7b, sweep): backward gathers as calls of their own "
+                         "(default: each backward reduce-scatter carries the next bucket's gather)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

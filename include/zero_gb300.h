@@ -242,6 +242,32 @@ ZERO_API int zero_reduce_scatter_bucket(zero_handle_t h, uint64_t a, uint64_t b,
                                void* shard16, const zero_hyper_t* hyper, void* stream);
 
 /*
+ * zero_reduce_scatter_gather_bucket -- zero_reduce_scatter_bucket of bucket
+ * [a, b) and zero_gather_bucket of bucket [ga, gb) in one call: the
+ * reduce-scatter of one layer's gradients in backward together with the
+ * gather of the next layer's parameters, fetched one layer ahead.
+ *   (ZeRO summary Sec. 5, P_os+g+p: in backward the parameters are gathered
+ *    again in reverse order, a layer's gradients are reduce-scattered as they
+ *    appear, and the next layer can be fetched while the current one is
+ *    processed; "ZeRO Stage 1/2/3" guide, ZeRO-3 config: prefetch_bucket_size.)
+ * The result is that of the two calls one after the other.  When both parts
+ * are 8-wide (a, b - a, ga and gb - ga multiples of 8) they run as one launch
+ * whose work counter hands out the reduce-scatter's chunks first and then
+ * the gather's, so that the gather fills the end of the reduce-scatter;
+ * otherwise the two calls are made in turn.  Either part may be empty.
+ *   The two buckets must not overlap, and no out[r] may share memory with
+ *   the 16-bit shard or with a gradient row of [a, b) (ZERO_EINVAL).
+ *   Arguments: those of zero_reduce_scatter_bucket, then ga, gb and out
+ *   (host array of N device pointers, gb - ga elements each) as for
+ *   zero_gather_bucket.  zero_bytes_moved counts both parts as this call.
+ * Stage 3 only.  Errors: EINVAL, ESTATE, ECUDA, ENOMEM.
+ */
+ZERO_API int zero_reduce_scatter_gather_bucket(zero_handle_t h, uint64_t a, uint64_t b,
+                                               const void* const* grads, float* master, float* m, float* v,
+                                               void* shard16, const zero_hyper_t* hyper, uint64_t ga,
+                                               uint64_t gb, void* const* out, void* stream);
+
+/*
  * zero_reduce_scatter_bucket_replicas -- ZeRO-2 with the gradients reduced
  * during backward: the reduce-scatter of bucket [a, b) as its gradients
  * appear, after which the ranks may release or reuse their gradient

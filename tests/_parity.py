@@ -89,12 +89,14 @@ def _draw(shape, sigma, seed, dtype=torch.float32, absolute=False):
 def run_case(psi: int, n: int, stage: int, dtype: str = "bf16", steps: int = 2, align: int = 8,
              mode: int = 0, double_buffer: bool = True, loss_scale: float = 1.0, hyper_kw=None,
              buckets: Optional[Sequence[Tuple[int, int]]] = None, inject=None, sigma: float = 1e-2,
-             seed: int = 0, warm: bool = True, hyper_steps=None) -> Stats:
+             seed: int = 0, warm: bool = True, hyper_steps=None, fused: bool = False) -> Stats:
     """Run `steps` steps on the GPU and in the oracle; compare after each step.
 
     inject: list of (step, rank, index, value) written into the gradients.
     hyper_steps: per step, hyper-parameter overrides on top of hyper_kw (a
     schedule: learning rate, weight decay, ... changing between steps).
+    fused: stage 3, backward through zero_reduce_scatter_gather_bucket (each
+    bucket's reduce-scatter carries the next bucket's gather).
     """
     hyper_kw = dict(hyper_kw or {})
     hb, ho = hyper_pair(mode=mode, **hyper_kw)
@@ -146,16 +148,34 @@ def run_case(psi: int, n: int, stage: int, dtype: str = "bf16", steps: int = 2, 
                 outs = [torch.zeros((max(8, (L + 7) // 8 * 8),), dtype=td, device="cuda") for _ in range(n)]
                 buf.gather(a, b, outs)
                 res_gather_fwd.append([bits16(o[:L]) for o in outs])
-            for idx in range(len(buckets) - 1, -1, -1):
+            order = list(range(len(buckets) - 1, -1, -1))
+
+            def new_outs(i):
+                L = buckets[i][1] - buckets[i][0]
+                return [torch.zeros((max(8, (L + 7) // 8 * 8),), dtype=td, device="cuda") for _ in range(n)]
+
+            bwd = {}
+            if fused and order:
+                bwd[order[0]] = new_outs(order[0])
+                buf.gather(buckets[order[0]][0], buckets[order[0]][1], bwd[order[0]])
+            for k, idx in enumerate(order):
                 a, b = buckets[idx]
                 L = b - a
-                outs = [torch.zeros((max(8, (L + 7) // 8 * 8),), dtype=td, device="cuda") for _ in range(n)]
-                buf.gather(a, b, outs)
-                res_gather_bwd.insert(0, [bits16(o[:L]) for o in outs])
+                if not fused:
+                    bwd[idx] = new_outs(idx)
+                    buf.gather(a, b, bwd[idx])
                 gb = [torch.zeros((max(8, (L + 7) // 8 * 8),), dtype=td, device="cuda") for _ in range(n)]
                 for r in range(n):
                     gb[r][:L].copy_(grads[r, a:b])
-                buf.reduce_scatter(a, b, gb, hb)
+                if fused and k + 1 < len(order):
+                    nxt = order[k + 1]
+                    bwd[nxt] = new_outs(nxt)
+                    buf.reduce_scatter_gather(a, b, gb, hb, buckets[nxt][0], buckets[nxt][1], bwd[nxt])
+                else:
+                    buf.reduce_scatter(a, b, gb, hb)
+            for idx in range(len(buckets)):
+                L = buckets[idx][1] - buckets[idx][0]
+                res_gather_bwd.append([bits16(o[:L]) for o in bwd[idx]])
             buf.step(hb)
             ost, ores = O.step_stage3(ost, [gbits[:, a:b] for (a, b) in buckets], buckets, ho)
             for bi in range(len(buckets)):

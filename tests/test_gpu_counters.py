@@ -247,3 +247,32 @@ def test_hbm_bytes_zeropp(bits):
     buf.step(B.hyper())
     c.expect(0, 0)
     buf.close()
+
+
+@pytest.mark.parametrize("spec", [True, False])
+def test_hbm_bytes_fused_reduce_scatter_gather(spec):
+    # one call: the reduce-scatter of one bucket and the gather of another,
+    # counted as the two parts' bytes together (one launch when 8-aligned,
+    # two calls otherwise)
+    buf = RankBuffers(PSI, N, 3, "bf16", double_buffer=spec)
+    P = buf.psi_pad
+    c = Calls(buf)
+    hyp = B.hyper()
+    grads = [torch.zeros(P + 8, dtype=torch.bfloat16, device="cuda") for _ in range(N)]
+    outs = [torch.zeros(P + 8, dtype=torch.bfloat16, device="cuda") for _ in range(N)]
+
+    def rs_bytes(L):
+        if spec:
+            return _nbytes(N, L, 2) + _nbytes(3, L, 4), _nbytes(3, L, 4) + _nbytes(1, L, 2)
+        return _nbytes(N, L, 2), _nbytes(1, L, 4)
+
+    for (a, b), (ga, gb) in (((12_000, P), (8_000, 12_000)), ((8_001, 12_000), (0, 8_001)), ((0, 8_001), (0, 0))):
+        buf.reduce_scatter_gather(a, b, grads, hyp, ga, gb, outs)
+        r, w = rs_bytes(b - a)
+        c.expect(r + _nbytes(1, gb - ga, 2), w + _nbytes(N, gb - ga, 2))
+    buf.step(hyp)
+    if spec:
+        c.expect(0, 0)
+    else:
+        c.expect(_nbytes(1, P, 4) + _nbytes(3, P, 4), _nbytes(3, P, 4) + _nbytes(1, P, 2))
+    buf.close()

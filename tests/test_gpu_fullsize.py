@@ -150,45 +150,59 @@ def test_toy_buffer_all_stages_full(stage):
     assert st.mismatches == 0
 
 
-def _zero3_step(fc, w, buf, part, buckets, hb, ho, step, shard0=None):
+def _zero3_step(fc, w, buf, part, buckets, hb, ho, step, fused=True):
     """One ZeRO-3 step over the given buckets (gathers before forward and
-    backward, then each bucket's gradients drawn on the device and
-    reduce-scattered), checked in full.  shard0: a device copy of the
-    16-bit shard before the step, or None to take one."""
+    backward, each bucket's gradients drawn on the device and
+    reduce-scattered; with `fused` each backward reduce-scatter carries the
+    next bucket's gather, as the bench times it), checked in full."""
     n, dt = w.n_ranks, w.dtype
     td = S.torch_dtype(dt)
     lmax = max(b - a for a, b in buckets)
     lpad = (lmax + 7) // 8 * 8
-    outs = torch.empty((n, lpad), dtype=td, device="cuda")
+    outs = torch.empty((2, n, lpad), dtype=td, device="cuda")
     gbuf = torch.empty((n, lpad), dtype=td, device="cuda")
-    if shard0 is None:
-        shard0 = buf.params.clone()
+    shard0 = buf.params.clone()
 
-    def check_gather(a, b):
+    def check_gather(a, b, o):
         # the gather is a copy of the owners' values: every rank's row equals the shard
         for r in range(n):
-            assert torch.equal(outs[r, :b - a], shard0[a:b])
+            assert torch.equal(o[r, :b - a], shard0[a:b])
+
+    def draw(a):
+        for r in range(n):
+            S.draw_grads(w, gbuf[r], w.psi, step, r, 1.0, offset=a)
 
     st0 = buf.status()
     slot = st0["state_slot"]
     for (a, b) in buckets:                       # forward
-        buf.gather(a, b, [outs[r] for r in range(n)])
-        check_gather(a, b)
-    for bi in range(len(buckets) - 1, -1, -1):   # backward
-        a, b = buckets[bi]
-        buf.gather(a, b, [outs[r] for r in range(n)])
-        check_gather(a, b)
-        for r in range(n):
-            S.draw_grads(w, gbuf[r], w.psi, step, r, 1.0, offset=a)
-        buf.reduce_scatter(a, b, [gbuf[r] for r in range(n)], hb)
+        buf.gather(a, b, [outs[0, r] for r in range(n)])
+        check_gather(a, b, outs[0])
+    back = list(reversed(buckets))               # backward
+    if fused:
+        buf.gather(back[0][0], back[0][1], [outs[0, r] for r in range(n)])
+        check_gather(back[0][0], back[0][1], outs[0])
+        for k, (a, b) in enumerate(back):
+            draw(a)
+            if k + 1 < len(back):
+                ga, gb = back[k + 1]
+                o = outs[(k + 1) % 2]
+                buf.reduce_scatter_gather(a, b, [gbuf[r] for r in range(n)], hb, ga, gb, [o[r] for r in range(n)])
+                check_gather(ga, gb, o)
+            else:
+                buf.reduce_scatter(a, b, [gbuf[r] for r in range(n)], hb)
+    else:
+        for (a, b) in back:
+            buf.gather(a, b, [outs[0, r] for r in range(n)])
+            check_gather(a, b, outs[0])
+            draw(a)
+            buf.reduce_scatter(a, b, [gbuf[r] for r in range(n)], hb)
     buf.step(hb)
     st = buf.status()
     assert not st["overflow"] and st["applied"] and st["steps_applied"] == st0["steps_applied"] + 1
     # the same gradients again (same generator, offset and buffer length), bucket by bucket
     tal = None
     for (a, b) in buckets:
-        for r in range(n):
-            S.draw_grads(w, gbuf[r], w.psi, step, r, 1.0, offset=a)
+        draw(a)
         tal = fc.compare(a, b, psi=w.psi, part=part, dtype=dt, grads=gbuf, g_base=a, old=buf.state(slot),
                          new=buf.state(st["state_slot"]), q=buf.params, loss_scale=1.0,
                          sc=O.step_scalars(ho, st0["steps_applied"] + 1), tally=tal)

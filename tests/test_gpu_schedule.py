@@ -50,9 +50,10 @@ def _state(buf):
 def test_prefetch_matches_sequential_and_oracle(double_buffer):
     h = B.hyper(weight_decay=0.01)
     results = []
-    for prefetch in (False, True):
+    # sequential, side-stream prefetch, and backward gathers fused into the reduce-scatters
+    for prefetch, fuse in ((False, False), (True, False), (False, True), (True, True)):
         part, buckets, buf, st, grads, gb = _setup(double_buffer)
-        sched = Zero3Schedule(buf, buckets, prefetch=prefetch)
+        sched = Zero3Schedule(buf, buckets, prefetch=prefetch, fuse=fuse)
         seen = []
 
         def fwd(i, rows):
@@ -65,8 +66,9 @@ def test_prefetch_matches_sequential_and_oracle(double_buffer):
         assert all(seen) and len(seen) == 3 * 2 * len(buckets)
         results.append(_state(buf))
         buf.close()
-    for x, y in zip(results[0][:4], results[1][:4]):
-        assert np.array_equal(x, y)
+    for other in results[1:]:
+        for x, y in zip(results[0][:4], other[:4]):
+            assert np.array_equal(x, y)
     # and the oracle
     part, buckets, buf, st, grads, gb = _setup(double_buffer)
     gbits = bits16(grads)
@@ -78,11 +80,12 @@ def test_prefetch_matches_sequential_and_oracle(double_buffer):
     buf.close()
 
 
-def test_cuda_graph_replay_matches_eager():
+@pytest.mark.parametrize("fuse", [False, True])
+def test_cuda_graph_replay_matches_eager(fuse):
     h = B.hyper(weight_decay=0.01)
     # eager: 4 steps
     part, buckets, buf, st, grads, gb = _setup()
-    sched = Zero3Schedule(buf, buckets, prefetch=True)
+    sched = Zero3Schedule(buf, buckets, prefetch=True, fuse=fuse)
     for _ in range(4):
         sched.step(h, lambda i: [gb[i][r] for r in range(N)])
     torch.cuda.synchronize()
@@ -90,7 +93,7 @@ def test_cuda_graph_replay_matches_eager():
     buf.close()
     # one eager warm-up step, capture one step, replay it three times
     part, buckets, buf, st, grads, gb = _setup()
-    sched = Zero3Schedule(buf, buckets, prefetch=True)
+    sched = Zero3Schedule(buf, buckets, prefetch=True, fuse=fuse)
     sched.step(h, lambda i: [gb[i][r] for r in range(N)])
     g = sched.capture(h, lambda i: [gb[i][r] for r in range(N)])
     torch.cuda.synchronize()

@@ -16,6 +16,6 @@ from ._binding import (  # noqa: F401
     zero_get_status, zero_init_partition, zero_last_error, zero_partition_info,
     zero_reduce_scatter_bucket, zero_reduce_scatter_bucket_replicas, zero_set_scaler, zero_step,
     zero_step_noalloc, zero_noalloc_scratch_bytes, zero_quantize_blocks, zero_dequantize_blocks, zero_gather_bucket_q8,
-    zero_reduce_scatter_bucket_q, ZERO_Q_BLOCK,
+    zero_reduce_scatter_bucket_q, ZERO_Q_BLOCK, zero_reduce_scatter_gather_bucket, zero_set_persistent,
     result_from_device, pointer_array,
 )

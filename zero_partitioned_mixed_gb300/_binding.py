@@ -24,7 +24,7 @@ EXPORTS = (
     "zero_bytes_moved", "zero_last_error", "zero_destroy", "zero_step_noalloc",
     "zero_reduce_scatter_bucket_replicas", "zero_quantize_blocks", "zero_dequantize_blocks",
     "zero_gather_bucket_q8", "zero_reduce_scatter_bucket_q", "zero_debug_hold_staged",
-    "zero_noalloc_scratch_bytes", "zero_set_persistent",
+    "zero_noalloc_scratch_bytes", "zero_set_persistent", "zero_reduce_scatter_gather_bucket",
 )
 ZERO_Q_BLOCK = 256
 
@@ -84,6 +84,8 @@ def load_library():
     lib.zero_step.argtypes = [P, C.POINTER(P), C.POINTER(P), P, P, P, C.POINTER(Hyper), P]
     lib.zero_gather_bucket.argtypes = [P, U64, U64, P, C.POINTER(P), P]
     lib.zero_reduce_scatter_bucket.argtypes = [P, U64, U64, C.POINTER(P), P, P, P, P, C.POINTER(Hyper), P]
+    lib.zero_reduce_scatter_gather_bucket.argtypes = [P, U64, U64, C.POINTER(P), P, P, P, P, C.POINTER(Hyper),
+                                                      U64, U64, C.POINTER(P), P]
     lib.zero_reduce_scatter_bucket_replicas.argtypes = [P, U64, U64, C.POINTER(P), P, P, P, C.POINTER(P),
                                                          C.POINTER(Hyper), P]
     lib.zero_quantize_blocks.argtypes = [I32, I32, P, U64, P, P, P]
@@ -210,6 +212,14 @@ def zero_gather_bucket(h, a: int, b: int, shard16, out, stream=None):
 def zero_reduce_scatter_bucket(h, a: int, b: int, grads, master, m, v, shard16, hyp: Hyper, stream=None):
     rc = load_library().zero_reduce_scatter_bucket(h, a, b, _ptr_array(grads), _ptr(master), _ptr(m),
                                                    _ptr(v), _ptr(shard16), C.byref(hyp), _stream(stream))
+    _check(rc, h)
+
+
+def zero_reduce_scatter_gather_bucket(h, a: int, b: int, grads, master, m, v, shard16, hyp: Hyper, ga: int,
+                                      gb: int, out, stream=None):
+    rc = load_library().zero_reduce_scatter_gather_bucket(h, a, b, _ptr_array(grads), _ptr(master), _ptr(m),
+                                                          _ptr(v), _ptr(shard16), C.byref(hyp), ga, gb,
+                                                          _ptr_array(out), _stream(stream))
     _check(rc, h)
 
 

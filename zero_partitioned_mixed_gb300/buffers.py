@@ -119,6 +119,11 @@ class RankBuffers:
             B.zero_reduce_scatter_bucket(self.h, a, b, grads, self.master, self.m, self.v, self.params, hyp,
                                          stream)
 
+    def reduce_scatter_gather(self, a: int, b: int, grads: List, hyp, ga: int, gb: int, out: List, stream=None):
+        """Stage 3: reduce-scatter of bucket [a, b) and gather of [ga, gb) into out, in one call."""
+        B.zero_reduce_scatter_gather_bucket(self.h, a, b, grads, self.master, self.m, self.v, self.params, hyp,
+                                            ga, gb, out, stream)
+
     def finish_bucketed_step(self, hyp, stream=None):
         """zero_step after the step's buckets were reduce-scattered (stages 2 and 3)."""
         B.zero_step(self.h, None, self._param_ptrs, self.master, self.m, self.v, hyp, stream)

@@ -199,9 +199,12 @@ bool same_hyper(const zero_hyper_t& x, const zero_hyper_t& y) {
 // Reduce-scatter of one bucket of a step whose gradients arrive bucket by
 // bucket (stage 3 always; stage 2 when the caller reduces during backward).
 // outs: the 16-bit shard (stage 3) or the N replicas (stage 2).
+// gout (stage 3, 8-wide, checked by the caller): the same launch then
+// gathers [ga, ga + gcount) of the shard outs[0] into gout[r].
 int rs_bucket(zero_handle* h, uint64_t a0, uint64_t b0, const void* const* grads, float* master, float* m,
               float* v, void* const* outs, const zero_hyper_t* hyper, void* stream, int qbits = 0,
-              const float* const* qscales = nullptr) {
+              const float* const* qscales = nullptr, uint64_t ga = 0, uint64_t gcount = 0,
+              void* const* gout = nullptr) {
     int rc = check_hyper(h, hyper);
     if (rc) return rc;
     if (a0 > b0 || b0 > h->psi_pad) return fail(h, ZERO_EINVAL, "bucket must satisfy 0 <= a <= b <= psi_pad");
@@ -266,6 +269,13 @@ int rs_bucket(zero_handle* h, uint64_t a0, uint64_t b0, const void* const* grads
         const cudaError_t e = zg::launch_q(spec ? zg::QKind::kRsQSpec : zg::QKind::kRsQWs, h->dtype, qbits,
                                            pick_vec(vec8, a), a, static_cast<cudaStream_t>(stream));
         if (e != cudaSuccess) return cuda_fail(h, e, "quantized reduce-scatter");
+    } else if (gout) {
+        a.params[0] = outs[0];   // the gather's source, also in two-pass mode
+        for (int r = 0; r < h->n; ++r) a.gout[r] = gout[r];
+        a.gbase = ga;
+        a.gcount = gcount;
+        const zg::Kind kind = spec ? zg::Kind::kRsSpecGather : zg::Kind::kRsWsGather;
+        if ((rc = launch(h, kind, vec8, a, static_cast<cudaStream_t>(stream), "reduce-scatter + gather"))) return rc;
     } else {
         const zg::Kind kind =
             !spec ? zg::Kind::kRsWs : (h->stage == 3 ? zg::Kind::kRsSpec : zg::Kind::kRsSpecReplicas);
@@ -278,9 +288,16 @@ int rs_bucket(zero_handle* h, uint64_t a0, uint64_t b0, const void* const* grads
     h->rs_calls += 1;
     h->covered.emplace_back(a0, b0);
     const uint64_t in_bytes = qbits ? N * (L * qbits / 8 + 8 * ((L + zg::kQBlock - 1) / zg::kQBlock)) : 2 * N * L;
-    if (spec) count(h, in_bytes + 12 * L, 12 * L + 2 * static_cast<uint64_t>(n_out) * L);
-    else count(h, in_bytes, 4 * L);
+    const uint64_t g_r = gout ? 2 * gcount : 0, g_w = gout ? 2 * N * gcount : 0;
+    if (spec) count(h, in_bytes + 12 * L + g_r, 12 * L + 2 * static_cast<uint64_t>(n_out) * L + g_w);
+    else count(h, in_bytes + g_r, 4 * L + g_w);
     return ZERO_OK;
+}
+
+// Byte ranges [p, p + n) and [q, q + k) share a byte.
+bool overlaps(const void* p, uint64_t n, const void* q, uint64_t k) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p), b = reinterpret_cast<uintptr_t>(q);
+    return n > 0 && k > 0 && a < b + k && b < a + n;
 }
 
 bool aligned8(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 7u) == 0; }
@@ -575,6 +592,44 @@ int zero_reduce_scatter_bucket(zero_handle_t h, uint64_t a0, uint64_t b0, const 
     if (h->stage != 3) return fail(h, ZERO_EINVAL, "zero_reduce_scatter_bucket is for stage 3");
     void* outs[1] = {shard16};
     return rs_bucket(h, a0, b0, grads, master, m, v, outs, hyper, stream);
+}
+
+int zero_reduce_scatter_gather_bucket(zero_handle_t h, uint64_t a0, uint64_t b0, const void* const* grads,
+                                      float* master, float* m, float* v, void* shard16, const zero_hyper_t* hyper,
+                                      uint64_t ga, uint64_t gb, void* const* out, void* stream) {
+    CallRange range_("zero_reduce_scatter_gather_bucket");
+    if (!h) return fail(nullptr, ZERO_EINVAL, "handle is NULL");
+    if (h->stage != 3) return fail(h, ZERO_EINVAL, "zero_reduce_scatter_gather_bucket is for stage 3");
+    if (a0 > b0 || b0 > h->psi_pad || ga > gb || gb > h->psi_pad)
+        return fail(h, ZERO_EINVAL, "buckets must satisfy 0 <= a <= b <= psi_pad and 0 <= ga <= gb <= psi_pad");
+    const uint64_t L = b0 - a0, GL = gb - ga;
+    if (L > 0 && GL > 0 && a0 < gb && ga < b0)
+        return fail(h, ZERO_EINVAL, "the gathered bucket overlaps the reduce-scattered one");
+    int rc = ZERO_OK;
+    if (GL > 0) {
+        if ((rc = check_ptr(h, shard16, "shard16"))) return rc;
+        if (!out) return fail(h, ZERO_EINVAL, "out is NULL");
+        for (int r = 0; r < h->n; ++r) {
+            if ((rc = check_ptr(h, out[r], "out[r]"))) return rc;
+            // both parts may run at once: the outputs must not share memory
+            // with what the reduce-scatter reads or writes
+            if (overlaps(out[r], 2 * GL, shard16, 2 * h->psi_pad))
+                return fail(h, ZERO_EINVAL, "out[r] overlaps the 16-bit shard");
+            for (int q = 0; L > 0 && grads && q < h->n; ++q)
+                if (overlaps(out[r], 2 * GL, grads[q], 2 * L))
+                    return fail(h, ZERO_EINVAL, "out[r] overlaps a gradient row of the reduce-scattered bucket");
+        }
+    }
+    const bool fuse = L > 0 && GL > 0 && (a0 % 8) == 0 && (L % 8) == 0 && (ga % 8) == 0 && (GL % 8) == 0;
+    void* outs[1] = {shard16};
+    if (fuse) return rs_bucket(h, a0, b0, grads, master, m, v, outs, hyper, stream, 0, nullptr, ga, GL, out);
+    // one part empty, or not 8-wide: the two calls one after the other
+    const uint64_t r0 = h->tot_r, w0 = h->tot_w;
+    if ((rc = rs_bucket(h, a0, b0, grads, master, m, v, outs, hyper, stream))) return rc;
+    if ((rc = zero_gather_bucket(h, ga, gb, shard16, out, stream))) return rc;
+    h->last_r = h->tot_r - r0;
+    h->last_w = h->tot_w - w0;
+    return ZERO_OK;
 }
 
 int zero_reduce_scatter_bucket_replicas(zero_handle_t h, uint64_t a0, uint64_t b0, const void* const* grads,

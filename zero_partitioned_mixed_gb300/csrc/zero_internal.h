@@ -153,6 +153,12 @@ struct Args {
     // its copies, so that its bounded waits run out (0: never)
     uint64_t hold_tile1;
     int ctr_slot;          // chunked launches: this launch's counter, ws.ctrs[ctr_slot]
+    // reduce-scatter fused with the gather of another bucket
+    // (zero_reduce_scatter_gather_bucket): after the reduce-scatter's chunks the
+    // launch copies params[0][gbase, gbase + gcount) to every gout[r]
+    void* gout[kMaxRanks];
+    uint64_t gbase;
+    uint64_t gcount;
 };
 
 enum class Kind : int {
@@ -170,6 +176,8 @@ enum class Kind : int {
     kRsSpec,          // stage 3 bucket reduce-scatter + fused speculative Adam
     kRsWs,            // bucket reduce-scatter into the workspace (stages 2/3)
     kRsSpecReplicas,  // stage 2 bucket reduce-scatter + fused speculative Adam + all-gather
+    kRsSpecGather,    // kRsSpec, then the gather of another bucket in the same launch (8-wide only)
+    kRsWsGather,      // kRsWs, then the gather of another bucket in the same launch (8-wide only)
 };
 
 // Per-thread vector width of a launch: 8 elements with 256-bit fp32 accesses

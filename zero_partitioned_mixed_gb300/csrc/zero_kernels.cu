@@ -56,8 +56,13 @@ __host__ __device__ inline uint64_t step_chunk_target(int n_ranks) { return n_ra
 // AdamW from the live slot into the shadow slot + cast + all-gather.  The
 // last block commits the shadow slot, or records the overflow (the
 // rollback kernel then restores the replicas).
-template <int DT, class IO>
-__global__ void __launch_bounds__(kThreads, 3) k_step_spec(const __grid_constant__ Args a) {
+// MINB CTAs per SM: 3 (80 registers), or 4 (64 registers, some spill) for
+// N <= 2, where an iteration moves few bytes and the extra warps keep more
+// loads in flight: psi = 2^29, N = 2: 2.60 against 2.70 ms; at N = 4 and 8
+// the fourth CTA was slower (3.25 against 3.21 ms, 4.54 against 4.46 ms).
+constexpr int kSmallN = 2;
+template <int DT, class IO, int MINB>
+__global__ void __launch_bounds__(kThreads, MINB) k_step_spec(const __grid_constant__ Args a) {
     pdl_enter();
     constexpr int W = IO::W;
     __shared__ Pro pro;
@@ -436,6 +441,27 @@ __global__ void k_commit_redo(DevStatus* st) {
 // load per store round on the full occupancy grid: this kernel writes N
 // bytes for every byte it reads, and fewer, deeper streams suit that mix.
 constexpr int kGatherPerSm = 3;
+
+// One chunk c of an 8-wide gather of nvec vectors from src (starting at
+// element base, a multiple of 8) to the n outputs.
+__device__ __forceinline__ void gather_chunk8(const void* src, uint64_t base, void* const* outs, int n, uint64_t c,
+                                              uint64_t clen, int U, uint64_t nvec) {
+    static_assert(kChunkU == 4, "one batch of loads covers a chunk");
+    uint4 x[kChunkU];
+    uint64_t vi[kChunkU];
+#pragma unroll
+    for (int u = 0; u < kChunkU; ++u) {
+        vi[u] = u < U ? chunk_vec(c, clen, u) : nvec;
+        if (vi[u] < nvec) x[u] = __ldcs(reinterpret_cast<const uint4*>(src) + (base / 8 + vi[u]));
+    }
+    for (int r = 0; r < n; ++r) {
+        uint4* out = reinterpret_cast<uint4*>(outs[r]);
+#pragma unroll
+        for (int u = 0; u < kChunkU; ++u)
+            if (vi[u] < nvec) __stcs(out + vi[u], x[u]);
+    }
+}
+
 template <class IO>
 __global__ void __launch_bounds__(kThreads) k_gather(const __grid_constant__ Args a) {
     pdl_enter();
@@ -451,20 +477,7 @@ __global__ void __launch_bounds__(kThreads) k_gather(const __grid_constant__ Arg
         if (c >= nchunks) break;
         ch.prefetch();
         if constexpr (W == 8) {
-            static_assert(kChunkU == 4, "one batch of loads covers a chunk");
-            uint4 x[kChunkU];
-            uint64_t vi[kChunkU];
-#pragma unroll
-            for (int u = 0; u < kChunkU; ++u) {
-                vi[u] = u < U ? chunk_vec(c, clen, u) : nvec;
-                if (vi[u] < nvec) x[u] = __ldcs(reinterpret_cast<const uint4*>(a.grads[0]) + (a.base / 8 + vi[u]));
-            }
-            for (int r = 0; r < a.n_ranks; ++r) {
-                uint4* out = reinterpret_cast<uint4*>(a.params[r]);
-#pragma unroll
-                for (int u = 0; u < kChunkU; ++u)
-                    if (vi[u] < nvec) __stcs(out + vi[u], x[u]);
-            }
+            gather_chunk8(a.grads[0], a.base, a.params, a.n_ranks, c, clen, U, nvec);
         } else {
             for (int u = 0; u < U; ++u) {
                 const uint64_t vi = chunk_vec(c, clen, u);
@@ -492,10 +505,20 @@ __global__ void __launch_bounds__(kThreads) k_gather(const __grid_constant__ Arg
 // from N = 8 up kChunkU measured better (shorter tail on 5e7-element buckets).
 __host__ __device__ inline int rs_chunk_cap(int n_ranks) { return n_ranks <= 4 ? 16 : kChunkU; }
 
-template <int DT, class IO, bool SPEC, bool TO_REPLICAS>
-__global__ void __launch_bounds__(kThreads, 3) k_rs(const __grid_constant__ Args a) {
+// MINB as for the step: 4 CTAs per SM for N <= 2 (psi = 2^29, N = 2,
+// 5e7-element buckets: 2.73 against 2.77 ms per step's reduce-scatters;
+// slower from N = 4 up).
+// GATHER (8-wide only): the launch's counter hands out the reduce-scatter's
+// chunks, then the chunks of the gather of [gbase, gbase + gcount) of the
+// 16-bit shard (params[0]) to gout[r], so that the CTAs that finish the
+// reduce-scatter early go on to the gather instead of waiting for the
+// launch's last chunks.  The two ranges are disjoint (checked on the host),
+// so the result is that of the two calls one after the other.
+template <int DT, class IO, bool SPEC, bool TO_REPLICAS, int MINB, bool GATHER>
+__global__ void __launch_bounds__(kThreads, MINB) k_rs(const __grid_constant__ Args a) {
     pdl_enter();
     constexpr int W = IO::W;
+    static_assert(!GATHER || W == 8, "the fused gather runs 8-wide");
     __shared__ Pro pro;
     __shared__ unsigned long long s_c[2];
     __shared__ double s_wp[2][kThreads / 32];
@@ -507,12 +530,16 @@ __global__ void __launch_bounds__(kThreads, 3) k_rs(const __grid_constant__ Args
     const uint64_t target = TO_REPLICAS ? kRsReplicaChunks : kMinChunks;
     const uint64_t clen = chunk_len(nvec, umax, target), nchunks = chunk_total(nvec, umax, target);
     const int U = chunk_u(nvec, umax, target);
+    // the gather's chunks follow the reduce-scatter's (none unless GATHER);
+    // its chunk geometry is formed again in its branch from the arguments,
+    // so that it holds no registers across the reduce-scatter's loop
+    const uint64_t ntotal = nchunks + (GATHER ? chunk_total(a.gcount / 8) : 0);
     ChunkCtr* ctr = a.ws.ctrs + a.ctr_slot;
     int bad = 0;
-    Chunks ch(ctr, s_c, nchunks);
+    Chunks ch(ctr, s_c, ntotal);
     for (;;) {
       const uint64_t c = ch.current();
-      if (c >= nchunks) break;
+      if (c >= nchunks) break;     // done, or the first of this CTA's gather chunks
       ch.prefetch();
       double acc = 0.0;
       for (int u = 0; u < U; ++u) {
@@ -557,6 +584,20 @@ __global__ void __launch_bounds__(kThreads, 3) k_rs(const __grid_constant__ Args
       }
       close_chunk(a.ws, c, nchunks, acc, s_wp, ch.parity(), 0);
       ch.advance();
+    }
+    if (GATHER) {
+        // chunks are handed out in order: once a CTA holds a gather chunk it
+        // gets no more reduce-scatter chunks
+        const uint64_t gvec = a.gcount / 8, gclen = chunk_len(gvec);
+        const int gU = chunk_u(gvec);
+        for (;;) {
+            const uint64_t c = ch.current();
+            if (c >= ntotal) break;
+            ch.prefetch();
+            gather_chunk8(a.params[0], a.gbase, a.gout, a.n_ranks, c - nchunks, gclen, gU, gvec);
+            __syncthreads();
+            ch.advance();
+        }
     }
     const int flag = __syncthreads_or(bad);
     if (publish(a, 0.0, flag, a.ws.partials, a.ws.flags)) {
@@ -616,7 +657,11 @@ cudaError_t launch_dw(Kind kind, const Args& a, cudaStream_t s, int* grid_out) {
     const uint64_t nvec = a.count / IO::W;
     switch (kind) {
         case Kind::kStepSpec:
-            return run_chunked_u(k_step_spec<DT, IO>, a, nvec, kStepChunkU, step_chunk_target(a.n_ranks), s, grid_out);
+            return a.n_ranks <= kSmallN
+                       ? run_chunked_u(k_step_spec<DT, IO, 4>, a, nvec, kStepChunkU, step_chunk_target(a.n_ranks), s,
+                                       grid_out)
+                       : run_chunked_u(k_step_spec<DT, IO, 3>, a, nvec, kStepChunkU, step_chunk_target(a.n_ranks), s,
+                                       grid_out);
         case Kind::kReduceWs: return run_chunked<kChunkU, kTwoPassChunks>(k_reduce<DT, IO, true>, a, nvec, s, grid_out);
         case Kind::kReduceNoWs: return run_chunked<kChunkU, kTwoPassChunks>(k_reduce<DT, IO, false>, a, nvec, s, grid_out);
         case Kind::kApplyWs: return run_chunked<kChunkU, kTwoPassChunks>(k_apply<DT, IO, true, false>, a, nvec, s, grid_out);
@@ -627,10 +672,26 @@ cudaError_t launch_dw(Kind kind, const Args& a, cudaStream_t s, int* grid_out) {
         case Kind::kRollbackShard: return run_chunked(k_rollback<DT, IO, true>, a, nvec, s, grid_out);
         case Kind::kFixupReplicas: return run_chunked(k_fixup<DT, IO>, a, nvec, s, grid_out);
         case Kind::kGather: return run_chunked(k_gather<IO>, a, nvec, s, grid_out, IO::W == 8 ? kGatherPerSm : 0);
-        case Kind::kRsSpec: return run_chunked_u(k_rs<DT, IO, true, false>, a, nvec, rs_chunk_cap(a.n_ranks), kMinChunks, s, grid_out);
-        case Kind::kRsSpecReplicas: return run_chunked_u(k_rs<DT, IO, true, true>, a, nvec, rs_chunk_cap(a.n_ranks), kRsReplicaChunks, s,
+        case Kind::kRsSpec:
+            return a.n_ranks <= kSmallN
+                       ? run_chunked_u(k_rs<DT, IO, true, false, 4, false>, a, nvec, rs_chunk_cap(a.n_ranks),
+                                       kMinChunks, s, grid_out)
+                       : run_chunked_u(k_rs<DT, IO, true, false, 3, false>, a, nvec, rs_chunk_cap(a.n_ranks),
+                                       kMinChunks, s, grid_out);
+        case Kind::kRsSpecReplicas: return run_chunked_u(k_rs<DT, IO, true, true, 3, false>, a, nvec, rs_chunk_cap(a.n_ranks), kRsReplicaChunks, s,
                                                             grid_out);
-        case Kind::kRsWs: return run_chunked_u(k_rs<DT, IO, false, false>, a, nvec, rs_chunk_cap(a.n_ranks), kMinChunks, s, grid_out);
+        case Kind::kRsWs: return run_chunked_u(k_rs<DT, IO, false, false, 3, false>, a, nvec, rs_chunk_cap(a.n_ranks), kMinChunks, s, grid_out);
+        case Kind::kRsSpecGather:
+        case Kind::kRsWsGather:
+            if constexpr (IO::W != 8) {
+                return cudaErrorInvalidValue;
+            } else {
+                // one CTA per chunk at most, over both parts of the launch
+                const uint64_t n = chunk_total(nvec, rs_chunk_cap(a.n_ranks), kMinChunks) + chunk_total(a.gcount / 8);
+                if (kind == Kind::kRsWsGather) return run(k_rs<DT, IO, false, false, 3, true>, a, n * kThreads, s, grid_out);
+                return a.n_ranks <= kSmallN ? run(k_rs<DT, IO, true, false, 4, true>, a, n * kThreads, s, grid_out)
+                                            : run(k_rs<DT, IO, true, false, 3, true>, a, n * kThreads, s, grid_out);
+            }
     }
     return cudaErrorInvalidValue;
 }

@@ -52,28 +52,40 @@ __device__ __forceinline__ float warp_qmax(float a) {
 
 constexpr float kTwo23 = 8388608.0f;
 
-// rint(clamp(q, 0, top)) as an integer for q = (x - lo) / scale rounded once
-// (IEEE division); a NaN q gives 0 (fmaxf returns the other operand).
+// A lane's codes rint(clamp(q, 0, top)) for q = (x - lo) / scale rounded once
+// (IEEE division), elements k < nv; a NaN q gives 0 (fmaxf returns the other
+// operand); 0 throughout when scale is 0.
 //
 // The division is taken only where it can matter.  With rcp = 1/scale
 // rounded once, u = d * rcp (d = x - lo) differs from the exact d / scale by
-// a factor (1 + e1)(1 + e2), |e1|, |e2| <= 2^-24, and the rounded quotient q
-// from it by at most 2^-24 relative, so |u - q| < u * 2^-22.  rint(clamp(.))
-// is constant between consecutive half-integers, so u and q give the same
-// code unless a half-integer lies within u * 2^-22 of u.  The test below
-// takes the division whenever one lies within u * 2^-20 (a margin of 4):
-// for values spread over the levels that is about one element in 4000.
-// fast is false for a block whose scale is not a normal number in
-// [2^-100, 2^100] (the bounds above assume no underflow or overflow), and
-// then every element is divided.
-__device__ __forceinline__ uint32_t code_of(float x, float lo, float scale, float rcp, bool fast, float top) {
-    const float d = __fsub_rn(x, lo);
-    float q = __fmul_rn(d, rcp);
-    // 0 <= q < 2^23 here, so q - floor(q) is exact
-    const float off = fabsf(__fsub_rn(__fsub_rn(q, floorf(q)), 0.5f));
-    if (!fast || !(off > __fmul_rn(fabsf(q), 0x1p-20f))) q = __fdiv_rn(d, scale);
-    const float u = fminf(fmaxf(q, 0.0f), top);
-    return __float_as_uint(__fadd_rn(u, kTwo23)) & 0x1FFu;
+// a factor (1 + e1)(1 + e2), |e1|, |e2| <= 2^-24, and the rounded quotient
+// from it by at most 2^-24 relative: the two lie within u * 2^-22 < 2^-14 of
+// each other (u <= top < 256).  rint(clamp(.)) is constant between
+// consecutive half-integers, so they give the same code unless u lies
+// within 2^-14 of a half-integer.  u + 2^23 rounds u to the integer the code
+// is read from, and u - ((u + 2^23) - 2^23) is then u's exact distance r to
+// it; the lane divides all its elements again when some |r| >= 0.5 - 2^-12
+// (a margin of 4): for values spread over the levels that is one lane in
+// about 500.  fast is false for a block whose scale is not a normal number
+// in [2^-100, 2^100] (the bound assumes no underflow or overflow), and then
+// every element is divided.
+__device__ __forceinline__ void codes8(const float (&x)[8], int nv, float lo, float scale, float rcp, bool fast,
+                                       float top, uint32_t (&q)[8]) {
+    float t[8];
+    bool near = !fast;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const float u = fminf(fmaxf(__fmul_rn(__fsub_rn(x[k], lo), rcp), 0.0f), top);
+        t[k] = __fadd_rn(u, kTwo23);
+        near |= k < nv && !(fabsf(__fsub_rn(u, __fsub_rn(t[k], kTwo23))) < 0x1.ffcp-2f);   // 0.5 - 2^-12
+    }
+    if (near) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            t[k] = __fadd_rn(fminf(fmaxf(__fdiv_rn(__fsub_rn(x[k], lo), scale), 0.0f), top), kTwo23);
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) q[k] = (k < nv && scale != 0.0f) ? (__float_as_uint(t[k]) & 0x1FFu) : 0u;
 }
 
 // float(q) for q < 2^23, exactly.
@@ -212,21 +224,28 @@ __device__ __forceinline__ f2 f2dequant(f2 q_biased, f2 two23, f2 sc, float lo) 
 }
 
 
-// A lane's 8 codes at element e0 as four pairs of 2^23-biased floats
-// (0x4B000000 | code): subtracting 2^23 gives the codes exactly.
+// A lane's 8 codes at element e0 as they lie in memory: 8 bytes (INT8,
+// both words used) or 4 bytes (INT4, .y unused).
 template <int BITS>
-__device__ __forceinline__ void load_codes8_biased(const void* codes, uint64_t e0, f2 (&q)[4]) {
+__device__ __forceinline__ uint2 load_codes8_raw(const void* codes, uint64_t e0) {
+    if (BITS == 8) return __ldcs(reinterpret_cast<const uint2*>(static_cast<const unsigned char*>(codes) + e0));
+    return make_uint2(__ldcs(reinterpret_cast<const unsigned int*>(static_cast<const unsigned char*>(codes) + (e0 >> 1))), 0u);
+}
+
+// Those codes as four pairs of 2^23-biased floats (0x4B000000 | code):
+// subtracting 2^23 gives the codes exactly.  Kept apart from the load so
+// that the loads of several ranks hold only their raw words in registers.
+template <int BITS>
+__device__ __forceinline__ void expand_codes8(uint2 w, f2 (&q)[4]) {
     if (BITS == 8) {
-        const uint2 w = __ldcs(reinterpret_cast<const uint2*>(static_cast<const unsigned char*>(codes) + e0));
         q[0] = f2bits(__byte_perm(w.x, 0x4B000000u, 0x7540u), __byte_perm(w.x, 0x4B000000u, 0x7541u));
         q[1] = f2bits(__byte_perm(w.x, 0x4B000000u, 0x7542u), __byte_perm(w.x, 0x4B000000u, 0x7543u));
         q[2] = f2bits(__byte_perm(w.y, 0x4B000000u, 0x7540u), __byte_perm(w.y, 0x4B000000u, 0x7541u));
         q[3] = f2bits(__byte_perm(w.y, 0x4B000000u, 0x7542u), __byte_perm(w.y, 0x4B000000u, 0x7543u));
     } else {
-        const uint32_t w = __ldcs(reinterpret_cast<const unsigned int*>(static_cast<const unsigned char*>(codes) + (e0 >> 1)));
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-            q[k] = f2bits(((w >> (8 * k)) & 0xFu) | 0x4B000000u, ((w >> (8 * k + 4)) & 0xFu) | 0x4B000000u);
+            q[k] = f2bits(((w.x >> (8 * k)) & 0xFu) | 0x4B000000u, ((w.x >> (8 * k + 4)) & 0xFu) | 0x4B000000u);
     }
 }
 
@@ -278,8 +297,7 @@ __device__ __forceinline__ void quantize_blocks_u(const unsigned short* src, uin
         bool fast;
         block_scale<BITS>(x[u], nv[u], scale, lo, rcp, fast);
         uint32_t q[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) q[k] = (k < nv[u] && scale != 0.0f) ? code_of(x[u][k], lo, scale, rcp, fast, top) : 0u;
+        codes8(x[u], nv[u], lo, scale, rcp, fast, top, q);
         emit(blk0 + u, (blk0 + u) * kQBlock + static_cast<uint64_t>(lane) * 8, nv[u], q, scale, lo);
     }
 }
@@ -394,24 +412,26 @@ __device__ __forceinline__ void reduce_group_q(const Args& a, uint64_t j, const 
         for (int k = 0; k < 4; ++k) s2[k] = f2pack(0.0f, 0.0f);
         int r = 0;
         for (; r + 8 <= n; r += 8) {
-            f2 q[8][4];
+            uint2 w[8];
             float2 sl[8];
 #pragma unroll
             for (int t = 0; t < 8; ++t) {
                 sl[t] = *reinterpret_cast<const float2*>(a.qsrc[r + t] + 2 * blk);
-                load_codes8_biased<BITS>(a.grads[r + t], j, q[t]);
+                w[t] = load_codes8_raw<BITS>(a.grads[r + t], j);
             }
 #pragma unroll
             for (int t = 0; t < 8; ++t) {
+                f2 q[4];
+                expand_codes8<BITS>(w[t], q);
                 const f2 sc = f2pack(sl[t].x, sl[t].x);
 #pragma unroll
-                for (int k = 0; k < 4; ++k) s2[k] = f2add(s2[k], f2dequant(q[t][k], two23, sc, sl[t].y));
+                for (int k = 0; k < 4; ++k) s2[k] = f2add(s2[k], f2dequant(q[k], two23, sc, sl[t].y));
             }
         }
         for (; r < n; ++r) {
             const float2 sl = *reinterpret_cast<const float2*>(a.qsrc[r] + 2 * blk);
             f2 q[4];
-            load_codes8_biased<BITS>(a.grads[r], j, q);
+            expand_codes8<BITS>(load_codes8_raw<BITS>(a.grads[r], j), q);
             const f2 sc = f2pack(sl.x, sl.x);
 #pragma unroll
             for (int k = 0; k < 4; ++k) s2[k] = f2add(s2[k], f2dequant(q[k], two23, sc, sl.y));
