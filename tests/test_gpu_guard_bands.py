@@ -138,3 +138,43 @@ def test_no_writes_outside_buffers_staged_step(psi, n):
     torch.cuda.synchronize()
     G.check()
     B.zero_destroy(h)
+
+
+@pytest.mark.parametrize("db", [True, False])
+@pytest.mark.parametrize("n", [2, 8])
+def test_no_writes_outside_buffers_fused_backward(db, n):
+    # ZeRO-3 backward through zero_reduce_scatter_gather_bucket: one launch for
+    # 8-aligned bucket pairs, two calls otherwise; guarded gradient rows,
+    # gather outputs, shard and state
+    G = Guarded()
+    psi = 70_001
+    h = B.zero_init_partition(psi, n, 3, B.ZERO_BF16, 8, B.ZERO_F_DOUBLE_BUFFER if db else 0)
+    P = B.zero_partition_info(h)[0]
+    shard = G.tensor(P, torch.bfloat16)
+    master, m, v = (G.tensor((2 if db else 1) * P, torch.float32) for _ in range(3))
+    master[:psi].normal_(0, 0.02)
+    shard.copy_(master[:P].to(torch.bfloat16))
+    # step 0: 8-aligned buckets (each pair one launch); step 1: unaligned ones (two calls)
+    layouts = [[(0, 30_000), (30_000, 30_008), (30_008, 61_000), (61_000, P)],
+               [(0, 30_000), (30_000, 30_005), (30_005, 61_000), (61_000, P)]]
+    hyp = B.hyper()
+    for step in range(2):
+        back = list(reversed(layouts[step]))
+        first = back[0]
+        B.zero_gather_bucket(h, first[0], first[1], shard, [G.tensor(first[1] - first[0], torch.bfloat16)
+                                                          for _ in range(n)])
+        for k, (a, b) in enumerate(back):
+            L = b - a
+            g = [G.tensor(L, torch.bfloat16) for _ in range(n)]
+            for t in g:
+                t.copy_(torch.randn(L, device="cuda").mul_(1e-2))
+            if k + 1 < len(back):
+                ga, gb = back[k + 1]
+                outs = [G.tensor(gb - ga, torch.bfloat16) for _ in range(n)]
+                B.zero_reduce_scatter_gather_bucket(h, a, b, g, master, m, v, shard, hyp, ga, gb, outs)
+            else:
+                B.zero_reduce_scatter_bucket(h, a, b, g, master, m, v, shard, hyp)
+        B.zero_step(h, None, [shard], master, m, v, hyp)
+    torch.cuda.synchronize()
+    G.check()
+    B.zero_destroy(h)
