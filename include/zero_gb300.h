@@ -256,7 +256,7 @@ ZERO_API int zero_reduce_scatter_bucket(zero_handle_t h, uint64_t a, uint64_t b,
  * the gather's, so that the gather fills the end of the reduce-scatter;
  * otherwise the two calls are made in turn.  Either part may be empty.
  *   The two buckets must not overlap, and no out[r] may share memory with
- *   the 16-bit shard or with a gradient row of [a, b) (ZERO_EINVAL).
+ *   the 16-bit shard, master, m, v or a gradient row of [a, b) (ZERO_EINVAL).
  *   Arguments: those of zero_reduce_scatter_bucket, then ga, gb and out
  *   (host array of N device pointers, gb - ga elements each) as for
  *   zero_gather_bucket.  zero_bytes_moved counts both parts as this call.

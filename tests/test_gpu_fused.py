@@ -72,8 +72,10 @@ def test_fused_refusals():
     refused(0, 4_000, grads, hyp, 4_000, P + 8, outs, msg="0 <= ga <= gb <= psi_pad")
     # an output row that is one of the gradient rows
     refused(0, 4_000, grads, hyp, 4_000, 8_000, [grads[1]] + outs[1:], msg="overlaps a gradient row")
-    # an output row inside the shard
+    # an output row inside the shard, or inside the fp32 state
     refused(0, 4_000, grads, hyp, 4_000, 8_000, [buf.params[4_000:]] + outs[1:], msg="overlaps the 16-bit shard")
+    refused(0, 4_000, grads, hyp, 4_000, 8_000, outs[:3] + [buf.m.view(torch.bfloat16)[16:]],
+            msg="overlaps master, m or v")
     # nothing was reduced: a whole step still goes through
     for (a, b), (ga, gb) in (((0, 4_000), (4_000, 8_000)), ((4_000, 8_000), (8_000, P)), ((8_000, P), (0, 0))):
         buf.reduce_scatter_gather(a, b, grads, hyp, ga, gb, outs)

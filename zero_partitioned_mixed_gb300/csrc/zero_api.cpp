@@ -615,6 +615,10 @@ int zero_reduce_scatter_gather_bucket(zero_handle_t h, uint64_t a0, uint64_t b0,
             // with what the reduce-scatter reads or writes
             if (overlaps(out[r], 2 * GL, shard16, 2 * h->psi_pad))
                 return fail(h, ZERO_EINVAL, "out[r] overlaps the 16-bit shard");
+            const uint64_t state_bytes = 4 * h->psi_pad * (double_buffered(h) ? 2 : 1);
+            for (const float* st : {master, m, v})
+                if (overlaps(out[r], 2 * GL, st, state_bytes))
+                    return fail(h, ZERO_EINVAL, "out[r] overlaps master, m or v");
             for (int q = 0; L > 0 && grads && q < h->n; ++q)
                 if (overlaps(out[r], 2 * GL, grads[q], 2 * L))
                     return fail(h, ZERO_EINVAL, "out[r] overlaps a gradient row of the reduce-scattered bucket");

@@ -243,9 +243,13 @@ __device__ __forceinline__ void expand_codes8(uint2 w, f2 (&q)[4]) {
         q[2] = f2bits(__byte_perm(w.y, 0x4B000000u, 0x7540u), __byte_perm(w.y, 0x4B000000u, 0x7541u));
         q[3] = f2bits(__byte_perm(w.y, 0x4B000000u, 0x7542u), __byte_perm(w.y, 0x4B000000u, 0x7543u));
     } else {
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-            q[k] = f2bits(((w.x >> (8 * k)) & 0xFu) | 0x4B000000u, ((w.x >> (8 * k + 4)) & 0xFu) | 0x4B000000u);
+        // even elements are the low nibbles, odd ones the high nibbles: split
+        // them into bytes, then place each byte under the 2^23 exponent
+        const uint32_t ev = w.x & 0x0F0F0F0Fu, od = (w.x >> 4) & 0x0F0F0F0Fu;
+        q[0] = f2bits(__byte_perm(ev, 0x4B000000u, 0x7540u), __byte_perm(od, 0x4B000000u, 0x7540u));
+        q[1] = f2bits(__byte_perm(ev, 0x4B000000u, 0x7541u), __byte_perm(od, 0x4B000000u, 0x7541u));
+        q[2] = f2bits(__byte_perm(ev, 0x4B000000u, 0x7542u), __byte_perm(od, 0x4B000000u, 0x7542u));
+        q[3] = f2bits(__byte_perm(ev, 0x4B000000u, 0x7543u), __byte_perm(od, 0x4B000000u, 0x7543u));
     }
 }
 
