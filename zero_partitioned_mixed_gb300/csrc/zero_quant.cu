@@ -52,6 +52,39 @@ __device__ __forceinline__ float warp_qmax(float a) {
 
 constexpr float kTwo23 = 8388608.0f;
 
+// Two fp32 lanes in one 64-bit register for the packed add/sub/mul.rn.f32x2
+// of sm_100 and later: each half is an ordinary fp32 operation rounded once,
+// so results are those of the scalar instructions, at half the issue cost.
+using f2 = unsigned long long;
+__device__ __forceinline__ f2 f2pack(float a, float b) {
+    f2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ f2 f2bits(uint32_t a, uint32_t b) {
+    f2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(a), "r"(b));
+    return r;
+}
+__device__ __forceinline__ void f2unpack(f2 x, float& a, float& b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(x));
+}
+__device__ __forceinline__ f2 f2add(f2 a, f2 b) {
+    f2 r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ f2 f2sub(f2 a, f2 b) {
+    f2 r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ f2 f2mul(f2 a, f2 b) {
+    f2 r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
 // A lane's codes rint(clamp(q, 0, top)) for q = (x - lo) / scale rounded once
 // (IEEE division), elements k < nv; a NaN q gives 0 (fmaxf returns the other
 // operand); 0 throughout when scale is 0.
@@ -73,11 +106,19 @@ __device__ __forceinline__ void codes8(const float (&x)[8], int nv, float lo, fl
                                        float top, uint32_t (&q)[8]) {
     float t[8];
     bool near = !fast;
+    // pairs of elements in packed operations (each half one IEEE-rounded
+    // fp32 operation; no multiply feeds an add, so nothing is contracted)
+    const f2 lo2 = f2pack(lo, lo), rcp2 = f2pack(rcp, rcp), two23 = f2pack(kTwo23, kTwo23);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const float u = fminf(fmaxf(__fmul_rn(__fsub_rn(x[k], lo), rcp), 0.0f), top);
-        t[k] = __fadd_rn(u, kTwo23);
-        near |= k < nv && !(fabsf(__fsub_rn(u, __fsub_rn(t[k], kTwo23))) < 0x1.ffcp-2f);   // 0.5 - 2^-12
+    for (int k = 0; k < 8; k += 2) {
+        float q0, q1, r0, r1;
+        f2unpack(f2mul(f2sub(f2pack(x[k], x[k + 1]), lo2), rcp2), q0, q1);
+        const f2 u = f2pack(fminf(fmaxf(q0, 0.0f), top), fminf(fmaxf(q1, 0.0f), top));
+        const f2 tt = f2add(u, two23);
+        f2unpack(f2sub(u, f2sub(tt, two23)), r0, r1);
+        f2unpack(tt, t[k], t[k + 1]);
+        // 0.5 - 2^-12
+        near |= (k < nv && !(fabsf(r0) < 0x1.ffcp-2f)) || (k + 1 < nv && !(fabsf(r1) < 0x1.ffcp-2f));
     }
     if (near) {
 #pragma unroll
@@ -189,28 +230,6 @@ __device__ __forceinline__ void load_codes8(const void* codes, uint64_t e0, uint
     }
 }
 
-// Two fp32 lanes in one 64-bit register for the packed add/sub/mul.rn.f32x2
-// of sm_100 and later: each half is an ordinary fp32 operation rounded once,
-// so results are those of the scalar instructions, at half the issue cost.
-using f2 = unsigned long long;
-__device__ __forceinline__ f2 f2pack(float a, float b) {
-    f2 r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
-    return r;
-}
-__device__ __forceinline__ f2 f2bits(uint32_t a, uint32_t b) {
-    f2 r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(a), "r"(b));
-    return r;
-}
-__device__ __forceinline__ void f2unpack(f2 x, float& a, float& b) {
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(x));
-}
-__device__ __forceinline__ f2 f2add(f2 a, f2 b) {
-    f2 r;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
 // lo + q*scale for a pair, with the multiply packed and the add scalar: a
 // packed multiply feeding a packed add may be fused into one packed FMA
 // (observed: results then differ from two separately rounded operations).
