@@ -1018,8 +1018,9 @@ def run_other(args, ws, rank, local):
                     ms, bps, st = bench_stage3(w, S.flat_buckets(pp, n, 50_000_000), args.steps, args.warmup,
                                                torch, S, Z, flush_l2=flush, fused=not args.separate)
                 else:
+                    mode = Z.ZERO_MODE_SPECULATIVE_STAGED if args.mode == "staged" else None
                     ms, bps, st = bench_dense(w, stage, args.steps, args.warmup, torch, S, Z, flush_l2=flush,
-                                              sets_max=1)
+                                              sets_max=1, mode=mode)
                 extra = {"psi": psi, "n_ranks": n, "stage": stage,
                          "l2": "256 MiB written between timed calls" if flush else "inputs larger than L2"}
                 if stage == 3:
@@ -1042,7 +1043,8 @@ def main(argv=None):
                                       "flat-zero3", "flat-zeropp", "schedule", "gpt2-zero3-persist"],
                     default="flat1.5b")
     ap.add_argument("--mode", choices=["auto", "staged"], default="auto",
-                    help="flat workload: the step kernel (staged = inputs through shared memory by bulk copies)")
+                    help="flat workload and the sweep's stages 1/2: the step kernel (staged = inputs through "
+                         "shared memory by bulk copies)")
     ap.add_argument("--rs-bits", type=int, choices=[8, 4], default=8,
                     help="flat-zeropp: code width of the quantized gradient reduce-scatter")
     ap.add_argument("--no-e2e", action="store_true")

@@ -547,3 +547,46 @@ def test_double_buffer_chosen_from_free_memory():
     buf = RankBuffers(1 << 20, 8, 3, "bf16", double_buffer=None)
     assert buf.double_buffer
     buf.close()
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("stage", [1, 3])
+def test_cast_at_the_limits_of_the_16_bit_formats(dtype, stage):
+    # Zero gradients and zero moments leave the master unchanged (AdamW
+    # without decay adds -step * 0 / (0 + eps)), so the replicas or the shard
+    # after a step are the cast of the master: values at fp16's overflow
+    # threshold (65520 rounds to inf, 65519.996 to 65504), past bf16's
+    # largest finite value, in the subnormal ranges, and at ties to even.
+    import oracle as O
+    from zero_partitioned_mixed_gb300 import _binding as B
+    from zero_partitioned_mixed_gb300.buffers import RankBuffers
+    vals = np.array([65504.0, 65519.996, 65520.0, -65520.0, 1e10, -1e38, 3.3895314e38, 3.4e38,
+                     2.0 ** -24, 2.0 ** -25, 3 * 2.0 ** -26, 2.0 ** -14 * 1.5, 1.0 + 2.0 ** -11, 1.0 + 3 * 2.0 ** -11,
+                     1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, 1e-40, -1e-45, 0.0, -0.0], np.float32)
+    psi, n = 4096, 4
+    master = np.resize(vals, psi).astype(np.float32)
+    buf = RankBuffers(psi, n, stage, dtype)
+    P = buf.psi_pad
+    part = O.partition(psi, n, 8)
+    ost = O.init_state(stage, dtype, part, master)
+    buf.master[:P].copy_(torch.from_numpy(ost.master))
+    td = torch.float16 if dtype == "fp16" else torch.bfloat16
+    if stage == 3:
+        buf.params[:P].copy_(torch.from_numpy(ost.params.view(np.int16)).view(td))
+        buf.reduce_scatter(0, P, [torch.zeros(P, dtype=td, device="cuda") for _ in range(n)], B.hyper())
+        buf.step(B.hyper())
+    else:
+        buf.params[:, :P].copy_(torch.from_numpy(ost.params.view(np.int16)).view(td))
+        buf.grads.zero_()
+        buf.step(B.hyper())
+    zeros = np.zeros((n, P), np.uint16)
+    ost, res = O.step(ost, zeros, O.Hyper(), [(0, P)] if stage == 3 else None)
+    s = buf.status()
+    assert s["applied"] and res.applied
+    got = buf.params[:P] if stage == 3 else buf.params[:, :P]
+    got = got.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.array_equal(got, ost.params)
+    want = O.rne16(master, dtype)
+    first = got[:psi] if stage == 3 else got[0, :psi]
+    assert np.array_equal(first, want)
+    buf.close()
