@@ -27,8 +27,9 @@
  *    library owns only its workspace (status word, norm partials, chunk
  *    counters, and for some modes an fp32 gradient buffer of psi_pad floats).
  *  - Device pointers must be 16-byte aligned.  The 128-bit vector path runs
- *    when psi_pad (or a bucket's bounds) are multiples of 8; otherwise an
- *    element-wise path runs with the same arithmetic.
+ *    when psi_pad (or a bucket's bounds) are multiples of 8, and for a bucket
+ *    of double-buffered state also psi_pad (the second slot's offset);
+ *    otherwise an element-wise path runs with the same arithmetic.
  *  - Calls are asynchronous on the given CUDA stream (a cudaStream_t passed
  *    as void*, NULL = legacy default stream).  One host thread per handle.
  *    The reduce-scatters and steps of one handle share its status word and

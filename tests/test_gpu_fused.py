@@ -87,3 +87,16 @@ def test_fused_refusals():
         B.zero_reduce_scatter_gather_bucket(b2.h, 0, 8, grads, b2.master, b2.m, b2.v, b2.params[0], hyp, 8, 16,
                                             outs)
     b2.close()
+
+
+@pytest.mark.parametrize("stage,fused", [(3, False), (3, True), (2, False)])
+def test_bucketed_steps_when_psi_pad_is_not_a_multiple_of_8(stage, fused):
+    # N = 5 and align 2 give psi_pad = 31,910: the second state slot starts
+    # off an 8-float boundary, so the 8-aligned buckets must still take the
+    # element-wise path (an 8-wide access there would be misaligned)
+    psi, n = 31_910, 5
+    buckets = [(0, 13_520), (13_520, 16_280), (16_280, 17_952), (17_952, 24_864), (24_864, 31_910)]
+    st = run_case(psi, n, stage, "bf16", steps=3, align=2, double_buffer=True, loss_scale=65536.0,
+                  buckets=buckets, fused=fused)
+    st.check()
+    assert st.mismatches == 0, st

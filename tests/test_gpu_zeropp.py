@@ -132,12 +132,20 @@ def test_quantized_gather_matches_oracle(a, b):
 
 @pytest.mark.parametrize("bits", [8, 4])
 @pytest.mark.parametrize("double_buffer", [True, False])
-def test_quantized_reduce_scatter_step_matches_oracle(bits, double_buffer):
-    psi, n, dt = 150_001, 4, "bf16"
-    part = O.partition(psi, n, 8)
+@pytest.mark.parametrize("psi,n,align,cuts", [
+    (150_001, 4, 8, [40_000, 40_013, 99_999]),
+    # psi_pad = 31,910 is not a multiple of 8: with two state slots the
+    # second starts off a vector boundary, so even the 8-aligned buckets
+    # must take the element-wise path
+    (31_910, 5, 2, [13_520, 16_280, 24_864]),
+])
+def test_quantized_reduce_scatter_step_matches_oracle(bits, double_buffer, psi, n, align, cuts):
+    dt = "bf16"
+    part = O.partition(psi, n, align)
     P = part.psi_pad
-    buckets = [(0, 40_000), (40_000, 40_013), (40_013, 99_999), (99_999, P)]
-    buf = RankBuffers(psi, n, 3, dt, double_buffer=double_buffer)
+    edges = [0] + cuts + [P]
+    buckets = list(zip(edges, edges[1:]))
+    buf = RankBuffers(psi, n, 3, dt, align=align, double_buffer=double_buffer)
     g = torch.Generator(device="cuda")
     g.manual_seed(bits)
     master = torch.randn(psi, generator=g, device="cuda") * 0.02
@@ -150,7 +158,7 @@ def test_quantized_reduce_scatter_step_matches_oracle(bits, double_buffer):
         grads = torch.zeros((n, buf.stride), dtype=torch.bfloat16, device="cuda")
         grads[:, :psi] = (torch.randn((n, psi), generator=g, device="cuda") * 1e-2).to(torch.bfloat16)
         if step == 1:
-            grads[2, 77_777] = float("inf")
+            grads[2, psi // 2 + 3] = float("inf")
         gb = bits16(grads)
         for (a, b) in reversed(buckets):
             L = b - a

@@ -164,6 +164,14 @@ zg::Vec pick_vec(bool vec8, const zg::Args& a) {
     return s32 ? zg::Vec::k8s32 : zg::Vec::k8s16;
 }
 
+// The 8-wide path of a bucket [a0, a0 + L) that touches the fp32 state: the
+// bucket on 8-element boundaries, and with two state slots the second slot's
+// base (psi_pad floats in) on one too, else its vector accesses would be
+// misaligned.
+bool bucket_vec8(const zero_handle* h, uint64_t a0, uint64_t L) {
+    return (a0 % 8) == 0 && (L % 8) == 0 && (!double_buffered(h) || (h->psi_pad % 8) == 0);
+}
+
 // Each chunked launch its own counter slot: a gather on one stream may
 // overlap a reduce-scatter on another.
 int next_slot(zero_handle* h) { return static_cast<int>(h->launch_seq++ % zg::kCtrSlots); }
@@ -264,7 +272,7 @@ int rs_bucket(zero_handle* h, uint64_t a0, uint64_t b0, const void* const* grads
     a.base = a0;
     a.count = L;
     a.bucket_index = h->rs_calls;
-    const bool vec8 = (a0 % 8) == 0 && (L % 8) == 0;
+    const bool vec8 = bucket_vec8(h, a0, L);
     if (qbits) {
         const cudaError_t e = zg::launch_q(spec ? zg::QKind::kRsQSpec : zg::QKind::kRsQWs, h->dtype, qbits,
                                            pick_vec(vec8, a), a, static_cast<cudaStream_t>(stream));
@@ -624,7 +632,7 @@ int zero_reduce_scatter_gather_bucket(zero_handle_t h, uint64_t a0, uint64_t b0,
                     return fail(h, ZERO_EINVAL, "out[r] overlaps a gradient row of the reduce-scattered bucket");
         }
     }
-    const bool fuse = L > 0 && GL > 0 && (a0 % 8) == 0 && (L % 8) == 0 && (ga % 8) == 0 && (GL % 8) == 0;
+    const bool fuse = L > 0 && GL > 0 && bucket_vec8(h, a0, L) && (ga % 8) == 0 && (GL % 8) == 0;
     void* outs[1] = {shard16};
     if (fuse) return rs_bucket(h, a0, b0, grads, master, m, v, outs, hyper, stream, 0, nullptr, ga, GL, out);
     // one part empty, or not 8-wide: the two calls one after the other
