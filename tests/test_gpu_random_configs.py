@@ -74,3 +74,170 @@ def test_random_configuration_matches_oracle(seed):
     st.check()
     if "max_norm" not in c["hyper_kw"]:
         assert st.mismatches == 0, (c, st)
+
+
+def _quantize_rows(rows, L, dt, bits):
+    import torch
+    from zero_partitioned_mixed_gb300 import _binding as B
+    nb = (L + 255) // 256
+    codes, scales = [], []
+    for src in rows:
+        c = torch.zeros(max(16, (L + 15) // 16 * 16), dtype=torch.uint8, device="cuda")
+        s = torch.zeros(max(2, 2 * nb), dtype=torch.float32, device="cuda")
+        B.zero_quantize_blocks(B.ZERO_BF16 if dt == "bf16" else B.ZERO_FP16, bits, src, L, c, s)
+        codes.append(c)
+        scales.append(s)
+    return codes, scales
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_zeropp_step_matches_oracle(seed):
+    # ZeRO-3 steps whose reduce-scatter takes the ranks' quantized gradients,
+    # at random shapes, bucket layouts, code widths and modes, with overflow
+    import torch
+
+    import oracle as O
+    from _parity import bits16, bits32
+    from zero_partitioned_mixed_gb300 import _binding as B
+    from zero_partitioned_mixed_gb300 import synth as S
+    from zero_partitioned_mixed_gb300.buffers import RankBuffers
+    rng = np.random.default_rng(1000 + seed)
+    n = int(rng.choice([1, 2, 3, 4, 5, 8]))
+    align = int(rng.choice([1, 2, 8]))
+    psi = int(rng.integers(1, 40_000))
+    dt = str(rng.choice(["fp16", "bf16"]))
+    bits = int(rng.choice([8, 4]))
+    db = bool(rng.integers(0, 2))
+    part = O.partition(psi, n, align)
+    P = part.psi_pad
+    buckets = _buckets(rng, P, int(rng.choice([1, 8])))
+    buf = RankBuffers(psi, n, 3, dt, align=align, double_buffer=db)
+    td = S.torch_dtype(dt)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    master = torch.randn(psi, generator=g, device="cuda") * 0.02
+    st = O.init_state(3, dt, part, master.cpu().numpy())
+    buf.state(0)[0].copy_(torch.from_numpy(st.master))
+    buf.params[:P].copy_(torch.from_numpy(st.params.view(np.int16)).view(td))
+    hb, ho = B.hyper(weight_decay=0.05), O.Hyper(weight_decay=0.05)
+    bad_step = int(rng.integers(0, 4))
+    for step in range(3):
+        grads = torch.zeros((n, max(8, (P + 7) // 8 * 8)), dtype=td, device="cuda")
+        grads[:, :psi] = (torch.randn((n, psi), generator=g, device="cuda") * 1e-2).to(td)
+        if step == bad_step:
+            grads[int(rng.integers(0, n)), int(rng.integers(0, psi))] = float("inf")
+        gb = bits16(grads)
+        for (a, b) in reversed(buckets):
+            L = b - a
+            rows = []
+            for r in range(n):
+                src = torch.zeros(max(8, (L + 7) // 8 * 8), dtype=td, device="cuda")
+                src[:L].copy_(grads[r, a:b])
+                rows.append(src[:L])
+            codes, scales = _quantize_rows(rows, L, dt, bits)
+            B.zero_reduce_scatter_bucket_q(buf.h, a, b, bits, codes, scales, buf.master, buf.m, buf.v,
+                                           buf.params, hb)
+        buf.step(hb)
+        st, res = O.step_stage3_quantized(st, [gb[:, a:b] for (a, b) in buckets], buckets, ho, bits)
+        s = buf.status()
+        assert bool(s["overflow"]) == res.overflow and s["steps_applied"] == st.t
+        if res.applied:
+            assert abs(s["grad_norm"] - res.norm) <= 1e-5 * res.norm
+        gm, gmm, gv = buf.state(s["state_slot"])
+        assert np.array_equal(bits32(gm), st.master.view(np.uint32))
+        assert np.array_equal(bits32(gmm), st.m.view(np.uint32))
+        assert np.array_equal(bits32(gv), st.v.view(np.uint32))
+        assert np.array_equal(bits16(buf.params[:P]), st.params)
+    buf.close()
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_random_shapes_write_nothing_outside_their_buffers(seed):
+    # every buffer a call touches sits between sentinel bands; random stages,
+    # shapes, modes (the staged one included), bucket layouts, fused or
+    # separate ZeRO-3 backward, ZeRO++ calls; two steps, one with an overflow
+    import torch
+
+    from test_gpu_guard_bands import Guarded
+    from zero_partitioned_mixed_gb300 import _binding as B
+    rng = np.random.default_rng(2000 + seed)
+    G = Guarded()
+    stage = int(rng.choice([0, 1, 2, 3]))
+    n = int(rng.choice([1, 2, 3, 4, 5, 8, 19]))
+    align = int(rng.choice([1, 2, 8]))
+    psi = int(rng.integers(1, 30_000))
+    db = stage != 0 and bool(rng.integers(0, 2))
+    dt, td = (B.ZERO_BF16, torch.bfloat16) if rng.integers(0, 2) else (B.ZERO_FP16, torch.float16)
+    h = B.zero_init_partition(psi, n, stage, dt, align, B.ZERO_F_DOUBLE_BUFFER if db else 0)
+    P = B.zero_partition_info(h)[0]
+    rows = n if stage == 0 else (2 if db else 1)
+    master, m, v = (G.tensor(rows * P, torch.float32) for _ in range(3))
+    master[:psi].normal_(0, 0.02)
+    hyp_kw = {"max_norm": 1e-3} if rng.integers(0, 3) == 0 else {}
+    try:
+        for step in range(2):
+            inf_at = int(rng.integers(0, psi)) if step == 1 else -1
+            if stage in (0, 1, 2) and not (stage == 2 and rng.integers(0, 2)):
+                # stage 0 keeps g_hat in the workspace: AUTO or the workspace two-pass mode
+                modes = [0, 1] if stage == 0 else (
+                    [0, 1, 2] + ([3] if db else []) + ([4] if db and P % 8 == 0 and n <= 19 else []))
+                mode = int(rng.choice(modes))
+                grads = [G.tensor(P, td) for _ in range(n)]
+                params = [G.tensor(P, td) for _ in range(n)]
+                for gr in grads:
+                    gr[:psi].copy_(torch.randn(psi, device="cuda").mul_(1e-2))
+                if inf_at >= 0:
+                    grads[0][inf_at] = float("inf")
+                B.zero_step(h, grads, params, master, m, v, B.hyper(mode=mode, **hyp_kw))
+            elif stage == 2:
+                params = [G.tensor(P, td) for _ in range(n)]
+                for (a, b) in reversed(_buckets(rng, P, int(rng.choice([1, 8])))):
+                    L = b - a
+                    gr = [G.tensor(L, td) for _ in range(n)]
+                    for t in gr:
+                        t.copy_(torch.randn(L, device="cuda").mul_(1e-2))
+                    if a <= inf_at < b:
+                        gr[0][inf_at - a] = float("inf")
+                    B.zero_reduce_scatter_bucket_replicas(h, a, b, gr, master, m, v, params, B.hyper(**hyp_kw))
+                B.zero_step(h, None, params, master, m, v, B.hyper(**hyp_kw))
+            else:
+                shard = G.tensor(P, td)
+                back = list(reversed(_buckets(rng, P, int(rng.choice([1, 8])))))
+                fused = bool(rng.integers(0, 2))
+                quant = int(rng.choice([0, 0, 8, 4]))
+                out0 = [G.tensor(back[0][1] - back[0][0], td) for _ in range(n)]
+                B.zero_gather_bucket(h, back[0][0], back[0][1], shard, out0)
+                for k, (a, b) in enumerate(back):
+                    L = b - a
+                    gr = [G.tensor(L, td) for _ in range(n)]
+                    for t in gr:
+                        t.copy_(torch.randn(L, device="cuda").mul_(1e-2))
+                    if a <= inf_at < b:
+                        gr[0][inf_at - a] = float("inf")
+                    nxt = back[k + 1] if k + 1 < len(back) else None
+                    if quant:
+                        nb = (L + 255) // 256
+                        codes = [G.tensor(L if quant == 8 else (L + 1) // 2, torch.uint8) for _ in range(n)]
+                        scales = [G.tensor(2 * nb, torch.float32) for _ in range(n)]
+                        for r in range(n):
+                            B.zero_quantize_blocks(dt, quant, gr[r], L, codes[r], scales[r])
+                        B.zero_reduce_scatter_bucket_q(h, a, b, quant, codes, scales, master, m, v, shard,
+                                                       B.hyper(**hyp_kw))
+                        if nxt:
+                            qc = [G.tensor(nxt[1] - nxt[0], torch.uint8) for _ in range(n)]
+                            qs = [G.tensor(2 * ((nxt[1] - nxt[0] + 255) // 256), torch.float32) for _ in range(n)]
+                            B.zero_gather_bucket_q8(h, nxt[0], nxt[1], shard, qc, qs)
+                    elif fused and nxt:
+                        outs = [G.tensor(nxt[1] - nxt[0], td) for _ in range(n)]
+                        B.zero_reduce_scatter_gather_bucket(h, a, b, gr, master, m, v, shard, B.hyper(**hyp_kw),
+                                                            nxt[0], nxt[1], outs)
+                    else:
+                        B.zero_reduce_scatter_bucket(h, a, b, gr, master, m, v, shard, B.hyper(**hyp_kw))
+                        if nxt:
+                            outs = [G.tensor(nxt[1] - nxt[0], td) for _ in range(n)]
+                            B.zero_gather_bucket(h, nxt[0], nxt[1], shard, outs)
+                B.zero_step(h, None, [shard], master, m, v, B.hyper(**hyp_kw))
+        torch.cuda.synchronize()
+        G.check()
+    finally:
+        B.zero_destroy(h)
