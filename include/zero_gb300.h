@@ -403,7 +403,10 @@ ZERO_API int zero_bytes_moved(zero_handle_t h, zero_bytes_t* out);
  *   process exits.  psi_pad above ZERO_NOALLOC_MAX_PSI_PAD is rejected
  *   with ZERO_EINVAL.
  *   The first call on a device looks up that array's device address
- *   (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   (cudaGetSymbolAddress) and, like any first launch of a kernel, may have
+ *   the driver load the library's kernels onto the device; make that first
+ *   call before any stream capture.  Later calls leave the device's free
+ *   memory unchanged.
  *   Every call shares the one array and overwrites what the last call left
  *   there (it clears the status word first): calls that overlap on the GPU,
  *   from any thread or stream, race and give wrong results.  Order them.
