@@ -196,3 +196,62 @@ def test_quantized_calls_reject_bad_arguments():
     with pytest.raises(B.ZeroError):
         B.zero_gather_bucket_q8(buf.h, 0, 8, buf.params, [x, x], [x, x])
     buf.close()
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_zeropp_step_at_scale(bits):
+    # psi = 2^24 + 13 over 8 ranks in 4 buckets: the quantized gather's
+    # launches reach its full chunk count and the reduce-scatter a full
+    # grid; every code, scale, state element and shard element is compared
+    psi, n, dt = (1 << 24) + 13, 8, "bf16"
+    part = O.partition(psi, n, 8)
+    P = part.psi_pad
+    cut = P // 4 // 8 * 8
+    buckets = [(0, cut), (cut, 2 * cut), (2 * cut, 3 * cut + 5), (3 * cut + 5, P)]
+    buf = RankBuffers(psi, n, 3, dt, double_buffer=True)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(31 + bits)
+    master = torch.randn(psi, generator=g, device="cuda") * 0.02
+    st = O.init_state(3, dt, part, master.cpu().numpy())
+    buf.state(0)[0].copy_(torch.from_numpy(st.master))
+    buf.params[:P].copy_(torch.from_numpy(st.params.view(np.int16)).view(torch.bfloat16))
+    hb, ho = B.hyper(weight_decay=0.1), O.Hyper(weight_decay=0.1)
+    # the forward gather of every bucket, INT8, against the oracle's
+    shard_bits = bits16(buf.params[:P])
+    for (a, b) in buckets:
+        L = b - a
+        codes = [_codes_buf(L, 8) for _ in range(n)]
+        scales = [torch.zeros(2 * _nb(L), dtype=torch.float32, device="cuda") for _ in range(n)]
+        B.zero_gather_bucket_q8(buf.h, a, b, buf.params, codes, scales)
+        outs, _ = O.quantized_gather(shard_bits, a, b, dt, n)
+        for r in (0, n - 1):
+            c, s, l = outs[r]
+            assert np.array_equal(codes[r].cpu().numpy()[:L], c)
+            sc = scales[r].cpu().numpy()
+            assert np.array_equal(sc[0::2].view(np.uint32), s.view(np.uint32))
+            assert np.array_equal(sc[1::2].view(np.uint32), l.view(np.uint32))
+    # one step whose reduce-scatter takes the ranks' quantized gradients
+    grads = torch.zeros((n, buf.stride), dtype=torch.bfloat16, device="cuda")
+    grads[:, :psi] = (torch.randn((n, psi), generator=g, device="cuda") * 1e-2).to(torch.bfloat16)
+    gb = bits16(grads)
+    for (a, b) in reversed(buckets):
+        L = b - a
+        codes, scales = [], []
+        for r in range(n):
+            src = torch.zeros(max(8, (L + 7) // 8 * 8), dtype=torch.bfloat16, device="cuda")
+            src[:L].copy_(grads[r, a:b])
+            c, s = _quantize_gpu(src[:L], dt, bits)
+            codes.append(c)
+            scales.append(s)
+        B.zero_reduce_scatter_bucket_q(buf.h, a, b, bits, codes, scales, buf.master, buf.m, buf.v, buf.params, hb)
+    buf.step(hb)
+    st, res = O.step_stage3_quantized(st, [gb[:, a:b] for (a, b) in buckets], buckets, ho, bits)
+    s = buf.status()
+    assert not s["overflow"] and not res.overflow and s["steps_applied"] == 1
+    assert abs(s["grad_norm"] - res.norm) <= 1e-5 * res.norm
+    gm, gmm, gv = buf.state(s["state_slot"])
+    assert np.array_equal(bits32(gm), st.master.view(np.uint32))
+    assert np.array_equal(bits32(gmm), st.m.view(np.uint32))
+    assert np.array_equal(bits32(gv), st.v.view(np.uint32))
+    assert np.array_equal(bits16(buf.params[:P]), st.params)
+    buf.close()
