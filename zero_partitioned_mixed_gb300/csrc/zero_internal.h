@@ -33,7 +33,8 @@ constexpr int kCtrSlots = 64;       // launches of one handle that may be in fli
 // Measured per kernel: the stage 1/2 step does best with UMAX 16 and TARGET
 // 16384 (long chunks for large launches, many for mid-sized ones), the
 // two-pass kernels with TARGET 16384, the reduce-scatter into replicas with
-// 8192, the gather and the reduce-scatter into the shard with the default.
+// 8192, the gather with the default, the reduce-scatter into the shard with
+// the default (4096 at N <= 2).
 // Any (UMAX, TARGET) keeps the partials deterministic.
 constexpr uint64_t kMinChunks = 2048;        // the default TARGET
 constexpr uint64_t kMaxChunkTarget = 16384;  // the largest TARGET of a kernel that writes chunk partials

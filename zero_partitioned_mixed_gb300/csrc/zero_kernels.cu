@@ -44,8 +44,9 @@ constexpr int kStepChunkU = 16;
 constexpr uint64_t kStepChunks = 16384;
 constexpr uint64_t kTwoPassChunks = 16384;
 constexpr uint64_t kRsReplicaChunks = 8192;
+constexpr uint64_t kRsSmallNChunks = 4096;
 static_assert(kStepChunks <= kMaxChunkTarget && kTwoPassChunks <= kMaxChunkTarget &&
-                  kRsReplicaChunks <= kMaxChunkTarget,
+                  kRsReplicaChunks <= kMaxChunkTarget && kRsSmallNChunks <= kMaxChunkTarget,
               "the workspace holds the partials of at most 2 * kMaxChunkTarget chunks");
 // The step's target is kStepChunks from N = 8 up.  With N <= 4 an iteration
 // moves few bytes, the chunk bookkeeping weighs more, and the default target
@@ -504,6 +505,15 @@ __global__ void __launch_bounds__(kThreads) k_gather(const __grid_constant__ Arg
 // bytes and longer chunks pay (16 measured 1.5-2 % faster at N = 2 and 4);
 // from N = 8 up kChunkU measured better (shorter tail on 5e7-element buckets).
 __host__ __device__ inline int rs_chunk_cap(int n_ranks) { return n_ranks <= 4 ? 16 : kChunkU; }
+// Chunk target of the reduce-scatter: kRsReplicaChunks into the replicas;
+// into the shard or the workspace, kRsSmallNChunks for N <= 2 and the
+// default above.  At N = 2 a chunk of the default target lasts about 60 us
+// on 5e7-element buckets, and the launch's last chunks leave SMs idle; at
+// 4096 the stage-3 step at psi = 2^29 took 3.636 against 3.676 ms (6144:
+// 3.647, 8192: 3.719), and at N = 4 it was slower (4.639 against 4.617 ms).
+__host__ __device__ inline uint64_t rs_chunk_target(int n_ranks, bool to_replicas) {
+    return to_replicas ? kRsReplicaChunks : (n_ranks <= kSmallN ? kRsSmallNChunks : kMinChunks);
+}
 
 // MINB as for the step: 4 CTAs per SM for N <= 2 (psi = 2^29, N = 2,
 // 5e7-element buckets: 2.73 against 2.77 ms per step's reduce-scatters;
@@ -527,7 +537,7 @@ __global__ void __launch_bounds__(kThreads, MINB) k_rs(const __grid_constant__ A
     const uint64_t dst = static_cast<uint64_t>(pro.live ^ 1) * a.slot_stride;
     const uint64_t nvec = a.count / W;
     const int umax = rs_chunk_cap(a.n_ranks);
-    const uint64_t target = TO_REPLICAS ? kRsReplicaChunks : kMinChunks;
+    const uint64_t target = rs_chunk_target(a.n_ranks, TO_REPLICAS);
     const uint64_t clen = chunk_len(nvec, umax, target), nchunks = chunk_total(nvec, umax, target);
     const int U = chunk_u(nvec, umax, target);
     // the gather's chunks follow the reduce-scatter's (none unless GATHER);
@@ -675,19 +685,19 @@ cudaError_t launch_dw(Kind kind, const Args& a, cudaStream_t s, int* grid_out) {
         case Kind::kRsSpec:
             return a.n_ranks <= kSmallN
                        ? run_chunked_u(k_rs<DT, IO, true, false, 4, false>, a, nvec, rs_chunk_cap(a.n_ranks),
-                                       kMinChunks, s, grid_out)
+                                       rs_chunk_target(a.n_ranks, false), s, grid_out)
                        : run_chunked_u(k_rs<DT, IO, true, false, 3, false>, a, nvec, rs_chunk_cap(a.n_ranks),
-                                       kMinChunks, s, grid_out);
-        case Kind::kRsSpecReplicas: return run_chunked_u(k_rs<DT, IO, true, true, 3, false>, a, nvec, rs_chunk_cap(a.n_ranks), kRsReplicaChunks, s,
+                                       rs_chunk_target(a.n_ranks, false), s, grid_out);
+        case Kind::kRsSpecReplicas: return run_chunked_u(k_rs<DT, IO, true, true, 3, false>, a, nvec, rs_chunk_cap(a.n_ranks), rs_chunk_target(a.n_ranks, true), s,
                                                             grid_out);
-        case Kind::kRsWs: return run_chunked_u(k_rs<DT, IO, false, false, 3, false>, a, nvec, rs_chunk_cap(a.n_ranks), kMinChunks, s, grid_out);
+        case Kind::kRsWs: return run_chunked_u(k_rs<DT, IO, false, false, 3, false>, a, nvec, rs_chunk_cap(a.n_ranks), rs_chunk_target(a.n_ranks, false), s, grid_out);
         case Kind::kRsSpecGather:
         case Kind::kRsWsGather:
             if constexpr (IO::W != 8) {
                 return cudaErrorInvalidValue;
             } else {
                 // one CTA per chunk at most, over both parts of the launch
-                const uint64_t n = chunk_total(nvec, rs_chunk_cap(a.n_ranks), kMinChunks) + chunk_total(a.gcount / 8);
+                const uint64_t n = chunk_total(nvec, rs_chunk_cap(a.n_ranks), rs_chunk_target(a.n_ranks, false)) + chunk_total(a.gcount / 8);
                 if (kind == Kind::kRsWsGather) return run(k_rs<DT, IO, false, false, 3, true>, a, n * kThreads, s, grid_out);
                 return a.n_ranks <= kSmallN ? run(k_rs<DT, IO, true, false, 4, true>, a, n * kThreads, s, grid_out)
                                             : run(k_rs<DT, IO, true, false, 3, true>, a, n * kThreads, s, grid_out);
