@@ -52,6 +52,14 @@ __device__ __forceinline__ float warp_qmax(float a) {
 
 constexpr float kTwo23 = 8388608.0f;
 
+// 1/x from the hardware's approximate reciprocal (1 ulp); used only by the
+// screen in codes8, whose margin allows 2^-22 relative.
+__device__ __forceinline__ float rcp_approx(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
 // Two fp32 lanes in one 64-bit register for the packed add/sub/mul.rn.f32x2
 // of sm_100 and later: each half is an ordinary fp32 operation rounded once,
 // so results are those of the scalar instructions, at half the issue cost.
@@ -86,47 +94,65 @@ __device__ __forceinline__ f2 f2mul(f2 a, f2 b) {
 }
 
 // A lane's codes rint(clamp(q, 0, top)) for q = (x - lo) / scale rounded once
-// (IEEE division), elements k < nv; a NaN q gives 0 (fmaxf returns the other
-// operand); 0 throughout when scale is 0.
+// (IEEE division), a NaN q giving 0 (fmaxf returns the other operand), as
+// the words tb[k] = bits of 2^23 + code: the code is tb[k] & 0x1FF, and its
+// low byte for INT8.  Only elements k < nv are meaningful; finish_codes
+// forms the codes (0 for absent elements and when scale is 0).
 //
-// The division is taken only where it can matter.  With rcp = 1/scale
-// rounded once, u = d * rcp (d = x - lo) differs from the exact d / scale by
-// a factor (1 + e1)(1 + e2), |e1|, |e2| <= 2^-24, and the rounded quotient
-// from it by at most 2^-24 relative: the two lie within u * 2^-22 < 2^-14 of
-// each other (u <= top < 256).  rint(clamp(.)) is constant between
-// consecutive half-integers, so they give the same code unless u lies
-// within 2^-14 of a half-integer.  u + 2^23 rounds u to the integer the code
-// is read from, and u - ((u + 2^23) - 2^23) is then u's exact distance r to
-// it; the lane divides all its elements again when some |r| >= 0.5 - 2^-12
-// (a margin of 4): for values spread over the levels that is one lane in
-// about 500.  fast is false for a block whose scale is not a normal number
-// in [2^-100, 2^100] (the bound assumes no underflow or overflow), and then
-// every element is divided.
-__device__ __forceinline__ void codes8(const float (&x)[8], int nv, float lo, float scale, float rcp, bool fast,
-                                       float top, uint32_t (&q)[8]) {
+// The division is taken only where it can matter.  Let d = x - lo (rounded
+// once) and rcp = 1/scale to within 2^-22 relative (the hardware's
+// approximate reciprocal, which the PTX ISA documents to 1 ulp, 2^-23).  The
+// exact product p = d * rcp lies within 2^-22 p of d / scale, its rounding u
+// within 2^-24 u of p, and the rounded quotient Q within 2^-24 Q of
+// d / scale; with d / scale < 256, Q lies within 2^-14 + 2^-15 < 2^-13 of
+// u.  The code is read from u + 2^23 (for 0 <= u < 2^22 its low mantissa
+// bits hold k = rint(u); k = rint(p) should the compiler fuse the multiply
+// into the add, which changes nothing below), and r = u - ((u + 2^23) -
+// 2^23) = u - k is exact.  When |r| < 0.5 - 2^-12, |Q - k| < 0.5 - 2^-12 +
+// 2^-13 < 0.5, so k = rint(Q): the code.  Otherwise the lane divides all its
+// elements again: for values spread over the levels that is one lane in
+// about 250.
+//
+// No clamp is needed on the screened path.  It runs only for a block of
+// finite values whose scale is a normal number in [2^-100, 2^100] (`fast`;
+// the bounds above assume no underflow or overflow), and there every
+// present x >= lo, so 0 <= d <= hi - lo and 0 <= Q, u < top + 2^-12: k lies
+// in [0, top], and rint(clamp(Q)) = rint(Q) (Q > top only by less than 0.5).
+// Absent elements (index >= nv: copies of a present one, or 0 in a lane
+// with none) may only add a division: their codes are forced to 0, and a
+// NaN r of theirs drops out of the fmaxf.  A
+// block that is not fast (NaN, infinite, zero or extreme range) divides
+// every element with the clamp.
+__device__ __forceinline__ void codes8(const float (&x)[8], float lo, float scale, float rcp, bool fast, float top,
+                                       uint32_t (&tb)[8]) {
     float t[8];
-    bool near = !fast;
+    float rmax = 0.0f;
     // pairs of elements in packed operations (each half one IEEE-rounded
-    // fp32 operation; no multiply feeds an add, so nothing is contracted)
+    // fp32 operation)
     const f2 lo2 = f2pack(lo, lo), rcp2 = f2pack(rcp, rcp), two23 = f2pack(kTwo23, kTwo23);
 #pragma unroll
     for (int k = 0; k < 8; k += 2) {
-        float q0, q1, r0, r1;
-        f2unpack(f2mul(f2sub(f2pack(x[k], x[k + 1]), lo2), rcp2), q0, q1);
-        const f2 u = f2pack(fminf(fmaxf(q0, 0.0f), top), fminf(fmaxf(q1, 0.0f), top));
+        float r0, r1;
+        const f2 u = f2mul(f2sub(f2pack(x[k], x[k + 1]), lo2), rcp2);
         const f2 tt = f2add(u, two23);
         f2unpack(f2sub(u, f2sub(tt, two23)), r0, r1);
         f2unpack(tt, t[k], t[k + 1]);
-        // 0.5 - 2^-12
-        near |= (k < nv && !(fabsf(r0) < 0x1.ffcp-2f)) || (k + 1 < nv && !(fabsf(r1) < 0x1.ffcp-2f));
+        rmax = fmaxf(rmax, fmaxf(fabsf(r0), fabsf(r1)));
     }
-    if (near) {
+    // 0.5 - 2^-12
+    if (!fast || !(rmax < 0x1.ffcp-2f)) {
 #pragma unroll
         for (int k = 0; k < 8; ++k)
             t[k] = __fadd_rn(fminf(fmaxf(__fdiv_rn(__fsub_rn(x[k], lo), scale), 0.0f), top), kTwo23);
     }
 #pragma unroll
-    for (int k = 0; k < 8; ++k) q[k] = (k < nv && scale != 0.0f) ? (__float_as_uint(t[k]) & 0x1FFu) : 0u;
+    for (int k = 0; k < 8; ++k) tb[k] = __float_as_uint(t[k]);
+}
+
+// The codes of a lane from codes8's words.
+__device__ __forceinline__ void finish_codes(const uint32_t (&tb)[8], int nv, float scale, uint32_t (&q)[8]) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) q[k] = (k < nv && scale != 0.0f) ? (tb[k] & 0x1FFu) : 0u;
 }
 
 // float(q) for q < 2^23, exactly.
@@ -148,27 +174,33 @@ __device__ __forceinline__ int load_lane8(const void* src, uint64_t e0, uint64_t
 #pragma unroll
         for (int k = 0; k < 8; ++k) x[k] = widen<DT>(raw[k]);
     } else {
+        // absent elements repeat the lane's first one (0 in a lane with none),
+        // so that they change no min or max
+        const unsigned short* s = reinterpret_cast<const unsigned short*>(src);
+        const float x0 = nv > 0 ? widen<DT>(s[e0]) : 0.0f;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            x[k] = 0.0f;
-            if (k < nv) x[k] = widen<DT>(reinterpret_cast<const unsigned short*>(src)[e0 + k]);
-        }
+        for (int k = 0; k < 8; ++k) x[k] = (k < nv) ? widen<DT>(s[e0 + k]) : x0;
     }
     return nv;
 }
 
-// Block min/max over the warp; every lane gets {scale, lo}, the rounded
-// reciprocal of the scale and whether code_of may screen with it.
+// Block min/max over the warp; every lane gets {scale, lo}, the
+// approximate reciprocal of the scale and whether codes8 may screen with it.
 template <int BITS>
 __device__ __forceinline__ void block_scale(const float (&x)[8], int nv, float& scale, float& lo, float& rcp,
                                             bool& fast) {
-    float mn = __int_as_float(0x7F800000), mx = -__int_as_float(0x7F800000);
+    // absent elements repeat a present one (load_lane8); a lane with none
+    // contributes the identities
+    float mn = x[0], mx = x[0];
 #pragma unroll
-    for (int k = 0; k < 8; ++k)
-        if (k < nv) {
-            mn = qmin(mn, x[k]);
-            mx = qmax(mx, x[k]);
-        }
+    for (int k = 1; k < 8; ++k) {
+        mn = qmin(mn, x[k]);
+        mx = qmax(mx, x[k]);
+    }
+    if (nv == 0) {
+        mn = __int_as_float(0x7F800000);
+        mx = -__int_as_float(0x7F800000);
+    }
     // warp-wide, then +0.0 makes a zero bound +0 whatever the order of ties
     mn = __fadd_rn(warp_qmin(mn), 0.0f);
     mx = __fadd_rn(warp_qmax(mx), 0.0f);
@@ -177,10 +209,11 @@ __device__ __forceinline__ void block_scale(const float (&x)[8], int nv, float& 
     const float top = static_cast<float>((1 << BITS) - 1);
     scale = __fdiv_rn(range, top);
     fast = scale >= 0x1p-100f && scale <= 0x1p100f;
-    rcp = fast ? __frcp_rn(scale) : 0.0f;
+    rcp = fast ? rcp_approx(scale) : 0.0f;
 }
 
-// Eight byte codes (each < 256) packed little-endian into 8 bytes.
+// The low bytes of eight words (codes, or codes8's words for INT8) packed
+// little-endian into 8 bytes.
 __device__ __forceinline__ uint2 pack_u8x8(const uint32_t (&q)[8]) {
     uint2 w;
     w.x = __byte_perm(__byte_perm(q[0], q[1], 0x0040u), __byte_perm(q[2], q[3], 0x0040u), 0x5410u);
@@ -301,7 +334,8 @@ constexpr int kQUnrollGather = 2;
 constexpr int kQUnrollQuant = 4;
 
 // Quantize U consecutive blocks starting at block blk0 of src (count
-// elements) and hand each block's codes and {scale, lo} to `emit`.
+// elements) and hand each block's lane words (codes8) and {scale, lo} to
+// `emit`.
 template <int DT, int BITS, int kQUnroll, class Emit>
 __device__ __forceinline__ void quantize_blocks_u(const unsigned short* src, uint64_t count, uint64_t blk0,
                                                   uint64_t nb, bool vec, int lane, Emit&& emit) {
@@ -319,9 +353,9 @@ __device__ __forceinline__ void quantize_blocks_u(const unsigned short* src, uin
         float scale, lo, rcp;
         bool fast;
         block_scale<BITS>(x[u], nv[u], scale, lo, rcp, fast);
-        uint32_t q[8];
-        codes8(x[u], nv[u], lo, scale, rcp, fast, top, q);
-        emit(blk0 + u, (blk0 + u) * kQBlock + static_cast<uint64_t>(lane) * 8, nv[u], q, scale, lo);
+        uint32_t tb[8];
+        codes8(x[u], lo, scale, rcp, fast, top, tb);
+        emit(blk0 + u, (blk0 + u) * kQBlock + static_cast<uint64_t>(lane) * 8, nv[u], tb, scale, lo);
     }
 }
 
@@ -335,8 +369,10 @@ __global__ void __launch_bounds__(kThreads) k_quantize(const __grid_constant__ A
     const unsigned short* src = static_cast<const unsigned short*>(a.grads[0]) + a.base;
     for (uint64_t blk0 = warp_id() * kQUnrollQuant; blk0 < nb; blk0 += warp_count() * kQUnrollQuant) {
         quantize_blocks_u<DT, BITS, kQUnrollQuant>(src, a.count, blk0, nb, a.qvec != 0, lane,
-                                    [&](uint64_t blk, uint64_t e0, int nv, const uint32_t (&q)[8], float scale,
+                                    [&](uint64_t blk, uint64_t e0, int nv, const uint32_t (&tb)[8], float scale,
                                         float lo) {
+                                        uint32_t q[8];
+                                        finish_codes(tb, nv, scale, q);
                                         if (nv > 0) store_codes<BITS>(a.params[0], e0, nv, q);
                                         if (lane == 0)
                                             *reinterpret_cast<float2*>(a.qdst[0] + 2 * blk) = make_float2(scale, lo);
@@ -374,14 +410,18 @@ __global__ void __launch_bounds__(kThreads, 6) k_gather_q8(const __grid_constant
         const uint64_t blk0 = (c * U + u) * kPerIter + static_cast<uint64_t>(warp) * kQUnrollGather;
         if (blk0 >= nb) break;
         quantize_blocks_u<DT, 8, kQUnrollGather>(src, a.count, blk0, nb, a.qvec != 0, lane,
-                                 [&](uint64_t blk, uint64_t e0, int nv, const uint32_t (&q)[8], float scale,
+                                 [&](uint64_t blk, uint64_t e0, int nv, const uint32_t (&tb)[8], float scale,
                                      float lo) {
-                                     // the same 8 bytes to every rank, packed once
+                                     // the same 8 bytes to every rank, packed once, straight
+                                     // from the words' low bytes (all 0 when scale is 0)
                                      if (nv == 8) {
-                                         const uint2 w = pack_u8x8(q);
+                                         uint2 w = pack_u8x8(tb);
+                                         if (scale == 0.0f) w = make_uint2(0u, 0u);
                                          for (int r = 0; r < a.n_ranks; ++r)
                                              __stcs(reinterpret_cast<uint2*>(static_cast<unsigned char*>(a.params[r]) + e0), w);
                                      } else if (nv > 0) {
+                                         uint32_t q[8];
+                                         finish_codes(tb, nv, scale, q);
                                          for (int r = 0; r < a.n_ranks; ++r) store_codes<8>(a.params[r], e0, nv, q);
                                      }
                                      // lane r writes rank r's {scale, lo}
