@@ -107,6 +107,45 @@ def test_quantizer_divides_by_the_scale(dtype, bits):
     assert np.array_equal(sc[0::2].view(np.uint32), scale.view(np.uint32))
 
 
+def _same_floats(got, want):
+    # bit-equal, or NaN on both sides (a NaN's payload is not part of the format)
+    g, w = np.asarray(got, np.float32), np.asarray(want, np.float32)
+    both_nan = np.isnan(g) & np.isnan(w)
+    return bool(np.all(both_nan | (g.view(np.uint32) == w.view(np.uint32))))
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("bits", [8, 4])
+def test_quantizer_special_blocks(dtype, bits):
+    # blocks that the kernels leave to the clamped division (a NaN, +-inf, a
+    # range that overflows, a scale below 2^-100 from bf16 subnormals) and
+    # blocks at the edges of the screened path (constant +-0, fp16
+    # subnormals), each beside ordinary ones, in a buffer with a ragged end
+    rng = np.random.default_rng(5 + bits)
+    base = lambda: rng.normal(0, 1, 256).astype(np.float32)
+    blocks = [base()]
+    b = base(); b[17] = np.nan; blocks.append(b)
+    b = base(); b[3] = np.inf; blocks.append(b)
+    b = base(); b[200] = -np.inf; blocks.append(b)
+    big = np.float32(60000.0 if dtype == "fp16" else 3.0e38)
+    b = base(); b[0] = big; b[1] = -big; blocks.append(b)
+    tiny = np.float32(2.0 ** -24 if dtype == "fp16" else 2.0 ** -133)
+    blocks.append((rng.integers(0, 4, 256) * tiny).astype(np.float32))
+    blocks.append(np.zeros(256, np.float32))
+    b = np.zeros(256, np.float32); b[::2] = -0.0; blocks.append(b)
+    blocks.append(base()[:77])
+    xb = O.rne16(np.concatenate(blocks), dtype)
+    count = xb.size
+    dev = torch.zeros(max(8, (count + 7) // 8 * 8), dtype=S.torch_dtype(dtype), device="cuda")
+    dev[:count].copy_(torch.from_numpy(xb.view(np.int16)).view(S.torch_dtype(dtype)))
+    codes, scales = _quantize_gpu(dev[:count], dtype, bits)
+    with np.errstate(over="ignore"):            # hi - lo overflows in one block
+        packed, scale, lo = _oracle_codes(xb, dtype, bits)
+    assert np.array_equal(codes.cpu().numpy()[:packed.size], packed)
+    sc = scales.cpu().numpy()[:2 * _nb(count)]
+    assert _same_floats(sc[0::2], scale) and _same_floats(sc[1::2], lo)
+
+
 @pytest.mark.parametrize("a,b", [(0, 70_000), (1024, 1032), (13, 5_013), (256, 257)])
 def test_quantized_gather_matches_oracle(a, b):
     psi, n, dt = 80_000, 4, "bf16"

@@ -315,14 +315,18 @@ __device__ __forceinline__ uint32_t load_code1(const void* codes, uint64_t e) {
 __device__ __forceinline__ uint64_t warp_id() { return (static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; }
 __device__ __forceinline__ uint64_t warp_count() { return (static_cast<uint64_t>(gridDim.x) * blockDim.x) >> 5; }
 
-// Warp-iterations per chunk for the block-quantizing kernels: as few as
-// leave a launch about kQChunks chunks, at most 4.  The quantized gather
-// measured best with the finest chunks (no partials to commit): at
-// ψ = 2^29, N = 8, 2e8-element buckets, a step's gathers took 1.4 % less
-// than with 2048 chunks per launch.
-constexpr uint64_t kQChunks = 32768;
-__host__ __device__ inline int q_chunk_u(uint64_t iters) {
-    const uint64_t u = iters / kQChunks;
+// Warp-iterations per chunk for the quantized gather: as few as leave a
+// launch about q_chunk_target(N) chunks, at most 4.  With N = 8 the finest
+// chunks measured best (no partials to commit): at ψ = 2^29, 2e8-element
+// buckets, a step's gathers took 1.4 % less than with 2048 chunks per
+// launch, and the step 1.1 % less than with 8192.  With few ranks a chunk
+// writes few bytes and its closing barrier weighs more: at N = 2 the same
+// step took 3.61 ms with 8192 chunks per launch (4 iterations each) against
+// 3.69 ms with 32768, and at N = 4 the step's gathers 1.297 against 1.312 ms.
+constexpr int kQSmallN = 4;
+__host__ __device__ inline uint64_t q_chunk_target(int n_ranks) { return n_ranks <= kQSmallN ? 8192 : 32768; }
+__host__ __device__ inline int q_chunk_u(uint64_t iters, int n_ranks) {
+    const uint64_t u = iters / q_chunk_target(n_ranks);
     return u >= 4 ? 4 : (u < 1 ? 1 : static_cast<int>(u));
 }
 
@@ -398,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 6) k_gather_q8(const __grid_constant
     // would be too coarse here, so the chunk length counts warp-iterations
     constexpr uint64_t kPerIter = static_cast<uint64_t>(kThreads / 32) * kQUnrollGather;
     const uint64_t iters = (nb + kPerIter - 1) / kPerIter;
-    const int U = q_chunk_u(iters);
+    const int U = q_chunk_u(iters, a.n_ranks);
     const uint64_t nchunks = (iters + U - 1) / U;
     ChunkCtr* ctr = a.ws.ctrs + a.ctr_slot;
     Chunks ch(ctr, s_c, nchunks);
@@ -522,11 +526,14 @@ __device__ __forceinline__ void reduce_group_q(const Args& a, uint64_t j, const 
 
 // ZeRO-3 reduce-scatter of bucket [base, base+count) from the N ranks'
 // quantized gradients (qgZ): as k_rs, with the ranks' values dequantized.
-// Static grid-stride: with only 24 resident warps per SM this kernel waits
-// on its loads, and chunked scheduling's block barriers cost more (+6 % for
-// int8) than the balance gains.
+// Static grid-stride: this kernel waits on its loads, and chunked
+// scheduling's block barriers cost more (+6 % for int8, measured at 3 CTAs
+// per SM) than the balance gains.  4 CTAs per SM (64 registers, a short
+// spill): against 3, the int4 form's reduce-scatters took 3.9 % less, and
+// the int8 form's (since its codes stay raw words until used) 4.9 / 4.2 /
+// 0.7 % less at N = 2 / 4 / 8 (ψ = 2^29).
 template <int DT, class IO, int BITS, bool SPEC>
-__global__ void __launch_bounds__(kThreads, BITS == 4 ? 4 : 3) k_rs_q(const __grid_constant__ Args a) {
+__global__ void __launch_bounds__(kThreads, 4) k_rs_q(const __grid_constant__ Args a) {
     pdl_enter();
     constexpr int W = IO::W;
     __shared__ Pro pro;
@@ -593,7 +600,7 @@ cudaError_t launch_db(QKind kind, Vec vec, const Args& a, cudaStream_t s) {
             // one CTA per chunk at most (run() sizes the grid from threads)
             const uint64_t per_iter = static_cast<uint64_t>(kThreads / 32) * kQUnrollGather;
             const uint64_t iters = (nb + per_iter - 1) / per_iter;
-            const uint64_t nch = (iters + q_chunk_u(iters) - 1) / q_chunk_u(iters);
+            const uint64_t nch = (iters + q_chunk_u(iters, a.n_ranks) - 1) / q_chunk_u(iters, a.n_ranks);
             return run(k_gather_q8<DT>, a, nch * kThreads, s, nullptr);
         }
         case QKind::kDequantize: return run(k_dequantize<DT, BITS>, a, (a.count + 7) / 8, s, nullptr);
