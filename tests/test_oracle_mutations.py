@@ -47,6 +47,7 @@ PIN_RUNS = [
     (pins.test_norm_accumulates_in_double, dict(stage=2)),
     (pins.test_clip_scales_gradient_to_max_norm, {}),
     (pins.test_norm_sums_each_shard_left_to_right, dict(stage=1)),
+    (pins.test_norm_squares_beyond_fp32_range, dict(stage=1, x=2.0 ** 100)),
     (pins.test_replicas_equal_cast_of_master, {}),
     (pins.test_quantizer_is_lossless_on_its_grid, {}),
     (pins.test_quantizer_error_bound_and_order, {}),

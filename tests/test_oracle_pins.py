@@ -463,6 +463,21 @@ def test_norm_accumulates_in_double(stage):
 
 
 @pytest.mark.parametrize("stage", [1, 3])
+@pytest.mark.parametrize("x", [2.0 ** 100, 2.0 ** -130])
+def test_norm_squares_beyond_fp32_range(stage, x):
+    # One rank, bf16 g_hat = [x, x, x, x]: the squares 2^200 and 2^-260 lie
+    # outside fp32 (overflow, underflow) but are exact in fp64, so the norm
+    # is exactly 2x.
+    part = O.partition(4, 1, 1)
+    g = O.rne16(np.full((1, 4), x, np.float32), O.BF16)
+    assert np.array_equal(O.widen16(g, O.BF16), np.full((1, 4), x, np.float32))
+    st = O.init_state(stage, O.BF16, part, np.zeros(4, np.float32))
+    with np.errstate(over="ignore"):            # the fp32 g * g of the update is inf
+        _, res = O.step(st, g, O.Hyper(eps=1e-8), [(0, 4)] if stage == 3 else None)
+    assert res.norm == 2 * x
+
+
+@pytest.mark.parametrize("stage", [1, 3])
 def test_norm_sums_each_shard_left_to_right(stage):
     # Each owner adds its shard's squares in order, in fp64.  One rank,
     # bf16 g_hat = [1, 2^-27 x 16]: every square 2^-54 is below half an ulp
