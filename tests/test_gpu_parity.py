@@ -9,7 +9,7 @@ import numpy as np
 import pytest
 import torch
 
-from _parity import run_case
+from _parity import ULP16, ULP32, bits16, bits32, run_case, ulp16, ulp32
 
 pytestmark = pytest.mark.gpu
 
@@ -589,4 +589,58 @@ def test_cast_at_the_limits_of_the_16_bit_formats(dtype, stage):
     want = O.rne16(master, dtype)
     first = got[:psi] if stage == 3 else got[0, :psi]
     assert np.array_equal(first, want)
+    buf.close()
+
+
+@pytest.mark.parametrize("stage", [1, 3])
+@pytest.mark.parametrize("mag", [2.0 ** 70, 2.0 ** -75, "mixed"])
+def test_norm_of_gradients_whose_squares_leave_fp32(stage, mag):
+    # bf16 gradients reach magnitudes whose fp32 squares overflow (|g| >= 2^64)
+    # or fall below the normal range (|g| < 2^-63); the norm is defined in
+    # fp64, where every such square is exact.  With clipping on, the norm
+    # decides the clip factor and so the update.
+    import oracle as O
+    from zero_partitioned_mixed_gb300 import _binding as B
+    from zero_partitioned_mixed_gb300.buffers import RankBuffers
+    psi, n = 5003, 3
+    rng = np.random.default_rng(17 + stage)
+    part = O.partition(psi, n, 8)
+    P = part.psi_pad
+    master = (rng.normal(0, 0.02, psi)).astype(np.float32)
+    sign = np.where(rng.random((n, psi)) < 0.5, -1.0, 1.0)
+    g = sign * (1.0 + rng.random((n, psi)))
+    if mag == "mixed":
+        # squares near fp32's top (a group's sum overflows), below its
+        # normal range, and ordinary, side by side
+        g = g * rng.choice([2.0 ** 62, 2.0 ** -75, 1.0], size=(n, psi))
+    else:
+        g = g * mag
+    gbits = np.zeros((n, P), np.uint16)
+    gbits[:, :psi] = O.rne16(g.astype(np.float32), "bf16")
+    buf = RankBuffers(psi, n, stage, "bf16")
+    ost = O.init_state(stage, "bf16", part, master)
+    buf.master[:P].copy_(torch.from_numpy(ost.master))
+    dev = torch.from_numpy(gbits.view(np.int16)).cuda().view(torch.bfloat16)
+    hb, ho = B.hyper(max_norm=1.0), O.Hyper(max_norm=1.0)
+    if stage == 3:
+        buf.params[:P].copy_(torch.from_numpy(ost.params.view(np.int16)).view(torch.bfloat16))
+        buf.reduce_scatter(0, P, [dev[r] for r in range(n)], hb)
+        buf.step(hb)
+    else:
+        buf.params[:, :P].copy_(torch.from_numpy(ost.params.view(np.int16)).view(torch.bfloat16))
+        buf.grads[:, :P].copy_(dev)
+        buf.step(hb)
+    with np.errstate(over="ignore"):            # fp32 squares of the update may overflow
+        ost, res = O.step(ost, gbits, ho, [(0, P)] if stage == 3 else None)
+    s = buf.status()
+    assert res.applied and s["applied"] and not s["overflow"]
+    assert np.isfinite(res.norm) and res.norm > 0
+    assert abs(s["grad_norm"] - res.norm) <= 1e-5 * res.norm, (s["grad_norm"], res.norm)
+    want_clip = float(res.clip) if res.clip is not None else 1.0
+    assert s["clip_coef"] == want_clip
+    gm, gmm, gv = buf.state(s["state_slot"])
+    for got, want in ((gm, ost.master), (gmm, ost.m), (gv, ost.v)):
+        assert int(ulp32(bits32(got), want.view(np.uint32)).max()) <= ULP32
+    got16 = bits16(buf.params[:P]) if stage == 3 else bits16(buf.params[:, :P])
+    assert int(ulp16(got16, ost.params).max()) <= ULP16
     buf.close()

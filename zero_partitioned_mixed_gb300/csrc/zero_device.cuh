@@ -224,15 +224,21 @@ __device__ __forceinline__ void reduce_group(const Args& a, uint64_t j, const Pr
 
 // Squares of the real elements into the thread's fp64 accumulator: an
 // exact product (FMA error term) and a compensated fp32 sum per group, then
-// one fp64 add, so the result carries ~1e-14 relative error.
+// one fp64 add, so the result carries ~1e-14 relative error.  That holds
+// while every square and the group's sum lie in fp32's normal range.  A
+// group with an element of magnitude 2^60 or more (its sum may overflow),
+// or whose largest nonzero magnitude is below 2^-60 (its squares would be
+// subnormal or zero), is summed in fp64 instead, where the square of every
+// fp32 value is exact.  Non-finite elements only raise `bad`.
 template <int W>
 __device__ __forceinline__ void norm_group(const float (&g)[W], int valid, double& acc, int& bad) {
-    float hi = 0.0f, lo = 0.0f;
+    float hi = 0.0f, lo = 0.0f, amax = 0.0f;
 #pragma unroll
     for (int k = 0; k < W; ++k) {
         if (k < valid) {
             const float x = g[k];
             bad |= nonfinite(x) ? 1 : 0;
+            amax = fmaxf(amax, fabsf(x));
             const float p = __fmul_rn(x, x);
             const float e = __fmaf_rn(x, x, -p);
             const float s = __fadd_rn(hi, p);
@@ -242,7 +248,18 @@ __device__ __forceinline__ void norm_group(const float (&g)[W], int valid, doubl
             lo = __fadd_rn(lo, __fadd_rn(err, e));
         }
     }
-    acc = __dadd_rn(acc, __dadd_rn(static_cast<double>(hi), static_cast<double>(lo)));
+    if (!(amax < 0x1p60f) || (amax > 0.0f && amax < 0x1p-60f)) {
+        double q = 0.0;
+#pragma unroll
+        for (int k = 0; k < W; ++k)
+            if (k < valid) {
+                const double x = static_cast<double>(g[k]);
+                q = __dadd_rn(q, __dmul_rn(x, x));
+            }
+        acc = __dadd_rn(acc, q);
+    } else {
+        acc = __dadd_rn(acc, __dadd_rn(static_cast<double>(hi), static_cast<double>(lo)));
+    }
 }
 
 __device__ __forceinline__ int valid_count(uint64_t gi, int W, uint64_t psi) {
