@@ -294,3 +294,48 @@ def test_zeropp_step_at_scale(bits):
     assert np.array_equal(bits32(gv), st.v.view(np.uint32))
     assert np.array_equal(bits16(buf.params[:P]), st.params)
     buf.close()
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_quantized_reduce_scatter_extreme_scales(bits):
+    # bf16 gradient blocks whose scales lie above 2^100, in the subnormal
+    # range (bf16 subnormals), near 2^60 and ordinary, in one bucket of three
+    # ranks: the dequantized sums, the fp32 squares of the update (which
+    # overflow) and the norm (summed in fp64 there); every state element
+    # and the norm against the oracle
+    psi, n, dt = 256 * 12 + 77, 3, "bf16"
+    part = O.partition(psi, n, 8)
+    P = part.psi_pad
+    rng = np.random.default_rng(40 + bits)
+    mags = np.array([2.0 ** 110, 2.0 ** -130, 2.0 ** 60, 1.0, 2.0 ** 100, 2.0 ** -120,
+                     1e-3, 2.0 ** 110, 1.0, 2.0 ** -130, 1.0, 2.0 ** 50, 1.0])
+    g = rng.normal(0, 1, (n, psi)) * np.repeat(mags, 256)[:psi]
+    gbits = np.zeros((n, P), np.uint16)
+    gbits[:, :psi] = O.rne16(g.astype(np.float32), dt)
+    buf = RankBuffers(psi, n, 3, dt)
+    master = (rng.normal(0, 0.02, psi)).astype(np.float32)
+    st = O.init_state(3, dt, part, master)
+    buf.state(0)[0].copy_(torch.from_numpy(st.master))
+    buf.params[:P].copy_(torch.from_numpy(st.params.view(np.int16)).view(torch.bfloat16))
+    hb, ho = B.hyper(), O.Hyper()
+    dev = torch.from_numpy(gbits.view(np.int16)).cuda().view(torch.bfloat16)
+    codes, scales = [], []
+    for r in range(n):
+        c, s = _quantize_gpu(dev[r, :P], dt, bits)
+        codes.append(c)
+        scales.append(s)
+    assert float(scales[0][0].item()) > 2.0 ** 100
+    B.zero_reduce_scatter_bucket_q(buf.h, 0, P, bits, codes, scales, buf.master, buf.m, buf.v, buf.params, hb)
+    buf.step(hb)
+    with np.errstate(over="ignore", invalid="ignore"):
+        st, res = O.step_stage3_quantized(st, [gbits], [(0, P)], ho, bits)
+    s = buf.status()
+    assert bool(s["overflow"]) == res.overflow
+    if res.applied:
+        assert abs(s["grad_norm"] - res.norm) <= 1e-5 * res.norm
+    gm, gmm, gv = buf.state(s["state_slot"])
+    assert np.array_equal(bits32(gm), st.master.view(np.uint32))
+    assert np.array_equal(bits32(gmm), st.m.view(np.uint32))
+    assert np.array_equal(bits32(gv), st.v.view(np.uint32))
+    assert np.array_equal(bits16(buf.params[:P]), st.params)
+    buf.close()
