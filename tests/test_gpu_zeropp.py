@@ -146,12 +146,14 @@ def test_quantizer_special_blocks(dtype, bits):
     assert _same_floats(sc[0::2], scale) and _same_floats(sc[1::2], lo)
 
 
+@pytest.mark.parametrize("dt", ["bf16", "fp16"])
 @pytest.mark.parametrize("a,b", [(0, 70_000), (1024, 1032), (13, 5_013), (256, 257)])
-def test_quantized_gather_matches_oracle(a, b):
-    psi, n, dt = 80_000, 4, "bf16"
+def test_quantized_gather_matches_oracle(a, b, dt):
+    psi, n = 80_000, 4
     buf = RankBuffers(psi, n, 3, dt)
     P = buf.psi_pad
-    buf.params[:P].copy_((torch.randn(P, device="cuda") * 0.02).to(torch.bfloat16))
+    td = S.torch_dtype(dt)
+    buf.params[:P].copy_((torch.randn(P, device="cuda") * 0.02).to(td))
     L = b - a
     codes = [_codes_buf(L, 8) for _ in range(n)]
     scales = [torch.zeros(2 * _nb(L), dtype=torch.float32, device="cuda") for _ in range(n)]
@@ -162,8 +164,8 @@ def test_quantized_gather_matches_oracle(a, b):
         assert np.array_equal(codes[r].cpu().numpy()[:L], c)
         sc = scales[r].cpu().numpy()
         assert np.array_equal(sc[0::2], s) and np.array_equal(sc[1::2], l)
-        deq = torch.zeros(max(8, (L + 7) // 8 * 8), dtype=torch.bfloat16, device="cuda")
-        B.zero_dequantize_blocks(B.ZERO_BF16, 8, codes[r], scales[r], L, deq)
+        deq = torch.zeros(max(8, (L + 7) // 8 * 8), dtype=td, device="cuda")
+        B.zero_dequantize_blocks(ZDT[dt], 8, codes[r], scales[r], L, deq)
         assert np.array_equal(bits16(deq[:L]), view)
     assert buf.bytes_moved()["hbm_write_bytes"] == n * (L + 8 * _nb(L))
     buf.close()
